@@ -1,0 +1,281 @@
+"""Pins for the fp64 CPU oracle (no GPU).
+
+The oracle is trusted only because these checks tie it to facts outside
+itself. Nothing here re-types the oracle's formula; each check is one of:
+
+* a hand-worked example (``tests/golden/hand_example.json``, derived with
+  pencil from the pages' definition; cited inside the file);
+* a closed form of a special case (X a basis row: the sums collapse to one
+  entry of W plus s * A[k,:] B);
+* an independent library route (numpy fp64 matmul of the base product, and of
+  the "merge" mode X (W + s (A B)^T)^T that the icman.com.cn article's
+  section 2.1 says computes the same thing as per-sample branches);
+* invariants the method implies: id -1 rows are the base product, B = 0 gives
+  the base output, zero-padding the rank (alpha scaled to keep alpha/rank)
+  changes nothing (the vLLM tutorial's 性能注意事项 says mixed ranks get
+  aligned to the largest one), permuting tokens permutes rows, linearity in X;
+* strict mode (icman.com.cn article section 4.1): an unknown id is an error;
+* exhaustive brute force for the segment builder on every id vector of
+  length <= 5 over {-1, 0, 1, 2}: the output must be a permutation, sorted by
+  id, stable, with maximal segments.
+
+``test_planted_mistakes_are_caught`` builds mutated copies of the oracle's C
+source (a dropped term, a wrong sign, a transposed operand, an inverted scale,
+an unstable tie-break ...) and checks that every one fails at least one pin.
+"""
+import itertools
+import json
+import os
+import shutil
+import subprocess
+import tempfile
+
+import numpy as np
+import pytest
+
+import oracle
+import lora_inputs as L
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_example.json")
+
+
+def bits(a):
+    return L.f32_to_bf16_bits(np.asarray(a, np.float32))
+
+
+def val(b):
+    return L.bf16_bits_to_f32(b).astype(np.float64)
+
+
+def small_problem(seed, T=12, d_in=24, d_out=20, ranks=(3, 8, 5), std_ab=0.5):
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d_in), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.3)
+    ads = {}
+    for i, r in enumerate(ranks):
+        ad = L.make_adapter(seed, i, d_in, d_out, r, 2.0 * r + i, std=std_ab)
+        ads[i] = (ad.A, ad.B, ad.rank, ad.alpha)
+    ids = L.rng_for(seed, L.ROLE_IDS).integers(-1, len(ranks), size=T).astype(np.int32)
+    return X, W, ids, ads
+
+
+# ------------------------------------------------------------------ pins
+
+def pin_golden(lib):
+    g = json.load(open(GOLDEN))
+    X = bits(g["X"])
+    W = bits(g["W"])
+    ids = np.array(g["ids"], np.int32)
+    ads = {int(k): (bits(v["A"]), bits(v["B"]), v["rank"], v["alpha"])
+           for k, v in g["adapters"].items()}
+    # every fixture value is exact in bf16
+    assert np.array_equal(val(X), np.array(g["X"], np.float64))
+    Y = oracle.lora_linear(X, W, ids, ads, n_slots=2, lib=lib)
+    assert np.array_equal(Y, np.array(g["Y"], np.float64)), Y
+    seg = oracle.segments(ids, 2, lib=lib)
+    exp = g["segments"]
+    assert seg["order"].tolist() == exp["order"]
+    assert seg["n_base"] == exp["n_base"] and seg["num_seg"] == exp["num_seg"]
+    assert seg["seg_start"].tolist() == exp["seg_start"]
+    assert seg["seg_slot"].tolist() == exp["seg_slot"]
+
+
+def pin_basis_rows(lib):
+    """X = e_k: Y[t,n] = W[n,k] + s * sum_j A[k,j] B[j,n] (one term of each sum survives)."""
+    d_in, d_out, r = 7, 5, 3
+    _, W, _, _ = small_problem(11, d_in=d_in, d_out=d_out)
+    ad = L.make_adapter(11, 0, d_in, d_out, r, 6.0, std=0.5)
+    X = np.zeros((2 * d_in, d_in), np.float32)
+    ids = np.zeros(2 * d_in, np.int32)
+    for k in range(d_in):
+        X[k, k] = 1.0
+        X[d_in + k, k] = 1.0
+        ids[d_in + k] = -1
+    Y = oracle.lora_linear(bits(X), W, ids, {0: (ad.A, ad.B, r, ad.alpha)}, 1, lib=lib)
+    Wv, Av, Bv = val(W), val(ad.A), val(ad.B)
+    s = ad.alpha / r
+    for k in range(d_in):
+        for n in range(d_out):
+            lora_term = sum(Av[k, j] * Bv[j, n] for j in range(r))
+            assert abs(Y[k, n] - (Wv[n, k] + s * lora_term)) <= 1e-15 * (1 + abs(Y[k, n]))
+            assert Y[d_in + k, n] == Wv[n, k]
+
+
+def pin_base_rows_match_numpy(lib):
+    X, W, ids, ads = small_problem(1)
+    Y = oracle.lora_linear(X, W, ids, ads, 3, lib=lib)
+    ref = val(X) @ val(W).T
+    base = ids == -1
+    assert base.any()
+    np.testing.assert_allclose(Y[base], ref[base], rtol=1e-12, atol=1e-12)
+
+
+def pin_zero_B_is_base(lib):
+    X, W, ids, ads = small_problem(2)
+    zero = {k: (A, np.zeros_like(B), r, a) for k, (A, B, r, a) in ads.items()}
+    Y = oracle.lora_linear(X, W, ids, zero, 3, lib=lib)
+    Y_base = oracle.lora_linear(X, W, np.full_like(ids, -1), {}, 3, lib=lib)
+    assert np.array_equal(Y, Y_base)
+
+
+def pin_merge_mode(lib):
+    """Per-token branches equal the merged weight W + s (A B)^T applied with numpy."""
+    X, W, ids, ads = small_problem(3)
+    Y = oracle.lora_linear(X, W, ids, ads, 3, lib=lib)
+    Xv, Wv = val(X), val(W)
+    for t in range(X.shape[0]):
+        i = int(ids[t])
+        Wm = Wv.copy()
+        if i >= 0:
+            A, B, r, alpha = ads[i]
+            Wm = Wm + (alpha / r) * (val(A) @ val(B)).T
+        ref = Xv[t] @ Wm.T
+        np.testing.assert_allclose(Y[t], ref, rtol=1e-12, atol=1e-12)
+
+
+def pin_rank_padding(lib):
+    X, W, ids, ads = small_problem(4, ranks=(8, 8, 8))
+    padded = {}
+    for k, (A, B, r, a) in ads.items():
+        p = L.pad_adapter(L.Adapter(A, B, r, a), 64)
+        padded[k] = (p.A, p.B, p.rank, p.alpha)
+    Y = oracle.lora_linear(X, W, ids, ads, 3, lib=lib)
+    Yp = oracle.lora_linear(X, W, ids, padded, 3, lib=lib)
+    assert np.array_equal(Y, Yp)
+
+
+def pin_permutation(lib):
+    X, W, ids, ads = small_problem(5)
+    perm = L.rng_for(5, 99).permutation(X.shape[0])
+    Y = oracle.lora_linear(X, W, ids, ads, 3, lib=lib)
+    Yp = oracle.lora_linear(X[perm], W, ids[perm], ads, 3, lib=lib)
+    assert np.array_equal(Yp, Y[perm])
+
+
+def pin_linearity(lib):
+    X, W, ids, ads = small_problem(6)
+    g = L.rng_for(6, 98)
+    X1 = g.integers(-8, 9, size=X.shape).astype(np.float32)
+    X2 = g.integers(-8, 9, size=X.shape).astype(np.float32)   # X1 + X2 exact in bf16
+    Y1 = oracle.lora_linear(bits(X1), W, ids, ads, 3, lib=lib)
+    Y2 = oracle.lora_linear(bits(X2), W, ids, ads, 3, lib=lib)
+    Y12 = oracle.lora_linear(bits(X1 + X2), W, ids, ads, 3, lib=lib)
+    np.testing.assert_allclose(Y12, Y1 + Y2, rtol=1e-12, atol=1e-10)
+
+
+def pin_scale(lib):
+    """The branch scales with alpha and inversely with the rank the adapter is loaded with."""
+    X, W, ids, ads = small_problem(7)
+    ids = np.zeros_like(ids)
+    A, B, r, a = ads[0]
+    base = oracle.lora_linear(X, W, np.full_like(ids, -1), {}, 1, lib=lib)
+    d1 = oracle.lora_linear(X, W, ids, {0: (A, B, r, a)}, 1, lib=lib) - base
+    d2 = oracle.lora_linear(X, W, ids, {0: (A, B, r, 2 * a)}, 1, lib=lib) - base
+    np.testing.assert_allclose(d2, 2 * d1, rtol=1e-9, atol=1e-12)
+    # s = alpha / r: with alpha = r the branch is exactly (X A) B
+    d_unit = oracle.lora_linear(X, W, ids, {0: (A, B, r, float(r))}, 1, lib=lib) - base
+    np.testing.assert_allclose(d_unit, (val(X) @ val(A)) @ val(B), rtol=1e-9, atol=1e-10)
+
+
+def pin_strict_ids(lib):
+    X, W, ids, ads = small_problem(8)
+    bad = ids.copy()
+    bad[3] = 2                       # slot 2 is not loaded below
+    with pytest.raises(oracle.OracleError) as e:
+        oracle.lora_linear(X, W, bad, {0: ads[0], 1: ads[1]}, 3, lib=lib)
+    assert e.value.code == oracle.ERR_BAD_ADAPTER_ID
+    bad[3] = 3                       # out of range
+    with pytest.raises(oracle.OracleError):
+        oracle.lora_linear(X, W, bad, ads, 3, lib=lib)
+    with pytest.raises(oracle.OracleError):
+        oracle.segments(np.array([0, 5], np.int32), 3, lib=lib)
+    with pytest.raises(oracle.OracleError):
+        oracle.segments(np.array([0, -2], np.int32), 3, lib=lib)
+
+
+def check_segments_properties(ids, seg):
+    T = len(ids)
+    order = seg["order"]
+    assert sorted(order.tolist()) == list(range(T))                 # permutation
+    keys = ids[order]
+    assert all(keys[p] <= keys[p + 1] for p in range(T - 1))         # sorted by id
+    for p in range(T - 1):                                           # stable
+        if keys[p] == keys[p + 1]:
+            assert order[p] < order[p + 1]
+    nb = int(np.sum(ids == -1))
+    assert seg["n_base"] == nb
+    starts, slots = seg["seg_start"], seg["seg_slot"]
+    assert seg["num_seg"] == len(set(ids.tolist()) - {-1})
+    assert len(starts) == seg["num_seg"] + 1 and starts[-1] == T
+    if seg["num_seg"]:
+        assert starts[0] == nb
+    for s in range(seg["num_seg"]):                                  # maximal runs
+        a, b = starts[s], starts[s + 1]
+        assert b > a and np.all(keys[a:b] == slots[s])
+    assert np.all(np.diff(slots) > 0)
+
+
+def pin_segments_bruteforce(lib):
+    for T in range(0, 6):
+        for combo in itertools.product([-1, 0, 1, 2], repeat=T):
+            ids = np.array(combo, np.int32)
+            check_segments_properties(ids, oracle.segments(ids, 3, lib=lib))
+    g = L.rng_for(9, 97)
+    for _ in range(20):
+        ids = g.integers(-1, 50, size=int(g.integers(1, 3000))).astype(np.int32)
+        check_segments_properties(ids, oracle.segments(ids, 50, lib=lib))
+
+
+PINS = [pin_golden, pin_basis_rows, pin_base_rows_match_numpy, pin_zero_B_is_base,
+        pin_merge_mode, pin_rank_padding, pin_permutation, pin_linearity, pin_scale,
+        pin_strict_ids, pin_segments_bruteforce]
+
+
+@pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
+def test_pin(pin):
+    pin(oracle.load())
+
+
+# ------------------------------------------------------- planted mistakes
+
+MUTATIONS = {
+    "drop_base": ("Y[t * d_out + n] = base + s * delta;", "Y[t * d_out + n] = s * delta;"),
+    "drop_branch": ("Y[t * d_out + n] = base + s * delta;", "Y[t * d_out + n] = base;"),
+    "sign": ("Y[t * d_out + n] = base + s * delta;", "Y[t * d_out + n] = base - s * delta;"),
+    "no_scale": ("Y[t * d_out + n] = base + s * delta;", "Y[t * d_out + n] = base + delta;"),
+    "inverted_scale": ("s = alpha[i] / (double)r;", "s = (double)r / alpha[i];"),
+    "W_transposed": ("base += bf16_value(x[k]) * bf16_value(w[k]);",
+                     "base += bf16_value(x[k]) * bf16_value(W[k * d_out + n]);"),
+    "A_transposed": ("bf16_value(A[i][k * r + j])", "bf16_value(A[i][j * d_in + k])"),
+    "B_transposed": ("bf16_value(B[i][j * d_out + n])", "bf16_value(B[i][n * r + j])"),
+    "rank_off_by_one": ("for (int64_t j = 0; j < r; ++j) {", "for (int64_t j = 1; j < r; ++j) {"),
+    "unstable_ties": ("if (a->index != b->index) return a->index < b->index ? -1 : 1;",
+                      "if (a->index != b->index) return a->index < b->index ? 1 : -1;"),
+    "base_last": ("if (a->key != b->key) return a->key < b->key ? -1 : 1;",
+                  "if (a->key != b->key) return (uint32_t)a->key < (uint32_t)b->key ? -1 : 1;"),
+    "lenient_segment_ids": ("if (ids[t] < -1 || ids[t] >= n_slots) return ORACLE_ERR_BAD_ADAPTER_ID;",
+                            "if (ids[t] < -1) return ORACLE_ERR_BAD_ADAPTER_ID;"),
+}
+
+
+@pytest.mark.skipif(shutil.which("gcc") is None, reason="needs gcc")
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_planted_mistakes_are_caught(name):
+    src = open(oracle.SRC).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new)
+    with tempfile.TemporaryDirectory() as d:
+        c = os.path.join(d, "mut.c")
+        so = os.path.join(d, "libmut.so")
+        open(c, "w").write(mutated)
+        oracle.build(c, so)
+        lib = oracle.load(so)
+        failed = []
+        for pin in PINS:
+            try:
+                pin(lib)
+            except KeyboardInterrupt:
+                raise
+            except BaseException:  # noqa: BLE001  (pytest.raises failures are BaseException)
+                failed.append(pin.__name__)
+        assert failed, f"planted mistake {name!r} passed every pin"
