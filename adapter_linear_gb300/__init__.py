@@ -1,0 +1,260 @@
+"""Python binding of the GB300 multi-LoRA linear library (``include/lora_linear.h``).
+
+Argument marshalling only: every step of the layer runs in the CUDA kernels
+of ``liblora_linear.so``; torch tensors are used for device memory and
+streams. There is no CPU fall-back: if the library has not been built (see
+``adapter_linear_gb300.build``) every call raises ``LibraryMissing``.
+
+The functions keep the C names (``lora_pool_create``, ``lora_load_adapter``,
+``lora_linear`` ...); ``LoraPool`` wraps a handle for convenience.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "liblora_linear.so")
+
+LORA_OK = 0
+STATUS_NAMES = {
+    0: "LORA_OK", 1: "LORA_ERR_ARG", 2: "LORA_ERR_SHAPE", 3: "LORA_ERR_SLOT_RANGE",
+    4: "LORA_ERR_SLOT_OCCUPIED", 5: "LORA_ERR_SLOT_EMPTY", 6: "LORA_ERR_RANK",
+    7: "LORA_ERR_BAD_ADAPTER_ID", 8: "LORA_ERR_CUDA", 9: "LORA_ERR_OOM", 10: "LORA_ERR_TIMEOUT",
+    11: "LORA_ERR_UNSUPPORTED",
+}
+globals().update({v: k for k, v in STATUS_NAMES.items()})
+LORA_PATH_AUTO, LORA_PATH_DECODE, LORA_PATH_PREFILL = 0, 1, 2
+LORA_STATS_COUNT = 7
+STATS_FIELDS = ("loaded", "free_pages", "total_pages", "loads", "unloads", "calls", "bytes_held")
+
+# every symbol the header declares
+EXPORTS = (
+    "lora_pool_create", "lora_pool_destroy", "lora_pool_reserve", "lora_load_adapter",
+    "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
+    "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
+    "lora_status_string", "lora_abi_version",
+)
+
+
+class LibraryMissing(RuntimeError):
+    pass
+
+
+class LoraError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load (once) and type the C ABI. Raises LibraryMissing if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise LibraryMissing(
+            f"{path} is missing: build it with `python -m adapter_linear_gb300.build`")
+    lib = ctypes.CDLL(path)
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    sig = {
+        "lora_pool_create": [i32, i32, i32, i32, ctypes.POINTER(vp)],
+        "lora_pool_destroy": [vp],
+        "lora_pool_reserve": [vp, i32],
+        "lora_load_adapter": [vp, i32, vp, vp, i32, f32],
+        "lora_unload_adapter": [vp, i32],
+        "lora_linear": [vp, vp, vp, vp, i32, vp, vp],
+        "lora_linear_host": [vp, vp, vp, vp, i32, vp, vp],
+        "lora_base_linear": [vp, vp, vp, i32, vp, vp],
+        "lora_pool_check_errors": [vp],
+        "lora_build_segments": [vp, vp, i32, vp, vp, vp, vp, vp, vp],
+        "lora_pool_stats": [vp, vp],
+        "lora_pool_set_path": [vp, i32],
+        "lora_status_string": [i32],
+        "lora_abi_version": [],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = ctypes.c_int
+    lib.lora_status_string.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def _check(status: int, what: str):
+    if status != LORA_OK:
+        raise LoraError(status, what)
+
+
+def _ptr(t) -> Optional[int]:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+# ------------------------------------------------------ C-named thin wrappers
+
+def lora_pool_create(max_adapters: int, max_rank: int, d_in: int, d_out: int) -> int:
+    h = ctypes.c_void_p()
+    _check(load_library().lora_pool_create(max_adapters, max_rank, d_in, d_out, ctypes.byref(h)),
+           "lora_pool_create")
+    return h.value
+
+
+def lora_pool_destroy(pool: int) -> None:
+    _check(load_library().lora_pool_destroy(pool), "lora_pool_destroy")
+
+
+def lora_pool_reserve(pool: int, max_tokens: int) -> None:
+    _check(load_library().lora_pool_reserve(pool, max_tokens), "lora_pool_reserve")
+
+
+def lora_load_adapter(pool: int, slot: int, A, B, rank: int, alpha: float) -> int:
+    """A: bf16 d_in x rank, B: bf16 rank x d_out (contiguous; host or device). Returns status."""
+    return load_library().lora_load_adapter(pool, slot, _ptr(A), _ptr(B), rank, float(alpha))
+
+
+def lora_unload_adapter(pool: int, slot: int) -> int:
+    return load_library().lora_unload_adapter(pool, slot)
+
+
+def lora_linear(pool: int, X, W_base, ids, T: int, Y, stream=None) -> int:
+    return load_library().lora_linear(pool, _ptr(X), _ptr(W_base), _ptr(ids), T, _ptr(Y),
+                                      _stream(stream))
+
+
+def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream=None) -> int:
+    return load_library().lora_linear_host(pool, _ptr(X_host), _ptr(W_base), _ptr(ids_host), T,
+                                           _ptr(Y_host), _stream(stream))
+
+
+def lora_base_linear(pool: int, X, W_base, T: int, Y, stream=None) -> int:
+    return load_library().lora_base_linear(pool, _ptr(X), _ptr(W_base), T, _ptr(Y),
+                                           _stream(stream))
+
+
+def lora_pool_check_errors(pool: int) -> int:
+    return load_library().lora_pool_check_errors(pool)
+
+
+def lora_build_segments(pool: int, ids, T: int, order, n_base, num_seg, seg_start, seg_slot,
+                        stream=None) -> int:
+    return load_library().lora_build_segments(pool, _ptr(ids), T, _ptr(order), _ptr(n_base),
+                                              _ptr(num_seg), _ptr(seg_start), _ptr(seg_slot),
+                                              _stream(stream))
+
+
+def lora_pool_stats(pool: int) -> Dict[str, int]:
+    out = (ctypes.c_int64 * LORA_STATS_COUNT)()
+    _check(load_library().lora_pool_stats(pool, ctypes.cast(out, ctypes.c_void_p)),
+           "lora_pool_stats")
+    return dict(zip(STATS_FIELDS, list(out)))
+
+
+def lora_pool_set_path(pool: int, path: int) -> int:
+    return load_library().lora_pool_set_path(pool, path)
+
+
+def lora_status_string(status: int) -> str:
+    return load_library().lora_status_string(status).decode()
+
+
+def lora_abi_version() -> int:
+    return load_library().lora_abi_version()
+
+
+# --------------------------------------------------------------- convenience
+
+class LoraPool:
+    """Owns one pool handle; torch tensors in, torch tensors out."""
+
+    def __init__(self, max_adapters: int, max_rank: int, d_in: int, d_out: int):
+        self.max_adapters, self.max_rank, self.d_in, self.d_out = max_adapters, max_rank, d_in, d_out
+        self.handle = lora_pool_create(max_adapters, max_rank, d_in, d_out)
+
+    def close(self):
+        if self.handle:
+            lora_pool_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:  # noqa: BLE001
+            pass
+
+    def reserve(self, max_tokens: int):
+        lora_pool_reserve(self.handle, max_tokens)
+
+    def load_adapter(self, slot: int, A, B, rank: int, alpha: float):
+        A = A.contiguous()
+        B = B.contiguous()
+        _check(lora_load_adapter(self.handle, slot, A, B, rank, alpha), "lora_load_adapter")
+
+    def unload_adapter(self, slot: int):
+        _check(lora_unload_adapter(self.handle, slot), "lora_unload_adapter")
+
+    def set_path(self, path: int):
+        _check(lora_pool_set_path(self.handle, path), "lora_pool_set_path")
+
+    def linear(self, X, W, ids, Y=None, stream=None):
+        import torch
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=X.device)
+        _check(lora_linear(self.handle, X, W, ids, T, Y, stream), "lora_linear")
+        return Y
+
+    def linear_host(self, X_host, W, ids_host, Y_host, stream=None):
+        _check(lora_linear_host(self.handle, X_host, W, ids_host, X_host.shape[0], Y_host, stream),
+               "lora_linear_host")
+        return Y_host
+
+    def base_linear(self, X, W, Y=None, stream=None):
+        import torch
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=X.device)
+        _check(lora_base_linear(self.handle, X, W, T, Y, stream), "lora_base_linear")
+        return Y
+
+    def check_errors(self) -> int:
+        return lora_pool_check_errors(self.handle)
+
+    def build_segments(self, ids, stream=None):
+        import torch
+        T = ids.shape[0]
+        cap = min(T, self.max_adapters) + 1
+        dev = ids.device
+        order = torch.empty(max(T, 1), dtype=torch.int32, device=dev)
+        hdr = torch.zeros(2, dtype=torch.int32, device=dev)
+        seg_start = torch.zeros(cap, dtype=torch.int32, device=dev)
+        seg_slot = torch.zeros(cap, dtype=torch.int32, device=dev)
+        _check(lora_build_segments(self.handle, ids, T, order, hdr[0:1], hdr[1:2], seg_start,
+                                   seg_slot, stream), "lora_build_segments")
+        return order[:T], hdr, seg_start, seg_slot
+
+    def stats(self) -> Dict[str, int]:
+        return lora_pool_stats(self.handle)

@@ -1,0 +1,262 @@
+// gemm_decode.cu -- base product for decode batches (T <= 256) and the
+// finishing pass that adds the low-rank branch.
+//
+// At decode sizes the base GEMM is bound by reading W_base once from HBM, so
+// the layout is chosen to stream W at full bandwidth on every SM:
+//  * operands swapped: D[n, t] = sum_k W[n,k] X[t,k], so the long d_out side
+//    is the MMA's M (128 rows of W per tile) and the T tokens are its N
+//    (T rounded up to 16; rows past T read as zero from TMA);
+//  * stream-K: the (tile, 64-wide k-block) iteration space is cut into G equal
+//    contiguous ranges, one per CTA (G = number of SMs, or fewer for small
+//    problems), so every SM streams the same share of W. A range touches at
+//    most two tiles; each touched tile gets its own TMEM accumulator and is
+//    written as an fp32 partial sum [cta][0|1][T][128].
+//  * warp roles: warp 4 issues TMA loads (W tile 128x64, X tile T'x64, 128-byte
+//    swizzle) into a multi-stage ring; warp 5 issues tcgen05 MMAs
+//    (M=128, N=T', K=16) into TMEM; warps 0-3 read the accumulators back with
+//    tcgen05.ld (TMEM lane = output row n) and store the partials.
+// finish_decode_kernel then adds, per output element, the partials of the
+// CTAs that covered its tile in CTA order (deterministic), plus the low-rank
+// branch s_i V[t,:] B_i[:,n] (V already carries s_i) read from the
+// interleaved B pages (one 16-byte load = 8 rank rows of one column), and
+// rounds once to bf16 (round to nearest even).
+#include "device_common.cuh"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int kWTileBytes = 128 * 128;  // 128 rows x 64 bf16
+
+__host__ __device__ __forceinline__ int cta_start(int c, int U, int G)
+{
+    return (int)(((long long)c * U) / G);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       DecodePlan p, float *__restrict__ partials, int *err)
+{
+    extern __shared__ uint8_t dec_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dec_smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t x_bytes = (uint32_t)p.ntok * 128;
+    const uint32_t stage_bytes = kWTileBytes + x_bytes;
+    const int stages = p.stages;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
+    uint64_t *empty = full + stages;
+    uint64_t *acc_full = empty + stages;  // [2]
+    uint64_t *drain = acc_full + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
+    const int tile0 = u0 / p.KB;
+    const int nseg = (u1 > u0) ? (u1 - 1) / p.KB - tile0 + 1 : 0;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&acc_full[0], 1);
+        mbar_init(&acc_full[1], 1);
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmX);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t pol_w = policy_evict_first();  // W is read exactly once
+            int it = 0;
+            for (int u = u0; u < u1; ++u, ++it) {
+                const int s = it % stages;
+                if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err)) break;
+                const int tile = u / p.KB, kb = u - tile * p.KB;
+                uint8_t *ws = smem + (size_t)s * stage_bytes;
+                mbar_arrive_expect_tx(&full[s], stage_bytes);
+                tma_load_2d_hint(ws, &tmW, &full[s], kb * 64, tile * 128, pol_w);
+                tma_load_2d(ws + kWTileBytes, &tmX, &full[s], kb * 64, 0);
+            }
+            for (int i = 0; i < stages && i < it; ++i) {
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait(&full[j % stages], (uint32_t)(j / stages) & 1u, &dummy, err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, p.ntok);
+            int it = 0;
+            for (int u = u0; u < u1; ++u, ++it) {
+                const int s = it % stages;
+                if (!mbar_wait(&full[s], (uint32_t)(it / stages) & 1u, &abort_flag, err)) break;
+                tc_fence_after_sync();
+                const int tile = u / p.KB, kb = u - tile * p.KB;
+                const int seg = tile - tile0;
+                const uint32_t d = tmem + (uint32_t)(seg * p.ntok);
+                const uint32_t wa = smem_u32(smem + (size_t)s * stage_bytes);
+                const uint32_t xa = wa + kWTileBytes;
+                const bool first = (kb == 0) || (u == u0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16_ss(d, sdesc_k_sw128(wa + kk * 32), sdesc_k_sw128(xa + kk * 32), idesc,
+                                (first && kk == 0) ? 0u : 1u);
+                mma_commit(&empty[s]);
+                if (u == u1 - 1 || kb == p.KB - 1) mma_commit(&acc_full[seg]);
+            }
+            mma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        for (int seg = 0; seg < nseg; ++seg) {
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&acc_full[seg], 0, &abort_flag, err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            float *out = partials + (size_t)(c * 2 + seg) * p.T * 128 + warp * 32 + lane;
+            for (int col = 0; col < p.ntok; col += 16) {
+                uint32_t v[16];
+                tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(seg * p.ntok + col), v);
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    if (col + j < p.T) out[(size_t)(col + j) * 128] = __uint_as_float(v[j]);
+            }
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+constexpr int kFinishThreads = 256;  // one thread per output column
+constexpr int kFinishTokens = 4;     // tokens per CTA
+
+__global__ void __launch_bounds__(kFinishThreads)
+    finish_decode_kernel(DecodePlan p, const float *__restrict__ partials,
+                         const int32_t *__restrict__ ids, PoolDev pool, const float *__restrict__ V,
+                         int ldv, uint16_t *__restrict__ Y)
+{
+    const int n = blockIdx.x * kFinishThreads + threadIdx.x;
+    if (n >= pool.d_out) return;
+    const int tile = n >> 7, nl = n & 127;
+    const int kb_lo = tile * p.KB, kb_hi = kb_lo + p.KB;
+    // first CTA whose range contains kb_lo
+    int c_lo = (int)(((long long)kb_lo * p.G) / p.U);
+    while (c_lo > 0 && cta_start(c_lo, p.U, p.G) > kb_lo) --c_lo;
+    while (cta_start(c_lo + 1, p.U, p.G) <= kb_lo) ++c_lo;
+
+    const int t_begin = blockIdx.y * kFinishTokens;
+    const int t_end = min(p.T, t_begin + kFinishTokens);
+    for (int t = t_begin; t < t_end; ++t) {
+        float acc = 0.f;
+        for (int c = c_lo; c < p.G && cta_start(c, p.U, p.G) < kb_hi; ++c) {
+            const int seg = (cta_start(c, p.U, p.G) / p.KB == tile) ? 0 : 1;
+            acc += partials[((size_t)(c * 2 + seg) * p.T + t) * 128 + nl];
+        }
+        if (ids != nullptr) {
+            const int id = ids[t];
+            if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+                const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+                const int np = row[SLOT_NPAGES];
+                const float *vrow = V + (size_t)t * ldv;
+                for (int q = 0; q < np; ++q) {
+                    const int page = row[SLOT_PAGES + q];
+                    const uint4 b = ldg_nc_v4(pool.B_pages + ((size_t)page * pool.d_out + n) * kRankPage);
+                    const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
+                    const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
+                    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    acc = dot8_f32_bf16(vv, b, acc);
+                }
+            }
+        }
+        __nv_bfloat16 h = __float2bfloat16_rn(acc);
+        Y[(size_t)t * pool.d_out + n] = *reinterpret_cast<uint16_t *>(&h);
+    }
+}
+
+uint32_t pow2_cols(uint32_t n)
+{
+    uint32_t c = 32;
+    while (c < n) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms)
+{
+    DecodePlan p{};
+    p.T = T;
+    p.ntok = ((T + 15) / 16) * 16;
+    if (p.ntok < 16) p.ntok = 16;
+    p.KB = (d_in + 63) / 64;
+    p.n_tiles = (d_out + 127) / 128;
+    p.U = p.n_tiles * p.KB;
+    int G = num_sms;
+    if (G > p.U) G = p.U;
+    if (G < p.n_tiles) G = p.n_tiles;  // ranges never span more than two tiles
+    p.G = G;
+    const size_t stage_bytes = kWTileBytes + (size_t)p.ntok * 128;
+    int stages = (int)((200 * 1024) / stage_bytes);
+    if (stages > 8) stages = 8;
+    if (stages < 2) stages = 2;
+    p.stages = stages;
+    p.smem_bytes = 1024 + stages * stage_bytes + (2 * stages + 3) * 8 + 16;
+    p.tmem_cols = pow2_cols(2 * p.ntok);
+    return p;
+}
+
+size_t decode_partials_floats(const DecodePlan &p) { return (size_t)p.G * 2 * p.T * 128; }
+
+cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
+                               const DecodePlan &plan, int d_out, float *partials, int *err,
+                               cudaStream_t stream)
+{
+    (void)d_out;
+    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)plan.smem_bytes);
+    if (e != cudaSuccess) return e;
+    gemm_decode_kernel<<<plan.G, kThreads, plan.smem_bytes, stream>>>(tmW, tmX, plan, partials, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
+                                 const int32_t *ids, const PoolDev &pool, const float *V,
+                                 int ldv, uint16_t *Y, cudaStream_t stream)
+{
+    dim3 grid((pool.d_out + kFinishThreads - 1) / kFinishThreads,
+              (plan.T + kFinishTokens - 1) / kFinishTokens);
+    finish_decode_kernel<<<grid, kFinishThreads, 0, stream>>>(plan, partials, ids, pool, V, ldv, Y);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,264 @@
+// gemm_prefill.cu -- base product with the low-rank expand fused into the
+// epilogue, for prefill-sized batches (compute bound: a 16384 x 14336 x 4096
+// GEMM is ~2 TFLOP).
+//
+// Persistent kernel, one CTA per SM, output tiles of 128 tokens x 256 columns
+// walked in a grouped order (16 token-tiles share one sweep over the columns,
+// so their X rows stay in L2 while W streams).
+//  * warp 8: TMA producer. Per 64-wide k-block it loads X[128 x 64] and
+//    W[256 x 64] (128-byte swizzle) into a 4-stage ring (48 KB per stage).
+//  * warp 9: MMA issuer. tcgen05.mma M=128 N=256 K=16, four per k-block, into
+//    one of two TMEM accumulators (2 x 256 columns = all 512), so the
+//    epilogue of tile i overlaps the MMAs of tile i+1.
+//  * warps 0-7: epilogue. Warp w reads TMEM lanes 32*(w%4).. (its 32 token
+//    rows) and columns 128*(w/4).. in chunks of 32 with tcgen05.ld; for a row
+//    whose token has an adapter it adds sum_j V[t,j] B_i[j,n] (V carries s_i;
+//    B pages are interleaved so one 16-byte load gives 8 rank rows of one
+//    column, and rows of the same adapter hit the same addresses), rounds
+//    once to bf16 and stores Y. Y is written exactly once.
+#include "device_common.cuh"
+
+namespace lora {
+
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kXTileBytes = kBM * kBK * 2;   // 16 KB
+constexpr int kWTileBytes = kBN * kBK * 2;   // 32 KB
+constexpr int kStageBytes = kXTileBytes + kWTileBytes;
+constexpr int kStages = 4;
+constexpr int kGroupM = 16;
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 512;
+
+struct PrefillArgs {
+    int T, d_in, d_out;
+    int KB, tiles_m, tiles_n, num_tiles;
+    const int32_t *ids;
+    const float *V;
+    int ldv;
+    uint16_t *Y;
+    int *err;
+};
+
+__device__ __forceinline__ void tile_coords(int tile, const PrefillArgs &a, int &m, int &n)
+{
+    const int per_group = kGroupM * a.tiles_n;
+    const int g = tile / per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(kGroupM, a.tiles_m - first_m);
+    const int local = tile - g * per_group;
+    m = first_m + local % gm;
+    n = local / gm;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                        PrefillArgs a, PoolDev pool)
+{
+    extern __shared__ uint8_t pre_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(pre_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kStages * kStageBytes);
+    uint64_t *empty = full + kStages;
+    uint64_t *acc_full = empty + kStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;    // [2]
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(tmem_slot, kTmemCols);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_map(&tmX);
+        tma_prefetch_map(&tmW);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
+                int m, n;
+                tile_coords(tile, a, m, n);
+                for (int kb = 0; kb < a.KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    ok = mbar_wait(&empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &abort_flag, a.err);
+                    if (!ok) break;
+                    uint8_t *xs = smem + (size_t)s * kStageBytes;
+                    mbar_arrive_expect_tx(&full[s], kStageBytes);
+                    tma_load_2d(xs, &tmX, &full[s], kb * kBK, m * kBM);
+                    tma_load_2d(xs + kXTileBytes, &tmW, &full[s], kb * kBK, n * kBN);
+                }
+            }
+            for (int i = 0; i < kStages && i < it; ++i) {
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait(&full[j % kStages], (uint32_t)(j / kStages) & 1u, &dummy, a.err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, kBN);
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x, ++tc) {
+                const int buf = tc & 1;
+                ok = mbar_wait(&acc_empty[buf], ((uint32_t)(tc >> 1) & 1u) ^ 1u, &abort_flag, a.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                for (int kb = 0; kb < a.KB; ++kb, ++it) {
+                    const int s = it % kStages;
+                    ok = mbar_wait(&full[s], (uint32_t)(it / kStages) & 1u, &abort_flag, a.err);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t xa = smem_u32(smem + (size_t)s * kStageBytes);
+                    const uint32_t wa = xa + kXTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32), idesc,
+                                    (kb | kk) != 0);
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(&acc_full[buf]);
+            }
+            mma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, a.err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int quarter = warp & 3, half = warp >> 2;
+        int tc = 0;
+        for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++tc) {
+            int m, n;
+            tile_coords(tile, a, m, n);
+            const int buf = tc & 1;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(tc >> 1) & 1u, &abort_flag, a.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+
+            const int t = m * kBM + quarter * 32 + lane;
+            const bool row_ok = t < a.T;
+            int np = 0;
+            const int32_t *pages = nullptr;
+            const float *vrow = nullptr;
+            if (row_ok && a.ids != nullptr) {
+                const int id = a.ids[t];
+                if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+                    const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+                    np = row[SLOT_NPAGES];
+                    pages = row + SLOT_PAGES;
+                    vrow = a.V + (size_t)t * a.ldv;
+                }
+            }
+            uint16_t *yrow = a.Y + (size_t)t * a.d_out;
+#pragma unroll 1
+            for (int ch = 0; ch < 4; ++ch) {
+                const int col0 = half * 128 + ch * 32;
+                const int ncol = n * kBN + col0;
+                uint32_t r[32];
+                tmem_ld32_wait(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBN + col0), r);
+                float acc[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+                for (int q = 0; q < np; ++q) {
+                    const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
+                    const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
+                    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (ncol + j < a.d_out) {
+                            const uint4 b = ldg_nc_v4(bp + j * kRankPage);
+                            acc[j] = dot8_f32_bf16(vv, b, acc[j]);
+                        }
+                    }
+                }
+                if (row_ok) {
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        if (ncol + j < a.d_out) {
+                            uint4 o;
+                            o.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+                            o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+                            o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+                            o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+                            *reinterpret_cast<uint4 *>(yrow + ncol + j) = o;
+                        }
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, int T,
+                                const int32_t *ids, const PoolDev &pool, const float *V, int ldv,
+                                uint16_t *Y, int num_sms, int *err, cudaStream_t stream)
+{
+    PrefillArgs a{};
+    a.T = T;
+    a.d_in = pool.d_in;
+    a.d_out = pool.d_out;
+    a.KB = (pool.d_in + kBK - 1) / kBK;
+    a.tiles_m = (T + kBM - 1) / kBM;
+    a.tiles_n = (pool.d_out + kBN - 1) / kBN;
+    a.num_tiles = a.tiles_m * a.tiles_n;
+    a.ids = ids;
+    a.V = V;
+    a.ldv = ldv;
+    a.Y = Y;
+    a.err = err;
+    if (a.num_tiles == 0) return cudaSuccess;
+    const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16;
+    cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
+    gemm_prefill_kernel<<<grid, kThreads, smem, stream>>>(tmX, tmW, a, pool);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,104 @@
+// internal.h -- constants, device-table layouts and kernel launchers shared by
+// the translation units of the library (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace lora {
+
+// ---------------------------------------------------------------- pool layout
+// Page = 8 rank rows of one adapter.
+//   A arena: bf16 [num_pages][8][d_in]   (page q of adapter i holds columns
+//            8q..8q+7 of A_i, transposed: row jj = A_i[:, 8q+jj]).
+//   B arena: bf16 [num_pages][d_out][8]  (page q holds rows 8q..8q+7 of B_i,
+//            interleaved: element [n][jj] = B_i[8q+jj, n]).
+// Rank rows beyond an adapter's rank inside its last page are zero. Page 0 is
+// an all-zero page that pads MMA operands to a multiple of 16 rank rows.
+constexpr int kRankPage = 8;
+
+// Slot table: int32 [max_adapters][slot_stride]
+constexpr int SLOT_RANK = 0;    // rank (0 = empty slot)
+constexpr int SLOT_NPAGES = 1;  // ceil(rank / 8)
+constexpr int SLOT_SCALE = 2;   // alpha / rank as fp32 bits
+constexpr int SLOT_PAGES = 4;   // page ids, npages entries
+
+// Segment-table header (int32 [4])
+constexpr int HDR_NBASE = 0;    // tokens with id -1 (and invalid ids)
+constexpr int HDR_NUMSEG = 1;   // segments (distinct loaded ids present)
+constexpr int HDR_UNITS = 2;    // sum over segments of ceil(len / kShrinkRows)
+
+constexpr int kShrinkRows = 128;       // token rows per tensor-core shrink unit
+constexpr int kDecodeMaxT = 256;       // largest batch of the decode path
+
+// Device error word bits.
+constexpr int kErrBadIdBit = 1;
+constexpr int kErrTimeoutBit = 2;
+
+// Every mbarrier wait gives up after this long (then flags kErrTimeoutBit).
+constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
+
+struct SegTables {
+    int32_t *order;      // [T]
+    int32_t *hdr;        // [4]
+    int32_t *seg_start;  // [max_seg + 1]
+    int32_t *seg_slot;   // [max_seg]
+    int32_t *seg_ublk;   // [max_seg + 1]  prefix of ceil(len / kShrinkRows)
+};
+
+struct PoolDev {
+    const uint16_t *A_pages;  // bf16 bits
+    const uint16_t *B_pages;
+    const int32_t *slots;
+    int slot_stride;
+    int max_adapters;
+    int max_pages;            // pages per adapter at max_rank
+    int d_in, d_out;
+};
+
+// ------------------------------------------------------------------ launchers
+
+size_t seg_build_smem_bytes(int max_adapters);
+cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
+                             int *err, cudaStream_t stream);
+
+// Decode shrink (CUDA cores): V[t, 8q+jj] = s_i * X[t,:] . A_i[:, 8q+jj]
+cudaError_t launch_shrink_simt(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs,
+                               float *V, int ldv, cudaStream_t stream);
+
+// Prefill shrink (tcgen05): same result, 128-token units per segment.
+cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
+                             int T, const PoolDev &pool, SegTables tabs, float *V, int ldv,
+                             int num_sms, int *err, cudaStream_t stream);
+
+struct DecodePlan {
+    int T, ntok, KB, n_tiles, U, G, stages;
+    size_t smem_bytes;
+    uint32_t tmem_cols;
+};
+DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms);
+size_t decode_partials_floats(const DecodePlan &p);
+cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
+                               const DecodePlan &plan, int d_out, float *partials, int *err,
+                               cudaStream_t stream);
+// Y = bf16(sum of split-K partials + s_i V[t] B_i); ids == nullptr: no branch.
+cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
+                                 const int32_t *ids, const PoolDev &pool, const float *V,
+                                 int ldv, uint16_t *Y, cudaStream_t stream);
+
+cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, int T,
+                                const int32_t *ids, const PoolDev &pool, const float *V, int ldv,
+                                uint16_t *Y, int num_sms, int *err, cudaStream_t stream);
+
+// Pack a row-major A (d_in x rank) and B (rank x d_out) into pool pages.
+cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,
+                                int npages, const PoolDev &pool, uint16_t *A_pages,
+                                uint16_t *B_pages, cudaStream_t stream);
+
+// Host: build a 2-D bf16 TMA descriptor with 128-byte swizzle over a row-major
+// [rows x inner] tensor, box [box_rows x box_inner].
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace lora

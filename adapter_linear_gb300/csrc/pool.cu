@@ -1,0 +1,581 @@
+// pool.cu -- host runtime behind the C ABI: the paged adapter pool, the slot
+// table, scratch management and the kernel sequence of one lora_linear call.
+//
+// The pool follows the unified adapter memory pool of the vLLM tutorial
+// ("vLLM 的 Multi-LoRA 怎么实现", item 1) and the LoRA-Land blog's hot-plug API
+// (核心实现解析 / 3: load_adapter moves A,B to the GPU and indexes them;
+// unload_adapter releases them). Pages hold 8 rank rows; the arenas are
+// allocated once at creation, so load and unload only move pages between a
+// free list and the slot table and never allocate.
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/lora_linear.h"
+#include "device_common.cuh"
+
+using namespace lora;
+
+struct TmapEntry {
+    const void *base = nullptr;
+    uint64_t inner = 0, rows = 0;
+    uint32_t box_inner = 0, box_rows = 0;
+    CUtensorMap map;
+};
+
+struct lora_pool {
+    int device = 0, num_sms = 0;
+    int max_adapters = 0, max_rank = 0, d_in = 0, d_out = 0;
+    int max_pages = 0;   // pages per adapter at max_rank
+    int num_pages = 0;   // arena pages, page 0 = zero page
+    int slot_stride = 0;
+    int ldv = 0;         // fp32 row stride of the low-rank intermediate
+    uint16_t *A_pages = nullptr, *B_pages = nullptr;
+    int32_t *d_slots = nullptr;
+    std::vector<int32_t> h_slots;
+    std::vector<int32_t> free_pages;  // stack; back() is taken first
+    int *d_err = nullptr;
+    uint16_t *stage_A = nullptr, *stage_B = nullptr;
+    int32_t *d_page_list = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    CUtensorMap tmA;  // A arena [num_pages*8 rows x d_in], box 8 x 64
+
+    // per-call scratch, sized for cap_T tokens
+    int cap_T = 0;
+    int32_t *order = nullptr, *hdr = nullptr, *seg_start = nullptr, *seg_slot = nullptr,
+            *seg_ublk = nullptr;
+    float *V = nullptr;
+    float *partials = nullptr;
+    size_t partials_floats = 0;
+    // device staging of lora_linear_host
+    int cap_host_T = 0;
+    uint16_t *hx = nullptr, *hy = nullptr;
+    int32_t *hids = nullptr;
+
+    TmapEntry tmaps[6];
+    int tmap_next = 0;
+
+    int path = LORA_PATH_AUTO;
+    int64_t n_loads = 0, n_unloads = 0, n_calls = 0;
+    size_t bytes_held = 0;
+};
+
+namespace {
+
+#define CUDA_TRY(expr)                                  \
+    do {                                                \
+        cudaError_t e_ = (expr);                        \
+        if (e_ != cudaSuccess) return LORA_ERR_CUDA;    \
+    } while (0)
+
+lora_status alloc_dev(lora_pool *p, void **ptr, size_t bytes)
+{
+    if (bytes == 0) bytes = 16;
+    if (cudaMalloc(ptr, bytes) != cudaSuccess) {
+        cudaGetLastError();
+        *ptr = nullptr;
+        return LORA_ERR_OOM;
+    }
+    p->bytes_held += bytes;
+    return LORA_OK;
+}
+
+void free_dev(lora_pool *p, void *ptr, size_t bytes)
+{
+    if (ptr) {
+        cudaFree(ptr);
+        p->bytes_held -= bytes ? bytes : 16;
+    }
+}
+
+PoolDev pool_view(const lora_pool *p)
+{
+    PoolDev v;
+    v.A_pages = p->A_pages;
+    v.B_pages = p->B_pages;
+    v.slots = p->d_slots;
+    v.slot_stride = p->slot_stride;
+    v.max_adapters = p->max_adapters;
+    v.max_pages = p->max_pages;
+    v.d_in = p->d_in;
+    v.d_out = p->d_out;
+    return v;
+}
+
+size_t seg_entries(const lora_pool *p, int T) { return (size_t)std::min(T, p->max_adapters) + 1; }
+
+void free_scratch(lora_pool *p)
+{
+    const int T = p->cap_T;
+    if (T == 0) return;
+    free_dev(p, p->order, sizeof(int32_t) * T);
+    free_dev(p, p->hdr, sizeof(int32_t) * 4);
+    free_dev(p, p->seg_start, sizeof(int32_t) * seg_entries(p, T));
+    free_dev(p, p->seg_slot, sizeof(int32_t) * seg_entries(p, T));
+    free_dev(p, p->seg_ublk, sizeof(int32_t) * seg_entries(p, T));
+    free_dev(p, p->V, sizeof(float) * (size_t)T * p->ldv);
+    free_dev(p, p->partials, sizeof(float) * p->partials_floats);
+    p->order = p->hdr = p->seg_start = p->seg_slot = p->seg_ublk = nullptr;
+    p->V = p->partials = nullptr;
+    p->partials_floats = 0;
+    p->cap_T = 0;
+}
+
+lora_status ensure_scratch(lora_pool *p, int T)
+{
+    if (T <= p->cap_T) return LORA_OK;
+    CUDA_TRY(cudaDeviceSynchronize());  // earlier calls may still read the old scratch
+    free_scratch(p);
+    const size_t se = seg_entries(p, T);
+    const DecodePlan plan = plan_decode(std::min(T, kDecodeMaxT), p->d_in, p->d_out, p->num_sms);
+    const size_t pf = decode_partials_floats(plan);
+    lora_status st;
+    if ((st = alloc_dev(p, (void **)&p->order, sizeof(int32_t) * T)) ||
+        (st = alloc_dev(p, (void **)&p->hdr, sizeof(int32_t) * 4)) ||
+        (st = alloc_dev(p, (void **)&p->seg_start, sizeof(int32_t) * se)) ||
+        (st = alloc_dev(p, (void **)&p->seg_slot, sizeof(int32_t) * se)) ||
+        (st = alloc_dev(p, (void **)&p->seg_ublk, sizeof(int32_t) * se)) ||
+        (st = alloc_dev(p, (void **)&p->V, sizeof(float) * (size_t)T * p->ldv)) ||
+        (st = alloc_dev(p, (void **)&p->partials, sizeof(float) * pf))) {
+        p->cap_T = T;
+        p->partials_floats = pf;
+        free_scratch(p);
+        return st;
+    }
+    p->cap_T = T;
+    p->partials_floats = pf;
+    return LORA_OK;
+}
+
+SegTables seg_tables(const lora_pool *p)
+{
+    SegTables t;
+    t.order = p->order;
+    t.hdr = p->hdr;
+    t.seg_start = p->seg_start;
+    t.seg_slot = p->seg_slot;
+    t.seg_ublk = p->seg_ublk;
+    return t;
+}
+
+// Tensor maps are pure host descriptors of (pointer, shape, box); a small
+// per-pool cache avoids re-encoding them on every call with the same buffers.
+const CUtensorMap *tmap_for(lora_pool *p, const void *base, uint64_t inner, uint64_t rows,
+                            uint32_t box_inner, uint32_t box_rows)
+{
+    for (auto &e : p->tmaps)
+        if (e.base == base && e.inner == inner && e.rows == rows && e.box_inner == box_inner &&
+            e.box_rows == box_rows)
+            return &e.map;
+    TmapEntry &e = p->tmaps[p->tmap_next];
+    p->tmap_next = (p->tmap_next + 1) % (int)(sizeof(p->tmaps) / sizeof(p->tmaps[0]));
+    e.base = nullptr;
+    if (!make_tmap_bf16_2d(&e.map, base, inner, rows, inner * 2, box_inner, box_rows)) return nullptr;
+    e.base = base;
+    e.inner = inner;
+    e.rows = rows;
+    e.box_inner = box_inner;
+    e.box_rows = box_rows;
+    return &e.map;
+}
+
+__global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
+                                    int rank, const int32_t *__restrict__ pages, int npages, int d_in,
+                                    int d_out, uint16_t *__restrict__ A_pages,
+                                    uint16_t *__restrict__ B_pages)
+{
+    const size_t totA = (size_t)npages * kRankPage * d_in;
+    const size_t totB = (size_t)npages * d_out * kRankPage;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < totA + totB;
+         i += (size_t)gridDim.x * blockDim.x) {
+        if (i < totA) {
+            const size_t per_page = (size_t)kRankPage * d_in;
+            const int q = (int)(i / per_page);
+            const size_t rem = i % per_page;
+            const int jj = (int)(rem / d_in), k = (int)(rem % d_in);
+            const int j = q * kRankPage + jj;
+            A_pages[(size_t)pages[q] * per_page + rem] = (j < rank) ? A[(size_t)k * rank + j] : 0;
+        } else {
+            const size_t i2 = i - totA;
+            const size_t per_page = (size_t)d_out * kRankPage;
+            const int q = (int)(i2 / per_page);
+            const size_t rem = i2 % per_page;
+            const int n = (int)(rem / kRankPage), jj = (int)(rem % kRankPage);
+            const int j = q * kRankPage + jj;
+            B_pages[(size_t)pages[q] * per_page + rem] = (j < rank) ? B[(size_t)j * d_out + n] : 0;
+        }
+    }
+}
+
+bool dims_ok(int d) { return d > 0 && d <= LORA_MAX_DIM && d % 8 == 0; }
+
+lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t *ids, int T,
+                       void *Y, cudaStream_t stream, bool with_lora)
+{
+    if (!p || !X || !W || !Y || (with_lora && !ids) || T < 0) return LORA_ERR_ARG;
+    int path = p->path;
+    if (path == LORA_PATH_AUTO) path = T <= kDecodeMaxT ? LORA_PATH_DECODE : LORA_PATH_PREFILL;
+    if (path == LORA_PATH_DECODE && T > kDecodeMaxT) return LORA_ERR_ARG;
+    if (T == 0) return LORA_OK;
+    lora_status st = ensure_scratch(p, T);
+    if (st != LORA_OK) return st;
+
+    const PoolDev pd = pool_view(p);
+    const SegTables tabs = seg_tables(p);
+    const uint16_t *Xb = static_cast<const uint16_t *>(X);
+    uint16_t *Yb = static_cast<uint16_t *>(Y);
+
+    if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
+
+    if (path == LORA_PATH_DECODE) {
+        const DecodePlan plan = plan_decode(T, p->d_in, p->d_out, p->num_sms);
+        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 128);
+        const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, plan.ntok);
+        if (!tmW || !tmX) return LORA_ERR_ARG;
+        if (with_lora) CUDA_TRY(launch_shrink_simt(Xb, T, pd, tabs, p->V, p->ldv, stream));
+        CUDA_TRY(launch_gemm_decode(*tmW, *tmX, plan, p->d_out, p->partials, p->d_err, stream));
+        CUDA_TRY(launch_finish_decode(plan, p->partials, with_lora ? ids : nullptr, pd, p->V,
+                                      p->ldv, Yb, stream));
+    } else {
+        const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, 128);
+        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 256);
+        if (!tmW || !tmX) return LORA_ERR_ARG;
+        if (with_lora)
+            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, Xb, T, pd, tabs, p->V, p->ldv, p->num_sms,
+                                      p->d_err, stream));
+        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, T, with_lora ? ids : nullptr, pd, p->V, p->ldv,
+                                     Yb, p->num_sms, p->d_err, stream));
+    }
+    p->n_calls += 1;
+    return LORA_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+
+extern "C" {
+
+int lora_abi_version(void) { return LORA_ABI_VERSION; }
+
+const char *lora_status_string(lora_status s)
+{
+    switch (s) {
+    case LORA_OK: return "ok";
+    case LORA_ERR_ARG: return "invalid argument";
+    case LORA_ERR_SHAPE: return "invalid shape";
+    case LORA_ERR_SLOT_RANGE: return "slot out of range";
+    case LORA_ERR_SLOT_OCCUPIED: return "slot already holds an adapter";
+    case LORA_ERR_SLOT_EMPTY: return "slot is empty";
+    case LORA_ERR_RANK: return "rank out of range";
+    case LORA_ERR_BAD_ADAPTER_ID: return "a token id named no loaded adapter";
+    case LORA_ERR_CUDA: return "CUDA error";
+    case LORA_ERR_OOM: return "out of device memory";
+    case LORA_ERR_TIMEOUT: return "a kernel wait timed out";
+    case LORA_ERR_UNSUPPORTED: return "device is not compute capability 10.3";
+    }
+    return "unknown status";
+}
+
+lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out, lora_pool_t *out)
+{
+    if (!out) return LORA_ERR_ARG;
+    *out = nullptr;
+    if (max_adapters < 1 || max_adapters > LORA_MAX_ADAPTERS) return LORA_ERR_ARG;
+    if (max_rank < 1 || max_rank > LORA_MAX_RANK) return LORA_ERR_RANK;
+    if (!dims_ok(d_in) || !dims_ok(d_out)) return LORA_ERR_SHAPE;
+
+    int dev = 0, major = 0, minor = 0, sms = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+    CUDA_TRY(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+    if (major != 10 || minor != 3) return LORA_ERR_UNSUPPORTED;
+
+    lora_pool *p = new (std::nothrow) lora_pool();
+    if (!p) return LORA_ERR_OOM;
+    p->device = dev;
+    p->num_sms = sms;
+    p->max_adapters = max_adapters;
+    p->max_rank = max_rank;
+    p->d_in = d_in;
+    p->d_out = d_out;
+    p->max_pages = (max_rank + kRankPage - 1) / kRankPage;
+    p->num_pages = max_adapters * p->max_pages + 1;
+    p->slot_stride = ((SLOT_PAGES + p->max_pages + 3) / 4) * 4;
+    p->ldv = ((p->max_pages * kRankPage + 15) / 16) * 16;
+    p->h_slots.assign((size_t)max_adapters * p->slot_stride, 0);
+    p->free_pages.reserve(p->num_pages - 1);
+    for (int pg = p->num_pages - 1; pg >= 1; --pg) p->free_pages.push_back(pg);
+
+    const size_t a_bytes = (size_t)p->num_pages * kRankPage * d_in * 2;
+    const size_t b_bytes = (size_t)p->num_pages * d_out * kRankPage * 2;
+    lora_status st;
+    if ((st = alloc_dev(p, (void **)&p->A_pages, a_bytes)) ||
+        (st = alloc_dev(p, (void **)&p->B_pages, b_bytes)) ||
+        (st = alloc_dev(p, (void **)&p->d_slots, sizeof(int32_t) * p->h_slots.size())) ||
+        (st = alloc_dev(p, (void **)&p->d_err, sizeof(int))) ||
+        (st = alloc_dev(p, (void **)&p->stage_A, (size_t)d_in * max_rank * 2)) ||
+        (st = alloc_dev(p, (void **)&p->stage_B, (size_t)d_out * max_rank * 2)) ||
+        (st = alloc_dev(p, (void **)&p->d_page_list, sizeof(int32_t) * p->max_pages))) {
+        lora_pool_destroy(p);
+        return st;
+    }
+    if (cudaMemset(p->A_pages, 0, (size_t)kRankPage * d_in * 2) != cudaSuccess ||
+        cudaMemset(p->B_pages, 0, (size_t)d_out * kRankPage * 2) != cudaSuccess ||
+        cudaMemset(p->d_slots, 0, sizeof(int32_t) * p->h_slots.size()) != cudaSuccess ||
+        cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        !make_tmap_bf16_2d(&p->tmA, p->A_pages, d_in, (uint64_t)p->num_pages * kRankPage,
+                           (uint64_t)d_in * 2, 64, kRankPage) ||
+        cudaDeviceSynchronize() != cudaSuccess) {
+        lora_pool_destroy(p);
+        return LORA_ERR_CUDA;
+    }
+    *out = p;
+    return LORA_OK;
+}
+
+lora_status lora_pool_destroy(lora_pool_t p)
+{
+    if (!p) return LORA_ERR_ARG;
+    cudaDeviceSynchronize();
+    free_scratch(p);
+    free_dev(p, p->hx, (size_t)p->cap_host_T * p->d_in * 2);
+    free_dev(p, p->hy, (size_t)p->cap_host_T * p->d_out * 2);
+    free_dev(p, p->hids, sizeof(int32_t) * (size_t)p->cap_host_T);
+    free_dev(p, p->A_pages, 0);
+    free_dev(p, p->B_pages, 0);
+    free_dev(p, p->d_slots, 0);
+    free_dev(p, p->d_err, 0);
+    free_dev(p, p->stage_A, 0);
+    free_dev(p, p->stage_B, 0);
+    free_dev(p, p->d_page_list, 0);
+    if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    delete p;
+    return LORA_OK;
+}
+
+lora_status lora_pool_reserve(lora_pool_t p, int max_tokens)
+{
+    if (!p || max_tokens < 0) return LORA_ERR_ARG;
+    return ensure_scratch(p, max_tokens);
+}
+
+lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void *B, int rank,
+                              float alpha)
+{
+    if (!p || !A || !B) return LORA_ERR_ARG;
+    if (slot < 0 || slot >= p->max_adapters) return LORA_ERR_SLOT_RANGE;
+    if (rank < 1 || rank > p->max_rank) return LORA_ERR_RANK;
+    int32_t *row = &p->h_slots[(size_t)slot * p->slot_stride];
+    if (row[SLOT_RANK] != 0) return LORA_ERR_SLOT_OCCUPIED;
+    const int npages = (rank + kRankPage - 1) / kRankPage;
+    if ((int)p->free_pages.size() < npages) return LORA_ERR_OOM;
+
+    // calls already enqueued keep seeing the old pages and table
+    CUDA_TRY(cudaDeviceSynchronize());
+
+    std::vector<int32_t> pages(npages);
+    for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
+
+    cudaStream_t s = p->copy_stream;
+    const size_t a_bytes = (size_t)p->d_in * rank * 2, b_bytes = (size_t)rank * p->d_out * 2;
+    bool ok = cudaMemcpyAsync(p->stage_A, A, a_bytes, cudaMemcpyDefault, s) == cudaSuccess &&
+              cudaMemcpyAsync(p->stage_B, B, b_bytes, cudaMemcpyDefault, s) == cudaSuccess &&
+              cudaMemcpyAsync(p->d_page_list, pages.data(), sizeof(int32_t) * npages,
+                              cudaMemcpyHostToDevice, s) == cudaSuccess &&
+              launch_pack_adapter(p->stage_A, p->stage_B, rank, p->d_page_list, npages,
+                                  pool_view(p), p->A_pages, p->B_pages, s) == cudaSuccess;
+    std::vector<int32_t> new_row(p->slot_stride, 0);
+    new_row[SLOT_RANK] = rank;
+    new_row[SLOT_NPAGES] = npages;
+    const float scale = alpha / (float)rank;
+    std::memcpy(&new_row[SLOT_SCALE], &scale, sizeof(float));
+    for (int q = 0; q < npages; ++q) new_row[SLOT_PAGES + q] = pages[q];
+    ok = ok &&
+         cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, new_row.data(),
+                         sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice, s) == cudaSuccess;
+    ok = (cudaStreamSynchronize(s) == cudaSuccess) && ok;
+    if (!ok) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    p->free_pages.resize(p->free_pages.size() - npages);
+    std::copy(new_row.begin(), new_row.end(), row);
+    p->n_loads += 1;
+    return LORA_OK;
+}
+
+lora_status lora_unload_adapter(lora_pool_t p, int slot)
+{
+    if (!p) return LORA_ERR_ARG;
+    if (slot < 0 || slot >= p->max_adapters) return LORA_ERR_SLOT_RANGE;
+    int32_t *row = &p->h_slots[(size_t)slot * p->slot_stride];
+    if (row[SLOT_RANK] == 0) return LORA_ERR_SLOT_EMPTY;
+    CUDA_TRY(cudaDeviceSynchronize());
+    std::vector<int32_t> zero(p->slot_stride, 0);
+    if (cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, zero.data(),
+                        sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice,
+                        p->copy_stream) != cudaSuccess ||
+        cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    const int npages = row[SLOT_NPAGES];
+    for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
+    std::fill(row, row + p->slot_stride, 0);
+    p->n_unloads += 1;
+    return LORA_OK;
+}
+
+lora_status lora_linear(lora_pool_t p, const void *X, const void *W_base,
+                        const int32_t *token_adapter_ids, int T, void *Y, lora_stream_t stream)
+{
+    return run_linear(p, X, W_base, token_adapter_ids, T, Y, (cudaStream_t)stream, true);
+}
+
+lora_status lora_base_linear(lora_pool_t p, const void *X, const void *W_base, int T, void *Y,
+                             lora_stream_t stream)
+{
+    return run_linear(p, X, W_base, nullptr, T, Y, (cudaStream_t)stream, false);
+}
+
+lora_status lora_linear_host(lora_pool_t p, const void *X_host, const void *W_base,
+                             const int32_t *ids_host, int T, void *Y_host, lora_stream_t stream)
+{
+    if (!p || !X_host || !W_base || !ids_host || !Y_host || T < 0) return LORA_ERR_ARG;
+    if (T == 0) return LORA_OK;
+    if (T > p->cap_host_T) {
+        CUDA_TRY(cudaDeviceSynchronize());
+        free_dev(p, p->hx, (size_t)p->cap_host_T * p->d_in * 2);
+        free_dev(p, p->hy, (size_t)p->cap_host_T * p->d_out * 2);
+        free_dev(p, p->hids, sizeof(int32_t) * (size_t)p->cap_host_T);
+        p->hx = p->hy = nullptr;
+        p->hids = nullptr;
+        p->cap_host_T = 0;
+        lora_status st;
+        if ((st = alloc_dev(p, (void **)&p->hx, (size_t)T * p->d_in * 2)) ||
+            (st = alloc_dev(p, (void **)&p->hy, (size_t)T * p->d_out * 2)) ||
+            (st = alloc_dev(p, (void **)&p->hids, sizeof(int32_t) * (size_t)T)))
+            return st;
+        p->cap_host_T = T;
+    }
+    cudaStream_t s = (cudaStream_t)stream;
+    CUDA_TRY(cudaMemcpyAsync(p->hx, X_host, (size_t)T * p->d_in * 2, cudaMemcpyHostToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(p->hids, ids_host, sizeof(int32_t) * (size_t)T, cudaMemcpyHostToDevice, s));
+    lora_status st = run_linear(p, p->hx, W_base, p->hids, T, p->hy, s, true);
+    if (st != LORA_OK) return st;
+    CUDA_TRY(cudaMemcpyAsync(Y_host, p->hy, (size_t)T * p->d_out * 2, cudaMemcpyDeviceToHost, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    return LORA_OK;
+}
+
+lora_status lora_pool_check_errors(lora_pool_t p)
+{
+    if (!p) return LORA_ERR_ARG;
+    if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
+    int word = 0;
+    CUDA_TRY(cudaMemcpy(&word, p->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+    CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int)));
+    CUDA_TRY(cudaDeviceSynchronize());
+    if (word & kErrBadIdBit) return LORA_ERR_BAD_ADAPTER_ID;
+    if (word & kErrTimeoutBit) return LORA_ERR_TIMEOUT;
+    return LORA_OK;
+}
+
+lora_status lora_build_segments(lora_pool_t p, const int32_t *ids, int T, int32_t *order,
+                                int32_t *n_base, int32_t *num_seg, int32_t *seg_start,
+                                int32_t *seg_slot, lora_stream_t stream)
+{
+    if (!p || !ids || !order || !n_base || !num_seg || !seg_start || !seg_slot || T < 0)
+        return LORA_ERR_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T == 0) {
+        CUDA_TRY(cudaMemsetAsync(n_base, 0, sizeof(int32_t), s));
+        CUDA_TRY(cudaMemsetAsync(num_seg, 0, sizeof(int32_t), s));
+        CUDA_TRY(cudaMemsetAsync(seg_start, 0, sizeof(int32_t), s));
+        return LORA_OK;
+    }
+    lora_status st = ensure_scratch(p, T);
+    if (st != LORA_OK) return st;
+    const SegTables tabs = seg_tables(p);
+    CUDA_TRY(launch_seg_build(ids, T, pool_view(p), tabs, p->d_err, s));
+    const size_t se = seg_entries(p, T);
+    CUDA_TRY(cudaMemcpyAsync(order, p->order, sizeof(int32_t) * T, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(n_base, p->hdr + HDR_NBASE, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(num_seg, p->hdr + HDR_NUMSEG, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(seg_start, p->seg_start, sizeof(int32_t) * se, cudaMemcpyDeviceToDevice, s));
+    CUDA_TRY(cudaMemcpyAsync(seg_slot, p->seg_slot, sizeof(int32_t) * (se - 1), cudaMemcpyDeviceToDevice, s));
+    return LORA_OK;
+}
+
+lora_status lora_pool_stats(lora_pool_t p, int64_t *out)
+{
+    if (!p || !out) return LORA_ERR_ARG;
+    int64_t loaded = 0;
+    for (int i = 0; i < p->max_adapters; ++i)
+        if (p->h_slots[(size_t)i * p->slot_stride + SLOT_RANK] != 0) ++loaded;
+    out[0] = loaded;
+    out[1] = (int64_t)p->free_pages.size();
+    out[2] = (int64_t)p->num_pages - 1;
+    out[3] = p->n_loads;
+    out[4] = p->n_unloads;
+    out[5] = p->n_calls;
+    out[6] = (int64_t)p->bytes_held;
+    return LORA_OK;
+}
+
+lora_status lora_pool_set_path(lora_pool_t p, int path)
+{
+    if (!p || path < LORA_PATH_AUTO || path > LORA_PATH_PREFILL) return LORA_ERR_ARG;
+    p->path = path;
+    return LORA_OK;
+}
+
+}  // extern "C"
+
+// ============================================================== helpers
+
+namespace lora {
+
+cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,
+                                int npages, const PoolDev &pool, uint16_t *A_pages,
+                                uint16_t *B_pages, cudaStream_t stream)
+{
+    const size_t total = (size_t)npages * kRankPage * (pool.d_in + pool.d_out);
+    int grid = (int)std::min<size_t>((total + 255) / 256, 4096);
+    pack_adapter_kernel<<<grid, 256, 0, stream>>>(A, B, rank, pages, npages, pool.d_in, pool.d_out,
+                                                  A_pages, B_pages);
+    return cudaGetLastError();
+}
+
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows)
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    if (!encode || rows == 0) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+}  // namespace lora

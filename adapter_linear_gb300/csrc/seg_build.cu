@@ -1,0 +1,196 @@
+// seg_build.cu -- segment builder: the "Grouped Multi-LoRA Execution" step of
+// the LoRA-Land blog (核心实现解析 / 2. 多 LoRA 批处理调度): the batch is grouped
+// by LoRA id so every group can be run contiguously with its own A, B.
+//
+// One CTA performs a stable counting sort of the token indices by adapter id.
+// Key = id + 1 (key 0 collects the base-only tokens and any invalid id, so
+// they come first). The tokens are cut into 8 contiguous chunks, one per warp:
+//   A. each warp counts its chunk per key (warp match, leader adds);
+//   B. per-key warp prefixes + one block-wide exclusive scan over keys give
+//      every (key, warp) its first output position, and every present key
+//      >= 1 its segment (start, slot, prefix of 128-row units);
+//   C. each warp walks its chunk again in token order and scatters; within a
+//      32-token step equal keys are ranked by lane, so ties keep token order.
+// The result is unique (a stable sort), so it is compared bit for bit.
+#include "device_common.cuh"
+
+namespace lora {
+
+namespace {
+
+constexpr int kSegThreads = 256;
+constexpr int kSegWarps = kSegThreads / 32;
+
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Key of a token; flags ids that are neither -1 nor a loaded slot.
+__device__ __forceinline__ int token_key(int id, const PoolDev &pool, bool &bad)
+{
+    if (id == -1) return 0;
+    if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) return id + 1;
+    bad = true;
+    return 0;
+}
+
+__global__ void __launch_bounds__(kSegThreads, 1)
+    seg_build_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
+                     int *__restrict__ err)
+{
+    extern __shared__ uint32_t seg_smem[];
+    const int K = pool.max_adapters + 1;
+    uint32_t *cnt = seg_smem;                          // [K][kSegWarps]
+    uint32_t *koff = seg_smem + (size_t)K * kSegWarps;  // [K]
+    __shared__ uint32_t warp_tot[3][kSegWarps];
+    __shared__ int any_bad;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < K * kSegWarps; i += kSegThreads) cnt[i] = 0;
+    if (tid == 0) any_bad = 0;
+    __syncthreads();
+
+    const int chunk = (T + kSegWarps - 1) / kSegWarps;
+    const int t0 = min(T, warp * chunk), t1 = min(T, t0 + chunk);
+
+    // ---- A: per-warp counts
+    bool bad = false;
+    for (int base = t0; base < t1; base += 32) {
+        const int t = base + lane;
+        const bool valid = t < t1;
+        int key = 0;
+        if (valid) key = token_key(ids[t], pool, bad);
+        const unsigned active = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+            const unsigned same = __match_any_sync(active, key);
+            if (lane == __ffs(same) - 1) cnt[key * kSegWarps + warp] += __popc(same);
+        }
+    }
+    if (bad) any_bad = 1;
+    __syncthreads();
+
+    // ---- B1: exclusive prefix over warps inside each key; koff = key total
+    for (int k = tid; k < K; k += kSegThreads) {
+        uint32_t run = 0;
+#pragma unroll
+        for (int w = 0; w < kSegWarps; ++w) {
+            const uint32_t c = cnt[k * kSegWarps + w];
+            cnt[k * kSegWarps + w] = run;
+            run += c;
+        }
+        koff[k] = run;
+    }
+    __syncthreads();
+
+    // ---- B2: block-wide exclusive scan over keys of (tokens, segments, units)
+    const int per = (K + kSegThreads - 1) / kSegThreads;
+    const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
+    uint32_t sc = 0, ss = 0, su = 0;
+    for (int k = k_lo; k < k_hi; ++k) {
+        const uint32_t tot = koff[k];
+        sc += tot;
+        if (k >= 1 && tot > 0) {
+            ss += 1;
+            su += (tot + kShrinkRows - 1) / kShrinkRows;
+        }
+    }
+    uint32_t ic = sc, is = ss, iu = su;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t c = __shfl_up_sync(0xffffffffu, ic, o);
+        const uint32_t s = __shfl_up_sync(0xffffffffu, is, o);
+        const uint32_t u = __shfl_up_sync(0xffffffffu, iu, o);
+        if (lane >= o) {
+            ic += c;
+            is += s;
+            iu += u;
+        }
+    }
+    if (lane == 31) {
+        warp_tot[0][warp] = ic;
+        warp_tot[1][warp] = is;
+        warp_tot[2][warp] = iu;
+    }
+    __syncthreads();
+    uint32_t wc = 0, ws = 0, wu = 0, all_s = 0, all_u = 0;
+    for (int w = 0; w < kSegWarps; ++w) {
+        if (w < warp) {
+            wc += warp_tot[0][w];
+            ws += warp_tot[1][w];
+            wu += warp_tot[2][w];
+        }
+        all_s += warp_tot[1][w];
+        all_u += warp_tot[2][w];
+    }
+    uint32_t pc = wc + ic - sc, ps = ws + is - ss, pu = wu + iu - su;  // exclusive
+    if (tid == 0) tabs.hdr[HDR_NBASE] = (int32_t)koff[0];
+    __syncthreads();  // koff[0] read above before it is overwritten below
+    for (int k = k_lo; k < k_hi; ++k) {
+        const uint32_t tot = koff[k];
+        koff[k] = pc;
+        if (k >= 1 && tot > 0) {
+            tabs.seg_start[ps] = (int32_t)pc;
+            tabs.seg_slot[ps] = k - 1;
+            tabs.seg_ublk[ps] = (int32_t)pu;
+            ps += 1;
+            pu += (tot + kShrinkRows - 1) / kShrinkRows;
+        }
+        pc += tot;
+    }
+    if (tid == 0) {
+        tabs.hdr[HDR_NUMSEG] = (int32_t)all_s;
+        tabs.hdr[HDR_UNITS] = (int32_t)all_u;
+        tabs.seg_start[all_s] = T;
+        tabs.seg_ublk[all_s] = (int32_t)all_u;
+        if (any_bad) atomicOr(err, kErrBadIdBit);
+    }
+    __syncthreads();
+
+    // ---- C: stable scatter
+    for (int base = t0; base < t1; base += 32) {
+        const int t = base + lane;
+        const bool valid = t < t1;
+        bool unused = false;
+        int key = 0;
+        if (valid) key = token_key(ids[t], pool, unused);
+        const unsigned active = __ballot_sync(0xffffffffu, valid);
+        if (valid) {
+            const unsigned same = __match_any_sync(active, key);
+            const uint32_t pos =
+                koff[key] + cnt[key * kSegWarps + warp] + __popc(same & lanemask_lt());
+            tabs.order[pos] = t;
+            __syncwarp(active);
+            if (lane == __ffs(same) - 1) cnt[key * kSegWarps + warp] += __popc(same);
+        }
+        __syncwarp();
+    }
+}
+
+}  // namespace
+
+size_t seg_build_smem_bytes(int max_adapters)
+{
+    const size_t K = (size_t)max_adapters + 1;
+    return K * kSegWarps * sizeof(uint32_t) + K * sizeof(uint32_t);
+}
+
+cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
+                             int *err, cudaStream_t stream)
+{
+    const size_t smem = seg_build_smem_bytes(pool.max_adapters);
+    static bool configured = false;
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(seg_build_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)seg_build_smem_bytes(4096));
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(ids, T, pool, tabs, err);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

@@ -1,0 +1,365 @@
+// shrink.cu -- the low-rank "shrink" V = s_i * X[t,:] A_i for every token with
+// an adapter: the low-dimensional intermediate that the LoRA-Land blog
+// (核心实现解析 / 2) forms first, so that the extra work stays a small
+// fraction of the base product. V is fp32 [T][ldv], indexed by token; the
+// scale s_i = alpha_i / r_i is folded in here. Columns of the pages beyond an
+// adapter's rank come out as exact zeros (zero-padded pages).
+//
+// Two kernels compute the same V:
+//  * shrink_simt_kernel (decode batches): one CTA per (segment, page). The
+//    A page (8 x d_in bf16) is read once with 128-bit loads and applied to
+//    every token of the segment, four tokens at a time; the 32 partial dot
+//    products per thread are reduced with a warp transpose-reduce and one
+//    shared-memory pass.
+//  * shrink_tc_kernel (prefill batches): persistent; one unit = up to 128
+//    tokens of one segment. tcgen05 MMA M=128 (tokens) x N=16..256 (rank rows,
+//    padded with the zero page) x K=d_in, operands staged by TMA (X rows when
+//    the segment's tokens are contiguous, else gathered by the producer warp
+//    into the same 128-byte-swizzled layout), fp32 accumulator in TMEM,
+//    double-buffered so one unit's epilogue overlaps the next unit's MMAs.
+#include "device_common.cuh"
+
+namespace lora {
+
+// ============================================================ CUDA-core shrink
+
+namespace {
+
+constexpr int kSimtThreads = 256;
+constexpr int kTokGroup = 4;
+
+__global__ void __launch_bounds__(kSimtThreads)
+    shrink_simt_kernel(const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
+                       float *__restrict__ V, int ldv)
+{
+    const int q = blockIdx.x % pool.max_pages;
+    const int s = blockIdx.x / pool.max_pages;
+    if (s >= tabs.hdr[HDR_NUMSEG]) return;
+    const int slot = tabs.seg_slot[s];
+    const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
+    const int npages = row[SLOT_NPAGES];
+    if (q >= npages) return;
+    const float scale = __int_as_float(row[SLOT_SCALE]);
+    const int page = row[SLOT_PAGES + q];
+    const int d_in = pool.d_in;
+    const uint16_t *Ap = pool.A_pages + (size_t)page * kRankPage * d_in;
+    const int p0 = tabs.seg_start[s], p1 = tabs.seg_start[s + 1];
+    const int nchunk = d_in / 8;  // 16-byte chunks along k
+
+    __shared__ float red[kSimtThreads / 32][32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    for (int pb = p0; pb < p1; pb += kTokGroup) {
+        const int nt = min(kTokGroup, p1 - pb);
+        int tok[kTokGroup];
+#pragma unroll
+        for (int i = 0; i < kTokGroup; ++i) tok[i] = tabs.order[pb + min(i, nt - 1)];
+
+        float v[kTokGroup * kRankPage];
+#pragma unroll
+        for (int i = 0; i < kTokGroup * kRankPage; ++i) v[i] = 0.f;
+
+        for (int c = threadIdx.x; c < nchunk; c += kSimtThreads) {
+            uint4 a[kRankPage];
+#pragma unroll
+            for (int jj = 0; jj < kRankPage; ++jj) a[jj] = ldg_nc_v4(Ap + (size_t)jj * d_in + c * 8);
+            uint4 x[kTokGroup];
+#pragma unroll
+            for (int i = 0; i < kTokGroup; ++i)
+                x[i] = (i < nt) ? ldg_nc_v4(X + (size_t)tok[i] * d_in + c * 8) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+            for (int i = 0; i < kTokGroup; ++i)
+#pragma unroll
+                for (int jj = 0; jj < kRankPage; ++jj)
+                    v[i * kRankPage + jj] = dot8_bf16(x[i], a[jj], v[i * kRankPage + jj]);
+        }
+
+        // warp transpose-reduce: afterwards lane l holds the warp sum of v[l]
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            const bool upper = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < o; ++i) {
+                const float send = upper ? v[i] : v[i + o];
+                const float keep = upper ? v[i + o] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+        }
+        red[warp][lane] = v[0];
+        __syncthreads();
+        if (warp == 0) {
+            float tot = 0.f;
+#pragma unroll
+            for (int w = 0; w < kSimtThreads / 32; ++w) tot += red[w][lane];
+            const int i = lane / kRankPage, jj = lane % kRankPage;
+            if (i < nt) V[(size_t)tok[i] * ldv + q * kRankPage + jj] = scale * tot;
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_shrink_simt(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs,
+                               float *V, int ldv, cudaStream_t stream)
+{
+    const int max_seg = T < pool.max_adapters ? T : pool.max_adapters;
+    const int grid = max_seg * pool.max_pages;
+    if (grid == 0) return cudaSuccess;
+    shrink_simt_kernel<<<grid, kSimtThreads, 0, stream>>>(X, pool, tabs, V, ldv);
+    return cudaGetLastError();
+}
+
+// ========================================================== tensor-core shrink
+
+namespace {
+
+constexpr int kTcThreads = 192;          // warps 0-3 epilogue, 4 producer, 5 MMA
+constexpr int kXTileBytes = 128 * 128;   // 128 rows x 64 bf16
+
+struct UnitInfo {
+    int p0, p1;       // positions in `order`
+    int npages;       // adapter pages
+    int n;            // MMA N: npages * 8 rounded up to 16
+    float scale;
+    const int32_t *pages;
+};
+
+__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs)
+{
+    // segment s: largest s with seg_ublk[s] <= u (seg_ublk ascending, [num_seg + 1])
+    int lo = 0, hi = tabs.hdr[HDR_NUMSEG];
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (tabs.seg_ublk[mid] <= u) lo = mid; else hi = mid;
+    }
+    const int s = lo;
+    UnitInfo r;
+    r.p0 = tabs.seg_start[s] + (u - tabs.seg_ublk[s]) * kShrinkRows;
+    r.p1 = min(r.p0 + kShrinkRows, tabs.seg_start[s + 1]);
+    const int32_t *row = pool.slots + (size_t)tabs.seg_slot[s] * pool.slot_stride;
+    r.npages = row[SLOT_NPAGES];
+    r.n = ((r.npages * kRankPage + 15) / 16) * 16;
+    r.scale = __int_as_float(row[SLOT_SCALE]);
+    r.pages = row + SLOT_PAGES;
+    return r;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+    shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
+                     const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
+                     float *__restrict__ V, int ldv, int nmax, int stages, uint32_t tmem_cols,
+                     int *err)
+{
+    extern __shared__ uint8_t shrink_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(shrink_smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t p_bytes = (uint32_t)nmax * 128;
+    const uint32_t stage_bytes = kXTileBytes + p_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
+    uint64_t *empty = full + stages;
+    uint64_t *acc_full = empty + stages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;   // [2]
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int units = tabs.hdr[HDR_UNITS];
+    const int d_in = pool.d_in;
+    const int KB = (d_in + 63) / 64;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < stages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 4);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tmem_alloc(tmem_slot, tmem_cols);
+        tmem_relinquish();
+    }
+    if (warp == 4 && lane == 0) {
+        tma_prefetch_map(&tmX);
+        tma_prefetch_map(&tmA);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        int it = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
+            const UnitInfo ui = unit_info(u, pool, tabs);
+            const int row0 = tabs.order[ui.p0];
+            bool contiguous = true;
+            for (int r = lane; r < ui.p1 - ui.p0; r += 32)
+                contiguous &= (tabs.order[ui.p0 + r] == row0 + r);
+            contiguous = __all_sync(0xffffffffu, contiguous);
+            const int npad = ui.n / kRankPage;
+            const uint32_t bytes = (uint32_t)npad * 1024u + (contiguous ? kXTileBytes : 0u);
+            bool ok = true;
+            for (int kb = 0; kb < KB && ok; ++kb, ++it) {
+                const int s = it % stages;
+                const uint32_t ph = (uint32_t)(it / stages) & 1u;
+                if (lane == 0) ok = mbar_wait(&empty[s], ph ^ 1u, &abort_flag, err);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) break;
+                uint8_t *xs = smem + (size_t)s * stage_bytes;
+                uint8_t *ps = xs + kXTileBytes;
+                if (!contiguous) {
+                    // gather 128 rows x 64 bf16 into the 128-byte-swizzled layout
+                    for (int r = lane; r < 128; r += 32) {
+                        const int p = ui.p0 + r;
+                        const int tok = (p < ui.p1) ? tabs.order[p] : -1;
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const int k = kb * 64 + c * 8;
+                            uint4 val = make_uint4(0, 0, 0, 0);
+                            if (tok >= 0 && k < d_in) val = ldg_nc_v4(X + (size_t)tok * d_in + k);
+                            *reinterpret_cast<uint4 *>(xs + r * 128 + ((c ^ (r & 7)) << 4)) = val;
+                        }
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&full[s], bytes);
+                    if (contiguous) tma_load_2d(xs, &tmX, &full[s], kb * 64, row0);
+                    for (int q = 0; q < npad; ++q) {
+                        const int page = q < ui.npages ? ui.pages[q] : 0;
+                        tma_load_2d(ps + q * 1024, &tmA, &full[s], kb * 64, page * kRankPage);
+                    }
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+        }
+        // wait for this CTA's last loads to land before it may exit
+        if (lane == 0) {
+            for (int i = 0; i < stages && i < it; ++i) {
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait(&full[j % stages], (uint32_t)(j / stages) & 1u, &dummy, err);
+            }
+        }
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        if (lane == 0) {
+            int it = 0, uc = 0;
+            bool ok = true;
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+                const UnitInfo ui = unit_info(u, pool, tabs);
+                const int buf = uc & 1;
+                ok = mbar_wait(&acc_empty[buf], ((uint32_t)(uc >> 1) & 1u) ^ 1u, &abort_flag, err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t idesc = idesc_bf16_f32(128, ui.n);
+                const uint32_t d = tmem + (uint32_t)(buf * nmax);
+                for (int kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = it % stages;
+                    ok = mbar_wait(&full[s], (uint32_t)(it / stages) & 1u, &abort_flag, err);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t xa = smem_u32(smem + (size_t)s * stage_bytes);
+                    const uint32_t pa = xa + kXTileBytes;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(pa + kk * 32),
+                                    idesc, (kb | kk) != 0);
+                    mma_commit(&empty[s]);
+                }
+                if (ok) mma_commit(&acc_full[buf]);
+            }
+            mma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------ epilogue
+        int uc = 0;
+        for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+            const UnitInfo ui = unit_info(u, pool, tabs);
+            const int buf = uc & 1;
+            bool ok = true;
+            if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(uc >> 1) & 1u, &abort_flag, err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            const int r = warp * 32 + lane;
+            const int p = ui.p0 + r;
+            const bool valid = p < ui.p1;
+            const int tok = valid ? tabs.order[p] : 0;
+            float *vrow = V + (size_t)tok * ldv;
+            for (int col = 0; col < ui.n; col += 16) {
+                uint32_t v[16];
+                tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * nmax + col), v);
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 16; j += 4) {
+                        float4 o;
+                        o.x = ui.scale * __uint_as_float(v[j + 0]);
+                        o.y = ui.scale * __uint_as_float(v[j + 1]);
+                        o.z = ui.scale * __uint_as_float(v[j + 2]);
+                        o.w = ui.scale * __uint_as_float(v[j + 3]);
+                        *reinterpret_cast<float4 *>(vrow + col + j) = o;
+                    }
+                }
+            }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, tmem_cols);
+    }
+}
+
+uint32_t pow2_cols(uint32_t n)
+{
+    uint32_t c = 32;
+    while (c < n) c <<= 1;
+    return c;
+}
+
+}  // namespace
+
+cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
+                             int T, const PoolDev &pool, SegTables tabs, float *V, int ldv,
+                             int num_sms, int *err, cudaStream_t stream)
+{
+    const int nmax = ((pool.max_pages * kRankPage + 15) / 16) * 16;
+    const size_t stage_bytes = kXTileBytes + (size_t)nmax * 128;
+    int stages = (int)((200 * 1024) / stage_bytes);
+    if (stages > 6) stages = 6;
+    if (stages < 2) stages = 2;
+    const size_t smem = 1024 + stages * stage_bytes + (2 * stages + 5) * 8 + 16;
+    const uint32_t tmem_cols = pow2_cols(2 * nmax);
+    const int max_seg = T < pool.max_adapters ? T : pool.max_adapters;
+    const int max_units = (T + kShrinkRows - 1) / kShrinkRows + max_seg;
+    int grid = max_units < num_sms ? max_units : num_sms;
+    if (grid <= 0) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(shrink_tc_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, X, pool, tabs, V, ldv, nmax,
+                                                          stages, tmem_cols, err);
+    return cudaGetLastError();
+}
+
+}  // namespace lora

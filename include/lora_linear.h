@@ -1,0 +1,223 @@
+/*
+ * lora_linear.h -- C ABI of the GB300 (sm_103a) heterogeneous multi-LoRA linear layer.
+ *
+ * The layer: for a batch of T tokens, each tagged with an adapter slot id
+ * (-1 = base only),
+ *
+ *     Y[t,:] = X[t,:] W_base^T + (alpha_i / r_i) (X[t,:] A_i) B_i,   i = ids[t]
+ *
+ * with A_i d_in x r_i and B_i r_i x d_out, over adapters resident in one GPU
+ * pool. Definition: "LoRA-Land: 将大模型变成操作系统..." (blog), section
+ * 核心实现解析 / 2. 多 LoRA 批处理调度 (shared base weight, per-group A,B
+ * correction, X@A formed first as a low-dimensional intermediate; the printed
+ * equation's transposes are garbled, the row-token reading above is used);
+ * "多 LoRA 热插拔: 一模型服多租户" (vLLM tutorial), sections "LoRA 速览"
+ * (W'x = Wx + BAx) and "vLLM 的 Multi-LoRA 怎么实现" (one unified adapter
+ * memory pool; different adapters in one batch; the base path always shared);
+ * icman.com.cn Multi-LoRA article, section 3.2 (alpha controls the scale,
+ * read as s = alpha / rank).
+ *
+ * Conventions for every call:
+ *  - bf16 tensors are passed as raw pointers to bfloat16 values, row-major,
+ *    densely packed. X is T x d_in, W_base is d_out x d_in (the nn.Linear
+ *    layout), Y is T x d_out. d_in and d_out must be multiples of 8 and
+ *    X, W_base, Y 16-byte aligned (any cudaMalloc / torch allocation is).
+ *  - Device pointers are CUDA device (or managed) memory of the pool's device.
+ *  - Every call returns a lora_status; a call that returns an error has
+ *    enqueued no GPU work and changed no pool state.
+ *  - A pool is not thread-safe: use it from one host thread at a time.
+ *  - Only GB300-class devices (compute capability 10.3) are supported; on any
+ *    other device lora_pool_create returns LORA_ERR_UNSUPPORTED. There is no
+ *    CPU fall-back.
+ */
+#ifndef LORA_LINEAR_H
+#define LORA_LINEAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LORA_ABI_VERSION 1
+
+/* Opaque pool handle: owns the adapter page arenas, the slot table and all
+ * scratch memory of the calls below. */
+typedef struct lora_pool lora_pool;
+typedef lora_pool *lora_pool_t;
+
+/* A cudaStream_t (the same type, declared without the CUDA headers).
+ * NULL means the legacy default stream. */
+typedef struct CUstream_st *lora_stream_t;
+
+typedef enum {
+    LORA_OK = 0,
+    LORA_ERR_ARG = 1,             /* null pointer, negative size, bad option   */
+    LORA_ERR_SHAPE = 2,           /* d_in / d_out not a positive multiple of 8,
+                                     or beyond the limits below               */
+    LORA_ERR_SLOT_RANGE = 3,      /* slot outside [0, max_adapters)            */
+    LORA_ERR_SLOT_OCCUPIED = 4,   /* load into a slot that holds an adapter    */
+    LORA_ERR_SLOT_EMPTY = 5,      /* unload of an empty slot                   */
+    LORA_ERR_RANK = 6,            /* rank outside [1, max_rank]                */
+    LORA_ERR_BAD_ADAPTER_ID = 7,  /* a token id was neither -1 nor a loaded slot
+                                     (reported by lora_pool_check_errors)      */
+    LORA_ERR_CUDA = 8,            /* a CUDA runtime call failed                */
+    LORA_ERR_OOM = 9,             /* device allocation failed                  */
+    LORA_ERR_TIMEOUT = 10,        /* a kernel's bounded wait ran out (reported
+                                     by lora_pool_check_errors)                */
+    LORA_ERR_UNSUPPORTED = 11     /* no compute-capability-10.3 device         */
+} lora_status;
+
+/* Limits. */
+#define LORA_MAX_ADAPTERS 4096    /* slots per pool                            */
+#define LORA_MAX_RANK 256         /* largest rank a pool can hold              */
+#define LORA_MAX_DIM 65536        /* largest d_in / d_out                      */
+#define LORA_RANK_PAGE 8          /* rank rows per pool page                   */
+
+/* Which kernel family lora_linear uses. AUTO picks DECODE for T <= 256 and
+ * PREFILL above; DECODE accepts T <= 256 only. Both compute the same result. */
+typedef enum { LORA_PATH_AUTO = 0, LORA_PATH_DECODE = 1, LORA_PATH_PREFILL = 2 } lora_path;
+
+/*
+ * Create a pool on the current CUDA device for one linear layer of shape
+ * d_in -> d_out, with room for max_adapters adapters of rank <= max_rank.
+ *
+ * The unified adapter pool of the vLLM tutorial ("vLLM 的 Multi-LoRA 怎么实现",
+ * item 1) and the LoRA-Land blog (技术方案: only the A,B matrices are added per
+ * adapter). Memory is paged at rank granularity: each page holds 8 rank rows
+ * of one adapter (8 columns of A, stored transposed as 8 x d_in, and 8 rows
+ * of B, stored interleaved as d_out x 8); an adapter of rank r holds ceil(r/8)
+ * pages taken from a free list. All page arenas, the slot table and the error
+ * word are allocated here, once: loading and unloading never allocate.
+ * Scratch for lora_linear is sized by lora_pool_reserve (or grown by the
+ * first call with a larger T).
+ *
+ * Returns LORA_ERR_SHAPE for bad dimensions, LORA_ERR_RANK for max_rank
+ * outside [1, LORA_MAX_RANK], LORA_ERR_ARG for max_adapters outside
+ * [1, LORA_MAX_ADAPTERS] or out == NULL, LORA_ERR_OOM if the arenas do not
+ * fit, LORA_ERR_UNSUPPORTED on a device that is not compute capability 10.3.
+ * On success *out owns everything; release it with lora_pool_destroy.
+ */
+lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out,
+                             lora_pool_t *out);
+
+/* Wait for the pool's in-flight work, then free all its device memory.
+ * The handle is invalid afterwards. NULL returns LORA_ERR_ARG. */
+lora_status lora_pool_destroy(lora_pool_t pool);
+
+/*
+ * Size the per-call scratch for batches of up to max_tokens tokens (segment
+ * tables, the fp32 low-rank intermediate, split-K partial sums, host-call
+ * staging). Calls with larger T grow it on first use, which allocates and
+ * synchronises the device: call this first when lora_linear will run inside a
+ * CUDA graph capture.
+ */
+lora_status lora_pool_reserve(lora_pool_t pool, int max_tokens);
+
+/*
+ * Load an adapter into an empty slot ("load_adapter" of the LoRA-Land blog,
+ * 热插拔 API: A,B are moved to the GPU and indexed; the vLLM tutorial's
+ * 动态上下线: adapters come and go without restarting).
+ *   A: bf16, d_in x rank, row-major.  B: bf16, rank x d_out, row-major.
+ *   Host or device pointers (detected); the data is copied into pool pages
+ *   and the caller keeps ownership (it may free A,B on return). Device data
+ *   must be complete before the call (no stream ordering is applied).
+ *   alpha: the adapter's scale numerator; the pool stores s = alpha / rank
+ *   (fp32), rank being the rank passed here.
+ * Host-blocking. Before touching pages or the slot table it waits for every
+ * lora_linear call already enqueued on this pool, so earlier calls see the
+ * old state. Loading into an occupied slot is an error: a hot swap is
+ * unload, then load.
+ * Errors: SLOT_RANGE, SLOT_OCCUPIED, RANK, ARG (null A/B), CUDA.
+ */
+lora_status lora_load_adapter(lora_pool_t pool, int slot, const void *A, const void *B,
+                              int rank, float alpha);
+
+/* Unload ("unload_adapter", same sections): waits for enqueued calls, returns
+ * the slot's pages to the free list and marks it empty. Host-blocking.
+ * Errors: SLOT_RANGE, SLOT_EMPTY. */
+lora_status lora_unload_adapter(lora_pool_t pool, int slot);
+
+/*
+ * The hot path. For every token t: Y[t] = X[t] W_base^T + s_i (X[t] A_i) B_i
+ * with i = token_adapter_ids[t]; id -1 gives the base product only (the vLLM
+ * tutorial's 按请求切换 LoRA: no adapter -> pure base). The batch is grouped
+ * by adapter with a stable sort ("Grouped Multi-LoRA Execution", LoRA-Land
+ * blog section 2); the low-rank intermediate X A_i is kept in fp32 and the
+ * result is rounded to bf16 once.
+ *   X: device bf16 T x d_in.  W_base: device bf16 d_out x d_in.
+ *   token_adapter_ids: device int32[T].  Y: device bf16 T x d_out (written
+ *   once; must not alias X or W_base).  T >= 0 (T == 0 does nothing).
+ * Asynchronous: enqueued on `stream`, returns without waiting. X, W_base and
+ * the ids must stay valid until the stream reaches the call.
+ * Ids that are neither -1 nor a loaded slot do not fall back silently (the
+ * icman.com.cn article's section 4.1, strict mode): the kernels set the
+ * pool's device error word, and the next lora_pool_check_errors returns
+ * LORA_ERR_BAD_ADAPTER_ID. Such rows of Y are unspecified; other rows stay
+ * correct.
+ * Errors returned at once: ARG (null pointers, T < 0, T > 256 with a forced
+ * DECODE path), OOM (scratch growth failed), CUDA.
+ */
+lora_status lora_linear(lora_pool_t pool, const void *X, const void *W_base,
+                        const int32_t *token_adapter_ids, int T, void *Y,
+                        lora_stream_t stream);
+
+/*
+ * Same as lora_linear, but X, token_adapter_ids and Y are HOST pointers
+ * (pinned memory gives full copy speed). The call copies X and the ids into
+ * pool-owned device staging on `stream`, runs the layer, copies Y back and
+ * waits for the stream before returning. W_base stays a device pointer (the
+ * resident base weight).
+ */
+lora_status lora_linear_host(lora_pool_t pool, const void *X_host, const void *W_base,
+                             const int32_t *ids_host, int T, void *Y_host,
+                             lora_stream_t stream);
+
+/*
+ * Base product only, Y = X W_base^T, with the same GEMM kernels lora_linear
+ * uses (the reference point the adapter overhead is measured against).
+ * Same pointer and stream rules as lora_linear.
+ */
+lora_status lora_base_linear(lora_pool_t pool, const void *X, const void *W_base, int T,
+                             void *Y, lora_stream_t stream);
+
+/*
+ * Wait for the pool's last enqueued call, read and clear the device error
+ * word. Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID or LORA_ERR_TIMEOUT (the
+ * first of these present), or LORA_ERR_CUDA if the device reported an error.
+ */
+lora_status lora_pool_check_errors(lora_pool_t pool);
+
+/*
+ * Test hook: run only the segment builder on device ids[T] and copy its
+ * tables out (device pointers): order[T] (token indices stably sorted by id,
+ * base-only tokens first), *n_base, *num_seg, seg_start[num_seg + 1] (offsets
+ * into order; seg_start[0] = n_base, seg_start[num_seg] = T) and
+ * seg_slot[num_seg] (ascending slot ids). seg_start and seg_slot must have
+ * room for min(T, max_adapters) + 1 entries. Ids that are neither -1 nor a
+ * loaded slot are grouped with the base-only tokens and set the error word.
+ */
+lora_status lora_build_segments(lora_pool_t pool, const int32_t *ids, int T, int32_t *order,
+                                int32_t *n_base, int32_t *num_seg, int32_t *seg_start,
+                                int32_t *seg_slot, lora_stream_t stream);
+
+/* Pool counters, written to out[0..LORA_STATS_COUNT):
+ * loaded slots, free pages, total pages, loads, unloads, linear calls,
+ * bytes of device memory held. */
+#define LORA_STATS_COUNT 7
+lora_status lora_pool_stats(lora_pool_t pool, int64_t *out);
+
+/* Force a kernel family (lora_path); LORA_PATH_AUTO restores the default. */
+lora_status lora_pool_set_path(lora_pool_t pool, int path);
+
+/* Static description of a status code. */
+const char *lora_status_string(lora_status status);
+
+/* LORA_ABI_VERSION of the built library. */
+int lora_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LORA_LINEAR_H */
