@@ -34,8 +34,10 @@ EXPORTS = (
     "lora_pool_create", "lora_pool_destroy", "lora_pool_reserve", "lora_load_adapter",
     "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
     "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
-    "lora_status_string", "lora_abi_version",
+    "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
 )
+LORA_KERNEL_SLOTS = 4
+KERNEL_SLOT_NAMES = ("segment_build", "shrink", "base_gemm", "finish_expand")
 
 
 class LibraryMissing(RuntimeError):
@@ -76,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_pool_set_path": [vp, i32],
         "lora_status_string": [i32],
         "lora_abi_version": [],
+        "lora_pool_enable_timing": [vp, i32],
+        "lora_pool_kernel_times": [vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -171,6 +175,18 @@ def lora_pool_set_path(pool: int, path: int) -> int:
     return load_library().lora_pool_set_path(pool, path)
 
 
+def lora_pool_enable_timing(pool: int, enable: bool) -> int:
+    return load_library().lora_pool_enable_timing(pool, int(bool(enable)))
+
+
+def lora_pool_kernel_times(pool: int) -> Dict[str, float]:
+    """Device milliseconds of each kernel of the pool's last call (timing must be enabled)."""
+    out = (ctypes.c_float * LORA_KERNEL_SLOTS)()
+    _check(load_library().lora_pool_kernel_times(pool, ctypes.cast(out, ctypes.c_void_p)),
+           "lora_pool_kernel_times")
+    return dict(zip(KERNEL_SLOT_NAMES, list(out)))
+
+
 def lora_status_string(status: int) -> str:
     return load_library().lora_status_string(status).decode()
 
@@ -258,3 +274,9 @@ class LoraPool:
 
     def stats(self) -> Dict[str, int]:
         return lora_pool_stats(self.handle)
+
+    def enable_timing(self, enable: bool = True):
+        _check(lora_pool_enable_timing(self.handle, enable), "lora_pool_enable_timing")
+
+    def kernel_times(self) -> Dict[str, float]:
+        return lora_pool_kernel_times(self.handle)

@@ -300,6 +300,21 @@ __device__ __forceinline__ void tmem_ld32_wait(uint32_t taddr, uint32_t (&r)[32]
         : "memory");
 }
 
+// ----------------------------------------------------------- named barriers
+
+// Barrier `id` (1..15) over `count` threads (a multiple of 32); the calling
+// warps wait.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Arrive on barrier `id` without waiting for the others.
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ------------------------------------------------ programmatic dependent launch
 
 // Let the next kernel in the stream start its prologue now.

@@ -1,25 +1,32 @@
-// gemm_decode.cu -- base product for decode batches (T <= 256) and the
-// finishing pass that adds the low-rank branch.
+// gemm_decode.cu -- the decode path (T <= 256): two kernels.
 //
-// At decode sizes the base GEMM is bound by reading W_base once from HBM, so
-// the layout is chosen to stream W at full bandwidth on every SM:
-//  * operands swapped: D[n, t] = sum_k W[n,k] X[t,k], so the long d_out side
-//    is the MMA's M (128 rows of W per tile) and the T tokens are its N
-//    (T rounded up to 16; rows past T read as zero from TMA);
-//  * stream-K: the (tile, 64-wide k-block) iteration space is cut into G equal
-//    contiguous ranges, one per CTA (G = number of SMs, or fewer for small
-//    problems), so every SM streams the same share of W. A range touches at
-//    most two tiles; each touched tile gets its own TMEM accumulator and is
-//    written as an fp32 partial sum [cta][0|1][T][128].
-//  * warp roles: warp 4 issues TMA loads (W tile 128x64, X tile T'x64, 128-byte
-//    swizzle) into a multi-stage ring; warp 5 issues tcgen05 MMAs
-//    (M=128, N=T', K=16) into TMEM; warps 0-3 read the accumulators back with
-//    tcgen05.ld (TMEM lane = output row n) and store the partials.
-// finish_decode_kernel then adds, per output element, the partials of the
-// CTAs that covered its tile in CTA order (deterministic), plus the low-rank
-// branch s_i V[t,:] B_i[:,n] (V already carries s_i) read from the
-// interleaved B pages (one 16-byte load = 8 rank rows of one column), and
-// rounds once to bf16 (round to nearest even).
+// 1. gemm_decode_kernel: base product + the per-token low-rank shrink.
+//    At decode sizes the base GEMM is bound by reading W_base once from HBM, so
+//    the layout is chosen to stream W at full bandwidth on every SM:
+//    * operands swapped: D[n, t] = sum_k W[n,k] X[t,k], so the long d_out side
+//      is the MMA's M (128 rows of W per tile) and the T tokens are its N
+//      (T rounded up to 16; rows past T read as zero from TMA);
+//    * stream-K: the (tile, 64-wide k-block) iteration space is cut into G
+//      equal contiguous ranges, one per CTA (G = number of SMs, or fewer for
+//      small problems), so every SM streams the same share of W. A range
+//      touches at most two tiles; each touched tile gets its own TMEM
+//      accumulator and is written as an fp32 partial sum [cta][0|1][T][128];
+//    * warp roles: warp 4 issues TMA loads (W tile 128x64, X tile T'x64,
+//      128-byte swizzle) into a multi-stage ring and starts before TMEM is
+//      allocated; warp 5 allocates TMEM and issues tcgen05 MMAs (M=128, N=T',
+//      K=16); warps 0-3, idle until the accumulators are ready, first compute
+//      the low-rank shrink V[t, 8q..8q+7] = s_i X[t,:] A_i[:, 8q..8q+7] for
+//      the (token, page) pairs dealt to this CTA round-robin (a BGMV-style
+//      per-token gather: each pair reads one 8 x d_in A page with 128-bit
+//      loads), so the adapter reads overlap the W stream; then they read the
+//      accumulators back with tcgen05.ld (TMEM lane = output row n) and store
+//      the partials.
+// 2. finish_decode_kernel (launched with programmatic stream serialization, so
+//    it is resident and has prefetched its B pages before the GEMM ends): per
+//    output element, the partials of the CTAs that covered its tile are summed
+//    in CTA order (deterministic), the low-rank expand s_i V[t,:] B_i[:,n] is
+//    added from the interleaved B pages (one 16-byte load = 8 rank rows of one
+//    column; V already carries s_i), and the sum is rounded once to bf16.
 #include "device_common.cuh"
 
 namespace lora {
@@ -28,15 +35,61 @@ namespace {
 
 constexpr int kThreads = 192;
 constexpr int kWTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr uint32_t kBarSetup = 1;       // named barrier: all six warps, setup done
+constexpr uint32_t kBarShrink = 2;      // named barrier: the four epilogue warps
 
 __host__ __device__ __forceinline__ int cta_start(int c, int U, int G)
 {
     return (int)(((long long)c * U) / G);
 }
 
+struct ShrinkArgs {
+    const uint16_t *X;
+    const int32_t *ids;  // nullptr: base product only
+    float *V;
+    int ldv;
+};
+
+// One (token, page) pair of the shrink, computed by the 128 threads of warps 0-3.
+__device__ __forceinline__ void shrink_pair(int t, int page, float scale, const PoolDev &pool,
+                                            const ShrinkArgs &sa, int q, float (*red)[8])
+{
+    const int tid = threadIdx.x;  // 0..127
+    const int warp = tid >> 5, lane = tid & 31;
+    const int d_in = pool.d_in;
+    const uint16_t *Ap = pool.A_pages + (size_t)page * kRankPage * d_in;
+    const uint16_t *xr = sa.X + (size_t)t * d_in;
+    float acc[kRankPage];
+#pragma unroll
+    for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = 0.f;
+#pragma unroll 2
+    for (int c = tid; c < d_in / 8; c += 128) {
+        const uint4 x = ldg_nc_v4(xr + c * 8);
+        uint4 a[kRankPage];
+#pragma unroll
+        for (int jj = 0; jj < kRankPage; ++jj) a[jj] = ldg_nc_v4(Ap + (size_t)jj * d_in + c * 8);
+#pragma unroll
+        for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = dot8_bf16(x, a[jj], acc[jj]);
+    }
+#pragma unroll
+    for (int jj = 0; jj < kRankPage; ++jj)
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
+    if (lane == 0)
+#pragma unroll
+        for (int jj = 0; jj < kRankPage; ++jj) red[warp][jj] = acc[jj];
+    named_bar_sync(kBarShrink, 128);
+    if (tid < kRankPage) {
+        const float s = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
+        sa.V[(size_t)t * sa.ldv + q * kRankPage + tid] = scale * s;
+    }
+    named_bar_sync(kBarShrink, 128);
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       DecodePlan p, float *__restrict__ partials, int *err)
+                       DecodePlan p, float *__restrict__ partials, int *err, PoolDev pool,
+                       ShrinkArgs sa)
 {
     extern __shared__ uint8_t dec_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -50,6 +103,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t *drain = acc_full + 2;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     __shared__ int abort_flag;
+    __shared__ float red[4][kRankPage];
+
+    // the finishing kernel may start its independent prologue now
+    pdl_launch_dependents();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -57,32 +114,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tile0 = u0 / p.KB;
     const int nseg = (u1 > u0) ? (u1 - 1) / p.KB - tile0 + 1 : 0;
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < stages; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
-        }
-        mbar_init(&acc_full[0], 1);
-        mbar_init(&acc_full[1], 1);
-        mbar_init(drain, 1);
-        abort_flag = 0;
-        fence_mbar_init();
-    }
-    if (warp == 5) {
-        tmem_alloc(tmem_slot, p.tmem_cols);
-        tmem_relinquish();
-    }
-    if (warp == 4 && lane == 0) {
-        tma_prefetch_map(&tmW);
-        tma_prefetch_map(&tmX);
-    }
-    tc_fence_before_sync();
-    __syncthreads();
-    tc_fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-
     if (warp == 4) {
         // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            for (int i = 0; i < stages; ++i) {
+                mbar_init(&full[i], 1);
+                mbar_init(&empty[i], 1);
+            }
+            mbar_init(&acc_full[0], 1);
+            mbar_init(&acc_full[1], 1);
+            mbar_init(drain, 1);
+            abort_flag = 0;
+            fence_mbar_init();
+            tma_prefetch_map(&tmW);
+            tma_prefetch_map(&tmX);
+        }
+        __syncwarp();
+        named_bar_arrive(kBarSetup, kThreads);  // barriers are ready; do not wait for TMEM
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();  // W is read exactly once
             int it = 0;
@@ -104,6 +152,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+        named_bar_sync(kBarSetup, kThreads);
+        tc_fence_after_sync();
+        const uint32_t tmem = *tmem_slot;
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, p.ntok);
             int it = 0;
@@ -130,7 +184,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
     } else {
-        // ------------------------------------------------------------ epilogue
+        // ------------------------------------- warps 0-3: shrink, then epilogue
+        named_bar_sync(kBarSetup, kThreads);
+        tc_fence_after_sync();
+        const uint32_t tmem = *tmem_slot;
+        if (sa.ids != nullptr) {
+            const int pairs = p.T * pool.max_pages;
+            for (int u = c; u < pairs; u += p.G) {
+                const int t = u / pool.max_pages, q = u - t * pool.max_pages;
+                const int id = sa.ids[t];
+                if (!slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) continue;
+                const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+                if (q >= row[SLOT_NPAGES]) continue;
+                shrink_pair(t, row[SLOT_PAGES + q], __int_as_float(row[SLOT_SCALE]), pool, sa, q,
+                            red);
+            }
+        }
         for (int seg = 0; seg < nseg; ++seg) {
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[seg], 0, &abort_flag, err);
@@ -152,54 +221,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (warp == 5) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem, p.tmem_cols);
+        tmem_dealloc(*tmem_slot, p.tmem_cols);
     }
 }
 
 constexpr int kFinishThreads = 256;  // one thread per output column
-constexpr int kFinishTokens = 4;     // tokens per CTA
+constexpr int kPrefetchPages = 8;    // B pages fetched before the GEMM has finished
 
 __global__ void __launch_bounds__(kFinishThreads)
     finish_decode_kernel(DecodePlan p, const float *__restrict__ partials,
                          const int32_t *__restrict__ ids, PoolDev pool, const float *__restrict__ V,
-                         int ldv, uint16_t *__restrict__ Y)
+                         int ldv, uint16_t *__restrict__ Y, int *err)
 {
     const int n = blockIdx.x * kFinishThreads + threadIdx.x;
-    if (n >= pool.d_out) return;
+    const int t = blockIdx.y;
+    const bool col_ok = n < pool.d_out;
+
+    // ---- independent of the GEMM kernel: adapter of this token, its B values
+    int np = 0;
+    const int32_t *pages = nullptr;
+    uint4 b[kPrefetchPages];
+    if (ids != nullptr) {
+        const int id = ids[t];
+        if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+            const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+            np = row[SLOT_NPAGES];
+            pages = row + SLOT_PAGES;
+        } else if (id != -1 && threadIdx.x == 0 && blockIdx.x == 0) {
+            atomicOr(err, kErrBadIdBit);  // strict: never a silent base fall-back
+        }
+    }
+    if (col_ok) {
+#pragma unroll
+        for (int q = 0; q < kPrefetchPages; ++q)
+            if (q < np) b[q] = ldg_nc_v4(pool.B_pages + ((size_t)pages[q] * pool.d_out + n) * kRankPage);
+    }
     const int tile = n >> 7, nl = n & 127;
     const int kb_lo = tile * p.KB, kb_hi = kb_lo + p.KB;
-    // first CTA whose range contains kb_lo
+    // contributors of this tile: CTAs c_lo..c_hi (contiguous k-ranges); only c_lo can
+    // have started in the previous tile, in which case its partial for this tile is
+    // its second one
     int c_lo = (int)(((long long)kb_lo * p.G) / p.U);
     while (c_lo > 0 && cta_start(c_lo, p.U, p.G) > kb_lo) --c_lo;
     while (cta_start(c_lo + 1, p.U, p.G) <= kb_lo) ++c_lo;
+    int c_hi = c_lo;
+    while (c_hi + 1 < p.G && cta_start(c_hi + 1, p.U, p.G) < kb_hi) ++c_hi;
+    const int seg_lo = cta_start(c_lo, p.U, p.G) < kb_lo ? 1 : 0;
 
-    const int t_begin = blockIdx.y * kFinishTokens;
-    const int t_end = min(p.T, t_begin + kFinishTokens);
-    for (int t = t_begin; t < t_end; ++t) {
-        float acc = 0.f;
-        for (int c = c_lo; c < p.G && cta_start(c, p.U, p.G) < kb_hi; ++c) {
-            const int seg = (cta_start(c, p.U, p.G) / p.KB == tile) ? 0 : 1;
-            acc += partials[((size_t)(c * 2 + seg) * p.T + t) * 128 + nl];
+    // ---- partials and V are written by the GEMM kernel
+    pdl_wait_prior();
+    if (!col_ok) return;
+
+    float acc = partials[((size_t)(c_lo * 2 + seg_lo) * p.T + t) * 128 + nl];
+    for (int c = c_lo + 1; c <= c_hi; ++c) acc += partials[((size_t)(c * 2) * p.T + t) * 128 + nl];
+    const float *vrow = V + (size_t)t * ldv;
+    for (int q = 0; q < np; ++q) {
+        const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
+        const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
+        const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        uint4 bq;
+        if (q < kPrefetchPages) {
+#pragma unroll
+            for (int i = 0; i < kPrefetchPages; ++i)
+                if (i == q) bq = b[i];
+        } else {
+            bq = ldg_nc_v4(pool.B_pages + ((size_t)pages[q] * pool.d_out + n) * kRankPage);
         }
-        if (ids != nullptr) {
-            const int id = ids[t];
-            if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
-                const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
-                const int np = row[SLOT_NPAGES];
-                const float *vrow = V + (size_t)t * ldv;
-                for (int q = 0; q < np; ++q) {
-                    const int page = row[SLOT_PAGES + q];
-                    const uint4 b = ldg_nc_v4(pool.B_pages + ((size_t)page * pool.d_out + n) * kRankPage);
-                    const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
-                    const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
-                    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-                    acc = dot8_f32_bf16(vv, b, acc);
-                }
-            }
-        }
-        __nv_bfloat16 h = __float2bfloat16_rn(acc);
-        Y[(size_t)t * pool.d_out + n] = *reinterpret_cast<uint16_t *>(&h);
+        acc = dot8_f32_bf16(vv, bq, acc);
     }
+    __nv_bfloat16 h = __float2bfloat16_rn(acc);
+    Y[(size_t)t * pool.d_out + n] = *reinterpret_cast<uint16_t *>(&h);
 }
 
 uint32_t pow2_cols(uint32_t n)
@@ -237,26 +328,33 @@ DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms)
 size_t decode_partials_floats(const DecodePlan &p) { return (size_t)p.G * 2 * p.T * 128; }
 
 cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
-                               const DecodePlan &plan, int d_out, float *partials, int *err,
+                               const DecodePlan &plan, const PoolDev &pool, const uint16_t *X,
+                               const int32_t *ids, float *V, int ldv, float *partials, int *err,
                                cudaStream_t stream)
 {
-    (void)d_out;
-    cudaError_t e = cudaFuncSetAttribute(gemm_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)plan.smem_bytes);
+    cudaError_t e = ensure_smem_attr((const void *)gemm_decode_kernel, plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    gemm_decode_kernel<<<plan.G, kThreads, plan.smem_bytes, stream>>>(tmW, tmX, plan, partials, err);
+    ShrinkArgs sa{X, ids, V, ldv};
+    gemm_decode_kernel<<<plan.G, kThreads, plan.smem_bytes, stream>>>(tmW, tmX, plan, partials, err,
+                                                                      pool, sa);
     return cudaGetLastError();
 }
 
 cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
                                  const int32_t *ids, const PoolDev &pool, const float *V,
-                                 int ldv, uint16_t *Y, cudaStream_t stream)
+                                 int ldv, uint16_t *Y, int *err, cudaStream_t stream)
 {
-    dim3 grid((pool.d_out + kFinishThreads - 1) / kFinishThreads,
-              (plan.T + kFinishTokens - 1) / kFinishTokens);
-    finish_decode_kernel<<<grid, kFinishThreads, 0, stream>>>(plan, partials, ids, pool, V, ldv, Y);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((pool.d_out + kFinishThreads - 1) / kFinishThreads, plan.T);
+    cfg.blockDim = dim3(kFinishThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finish_decode_kernel, plan, partials, ids, pool, V, ldv, Y, err);
 }
 
 }  // namespace lora

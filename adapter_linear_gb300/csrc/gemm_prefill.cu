@@ -253,8 +253,7 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, 
     a.err = err;
     if (a.num_tiles == 0) return cudaSuccess;
     const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16;
-    cudaError_t e = cudaFuncSetAttribute(gemm_prefill_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_attr((const void *)gemm_prefill_kernel, smem);
     if (e != cudaSuccess) return e;
     const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
     gemm_prefill_kernel<<<grid, kThreads, smem, stream>>>(tmX, tmW, a, pool);

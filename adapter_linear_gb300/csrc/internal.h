@@ -79,13 +79,16 @@ struct DecodePlan {
 };
 DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms);
 size_t decode_partials_floats(const DecodePlan &p);
+// Base product (stream-K partials) + the per-token shrink V (ids == nullptr: no shrink).
 cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
-                               const DecodePlan &plan, int d_out, float *partials, int *err,
+                               const DecodePlan &plan, const PoolDev &pool, const uint16_t *X,
+                               const int32_t *ids, float *V, int ldv, float *partials, int *err,
                                cudaStream_t stream);
 // Y = bf16(sum of split-K partials + s_i V[t] B_i); ids == nullptr: no branch.
+// Launched with programmatic stream serialization after launch_gemm_decode.
 cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
                                  const int32_t *ids, const PoolDev &pool, const float *V,
-                                 int ldv, uint16_t *Y, cudaStream_t stream);
+                                 int ldv, uint16_t *Y, int *err, cudaStream_t stream);
 
 cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, int T,
                                 const int32_t *ids, const PoolDev &pool, const float *V, int ldv,
@@ -95,6 +98,11 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, 
 cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,
                                 int npages, const PoolDev &pool, uint16_t *A_pages,
                                 uint16_t *B_pages, cudaStream_t stream);
+
+// Host: raise a kernel's dynamic shared-memory limit to at least `bytes` on the
+// current device (remembered per kernel and device, so repeated launches do
+// not repeat the driver call).
+cudaError_t ensure_smem_attr(const void *kernel, size_t bytes);
 
 // Host: build a 2-D bf16 TMA descriptor with 128-byte swizzle over a row-major
 // [rows x inner] tensor, box [box_rows x box_inner].

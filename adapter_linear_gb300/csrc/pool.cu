@@ -61,6 +61,10 @@ struct lora_pool {
     int tmap_next = 0;
 
     int path = LORA_PATH_AUTO;
+    bool timing = false;
+    cudaEvent_t ev[LORA_KERNEL_SLOTS + 1] = {};
+    bool ev_used[LORA_KERNEL_SLOTS] = {};
+    int ev_last = 0;  // index of the last event the last timed call recorded
     int64_t n_loads = 0, n_unloads = 0, n_calls = 0;
     size_t bytes_held = 0;
 };
@@ -227,29 +231,48 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
 
     const PoolDev pd = pool_view(p);
     const SegTables tabs = seg_tables(p);
+    // measurement hook: event k+1 closes kernel slot k
+    for (bool &u : p->ev_used) u = false;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    if (p->timing && cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return LORA_ERR_CUDA;
+    auto mark = [&](int slot) -> bool {
+        if (!p->timing) return true;
+        if (slot >= 0) p->ev_used[slot] = true;
+        p->ev_last = slot + 1;
+        // inside a graph capture the records become event nodes replayed with the graph
+        const unsigned flags =
+            capture == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+        return cudaEventRecordWithFlags(p->ev[slot + 1], stream, flags) == cudaSuccess;
+    };
+    if (!mark(-1)) return LORA_ERR_CUDA;
     const uint16_t *Xb = static_cast<const uint16_t *>(X);
     uint16_t *Yb = static_cast<uint16_t *>(Y);
 
-    if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
-
     if (path == LORA_PATH_DECODE) {
+        // per-token (BGMV-style) shrink fused into the GEMM kernel: no segment tables
         const DecodePlan plan = plan_decode(T, p->d_in, p->d_out, p->num_sms);
         const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 128);
         const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, plan.ntok);
         if (!tmW || !tmX) return LORA_ERR_ARG;
-        if (with_lora) CUDA_TRY(launch_shrink_simt(Xb, T, pd, tabs, p->V, p->ldv, stream));
-        CUDA_TRY(launch_gemm_decode(*tmW, *tmX, plan, p->d_out, p->partials, p->d_err, stream));
+        CUDA_TRY(launch_gemm_decode(*tmW, *tmX, plan, pd, Xb, with_lora ? ids : nullptr, p->V,
+                                    p->ldv, p->partials, p->d_err, stream));
+        if (!mark(2)) return LORA_ERR_CUDA;
         CUDA_TRY(launch_finish_decode(plan, p->partials, with_lora ? ids : nullptr, pd, p->V,
-                                      p->ldv, Yb, stream));
+                                      p->ldv, Yb, p->d_err, stream));
+        if (!mark(3)) return LORA_ERR_CUDA;
     } else {
+        if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
+        if (!mark(0)) return LORA_ERR_CUDA;
         const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, 128);
         const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 256);
         if (!tmW || !tmX) return LORA_ERR_ARG;
         if (with_lora)
             CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, Xb, T, pd, tabs, p->V, p->ldv, p->num_sms,
                                       p->d_err, stream));
+        if (!mark(1)) return LORA_ERR_CUDA;
         CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, T, with_lora ? ids : nullptr, pd, p->V, p->ldv,
                                      Yb, p->num_sms, p->d_err, stream));
+        if (!mark(2)) return LORA_ERR_CUDA;
     }
     p->n_calls += 1;
     return LORA_OK;
@@ -357,6 +380,8 @@ lora_status lora_pool_destroy(lora_pool_t p)
     free_dev(p, p->stage_B, 0);
     free_dev(p, p->d_page_list, 0);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    for (auto &e : p->ev)
+        if (e) cudaEventDestroy(e);
     delete p;
     return LORA_OK;
 }
@@ -529,6 +554,34 @@ lora_status lora_pool_stats(lora_pool_t p, int64_t *out)
     return LORA_OK;
 }
 
+lora_status lora_pool_enable_timing(lora_pool_t p, int enable)
+{
+    if (!p) return LORA_ERR_ARG;
+    if (enable && !p->ev[0]) {
+        for (auto &e : p->ev) CUDA_TRY(cudaEventCreate(&e));
+    }
+    p->timing = enable != 0;
+    return LORA_OK;
+}
+
+lora_status lora_pool_kernel_times(lora_pool_t p, float *ms)
+{
+    if (!p || !ms) return LORA_ERR_ARG;
+    for (int k = 0; k < LORA_KERNEL_SLOTS; ++k) ms[k] = 0.f;
+    if (!p->ev[0]) return LORA_OK;
+    CUDA_TRY(cudaEventSynchronize(p->ev[p->ev_last]));
+    // slots are contiguous in launch order; an unused slot has no event of its own
+    int prev = 0;
+    for (int k = 0; k < LORA_KERNEL_SLOTS; ++k) {
+        if (!p->ev_used[k]) continue;
+        float t = 0.f;
+        CUDA_TRY(cudaEventElapsedTime(&t, p->ev[prev], p->ev[k + 1]));
+        ms[k] = t;
+        prev = k + 1;
+    }
+    return LORA_OK;
+}
+
 lora_status lora_pool_set_path(lora_pool_t p, int path)
 {
     if (!p || path < LORA_PATH_AUTO || path > LORA_PATH_PREFILL) return LORA_ERR_ARG;
@@ -551,6 +604,31 @@ cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, 
     pack_adapter_kernel<<<grid, 256, 0, stream>>>(A, B, rank, pages, npages, pool.d_in, pool.d_out,
                                                   A_pages, B_pages);
     return cudaGetLastError();
+}
+
+cudaError_t ensure_smem_attr(const void *kernel, size_t bytes)
+{
+    struct Entry {
+        const void *kernel;
+        int device;
+        size_t bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    for (Entry &x : done)
+        if (x.kernel == kernel && x.device == dev) {
+            if (x.bytes >= bytes) return cudaSuccess;
+            e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+            if (e == cudaSuccess) x.bytes = bytes;
+            return e;
+        }
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
+    return e;
 }
 
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,

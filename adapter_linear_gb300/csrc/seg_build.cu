@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kSegThreads = 256;
 constexpr int kSegWarps = kSegThreads / 32;
+constexpr size_t kSegSmemLimit = 200 * 1024;
 
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
@@ -39,30 +40,34 @@ __device__ __forceinline__ int token_key(int id, const PoolDev &pool, bool &bad)
 
 __global__ void __launch_bounds__(kSegThreads, 1)
     seg_build_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
-                     int *__restrict__ err)
+                     int *__restrict__ err, int cache_keys)
 {
     extern __shared__ uint32_t seg_smem[];
     const int K = pool.max_adapters + 1;
     uint32_t *cnt = seg_smem;                          // [K][kSegWarps]
     uint32_t *koff = seg_smem + (size_t)K * kSegWarps;  // [K]
+    int *keys = reinterpret_cast<int *>(koff + K);      // [T] when cache_keys
     __shared__ uint32_t warp_tot[3][kSegWarps];
     __shared__ int any_bad;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < K * kSegWarps; i += kSegThreads) cnt[i] = 0;
     if (tid == 0) any_bad = 0;
+    bool bad = false;
+    // keys computed once, by all threads in parallel (independent loads), when they fit
+    if (cache_keys)
+        for (int t = tid; t < T; t += kSegThreads) keys[t] = token_key(ids[t], pool, bad);
     __syncthreads();
 
     const int chunk = (T + kSegWarps - 1) / kSegWarps;
     const int t0 = min(T, warp * chunk), t1 = min(T, t0 + chunk);
 
     // ---- A: per-warp counts
-    bool bad = false;
     for (int base = t0; base < t1; base += 32) {
         const int t = base + lane;
         const bool valid = t < t1;
         int key = 0;
-        if (valid) key = token_key(ids[t], pool, bad);
+        if (valid) key = cache_keys ? keys[t] : token_key(ids[t], pool, bad);
         const unsigned active = __ballot_sync(0xffffffffu, valid);
         if (valid) {
             const unsigned same = __match_any_sync(active, key);
@@ -155,7 +160,7 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         const bool valid = t < t1;
         bool unused = false;
         int key = 0;
-        if (valid) key = token_key(ids[t], pool, unused);
+        if (valid) key = cache_keys ? keys[t] : token_key(ids[t], pool, unused);
         const unsigned active = __ballot_sync(0xffffffffu, valid);
         if (valid) {
             const unsigned same = __match_any_sync(active, key);
@@ -180,16 +185,12 @@ size_t seg_build_smem_bytes(int max_adapters)
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
                              int *err, cudaStream_t stream)
 {
-    const size_t smem = seg_build_smem_bytes(pool.max_adapters);
-    static bool configured = false;
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(seg_build_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)seg_build_smem_bytes(4096));
-        if (e != cudaSuccess) return e;
-        configured = true;
-    }
-    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(ids, T, pool, tabs, err);
+    size_t smem = seg_build_smem_bytes(pool.max_adapters);
+    const int cache_keys = smem + (size_t)T * sizeof(int) <= kSegSmemLimit;
+    if (cache_keys) smem += (size_t)T * sizeof(int);
+    cudaError_t e = ensure_smem_attr((const void *)seg_build_kernel, smem);
+    if (e != cudaSuccess) return e;
+    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(ids, T, pool, tabs, err, cache_keys);
     return cudaGetLastError();
 }
 

@@ -354,8 +354,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, con
     const int max_units = (T + kShrinkRows - 1) / kShrinkRows + max_seg;
     int grid = max_units < num_sms ? max_units : num_sms;
     if (grid <= 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(shrink_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
     shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, X, pool, tabs, V, ldv, nmax,
                                                           stages, tmem_cols, err);

@@ -1,0 +1,507 @@
+"""Benchmark of the heterogeneous multi-LoRA linear layer on GB300.
+
+One step = one lora_linear call (segment build, shrink, base GEMM, expand)
+over one batch of the Llama-2-7B q_proj decode workload: T=64 tokens,
+d_in=d_out=4096, 200 resident rank-16 adapters (alpha 32), ids uniform over
+0..199, synthetic seeded bf16 data. Inputs are resident in HBM when the timed
+region starts; L2 is flushed (a 2x-L2 buffer write, outside the events)
+before every timed step, so every step reads W and the adapters from HBM.
+
+Prints ONE JSON line (rank 0). value = tokens/s over all ranks; e2e = the
+same metric through lora_linear_host (pinned host X/ids in, host Y out,
+copies and the final sync inside the measured time); roofline = the
+dominant kernel (the base GEMM) against the measured HBM copy bandwidth;
+cpu_baseline = the fp64 CPU oracle on a bounded sample of the same workload.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   (the oracle as the reference arm)
+Multi-GPU (torchrun, one rank per GPU): replicas, no data-path collective.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import lora_inputs as L  # noqa: E402
+
+METRIC = ("LoRA-linear tokens/s, overhead vs base-only GEMM, adapter-path HBM GB/s "
+          "(1×GB300)")
+UNIT = "tokens/s"
+GEMM_SRC = os.path.join(ROOT, "adapter_linear_gb300", "csrc", "gemm_decode.cu")
+PROFILE = os.path.join(ROOT, "profiles", "gemm_decode_q_proj_T64.md")
+
+
+# ----------------------------------------------------------------- workloads
+
+def workload(name: str):
+    if name == "q_proj_decode":
+        p = L.q_proj_decode()
+        return p, {"workload": "Llama-2-7B q_proj decode", "T": 64, "d_in": 4096, "d_out": 4096,
+                   "adapters": 200, "rank": 16, "alpha": 32, "ids": "uniform 0..199"}
+    if name == "hotswap_T256":
+        p, _ = L.hotswap()
+        return p, {"workload": "q_proj decode, 2000 paged adapters, Zipf ids", "T": 256,
+                   "d_in": 4096, "d_out": 4096, "adapters": 2000, "rank": 16}
+    if name == "prefill_mixed":
+        p = L.prefill_mixed()
+        return p, {"workload": "gate_proj prefill, 8x2048 tokens, ranks 8..64", "T": 16384,
+                   "d_in": 4096, "d_out": 14336, "adapters": 8, "rank": "8,8,16,16,32,32,64,64"}
+    if name.startswith("llama3_"):
+        mod = name[len("llama3_"):]
+        (p,) = L.llama3_7mod(modules=[mod])
+        return p, {"workload": f"Llama-3-8B {mod} decode", "T": 32, "d_in": p.d_in,
+                   "d_out": p.d_out, "adapters": 32, "rank": 16}
+    if name == "tiny":
+        p = L.tiny()
+        return p, {"workload": "tiny", "T": 64, "d_in": 256, "d_out": 256, "adapters": 4, "rank": 8}
+    raise SystemExit(f"unknown workload {name}")
+
+
+def algorithmic_bytes(p):
+    """Bytes the layer must move once: X, W, Y, ids and the distinct adapters' A and B."""
+    T = p.T
+    distinct = set(int(i) for i in p.ids if i >= 0)
+    ad_bytes = sum(p.adapters[i].rank * (p.d_in + p.d_out) * 2 for i in distinct)
+    return {
+        "x": T * p.d_in * 2, "w": p.d_out * p.d_in * 2, "y": T * p.d_out * 2, "ids": T * 4,
+        "adapters": ad_bytes,
+        "adapter_A": sum(p.adapters[i].rank * p.d_in * 2 for i in distinct),
+        "adapter_B": sum(p.adapters[i].rank * p.d_out * 2 for i in distinct),
+    }
+
+
+def algorithmic_flops(p):
+    lora = sum(2 * p.adapters[int(i)].rank * (p.d_in + p.d_out) for i in p.ids if i >= 0)
+    return 2 * p.T * p.d_in * p.d_out + lora
+
+
+# ------------------------------------------------------------------- clocks
+
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (read-only queries) every
+    millisecond while the timed region runs."""
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import ctypes
+        self.ok = False
+        self.samples = []
+        self.max_mhz = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                return
+            import torch
+            props = torch.cuda.get_device_properties(torch_device)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+                return
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                self.max_mhz = float(mx.value)
+            self.reason_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                nv.nvmlDeviceGetCurrentClocksThrottleReasons
+            self.nv, self.h, self.ctypes = nv, h, ctypes
+            self.ok = True
+        except (OSError, AttributeError, ImportError):
+            self.ok = False
+
+    def _run(self):
+        c = self.ctypes
+        mhz, reasons = c.c_uint(), c.c_ulonglong()
+        while not self.stop:
+            if self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) == 0 and \
+                    self.reason_fn(self.h, c.byref(reasons)) == 0:
+                self.samples.append((float(mhz.value), int(reasons.value)))
+            time.sleep(0.001)
+
+    def __enter__(self):
+        if self.ok:
+            self.stop = False
+            self.thread = threading.Thread(target=self._run, daemon=True)
+            self.thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        if self.ok:
+            self.stop = True
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.samples:
+            return None
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items()
+                          if r & bit})
+        return {"sm_mhz": statistics.median(s for s, _ in self.samples),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml"}
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = float(f[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- profile data
+
+def source_digest(path=GEMM_SRC) -> str:
+    h = hashlib.sha256()
+    for f in (path, os.path.join(os.path.dirname(path), "device_common.cuh")):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the base GEMM from the committed ncu summary, if it was
+    taken on the current kernel source (else None)."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if not m_src or not m_bytes or m_src.group(1) != source_digest():
+        return None
+    return float(m_bytes.group(1))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return d.get("hbm_gbs"), d.get("bf16_tflops"), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# --------------------------------------------------------------- cpu oracle
+
+def cpu_oracle_rate(p, seconds: float, max_tokens: int):
+    """tokens/s of the fp64 oracle on the first `n` tokens of the batch, repeated until
+    `seconds` of wall time."""
+    import oracle
+    ads = oracle.problem_adapters(p)
+    n = min(max_tokens, p.T)
+    X, ids = p.X[:n], p.ids[:n]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        oracle.lora_linear(X, p.W, ids, ads, p.max_adapters)
+        done += n
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return done / el, oracle.num_threads(), f"{n} of {p.T} tokens per pass, {done} tokens in {el:.1f} s"
+
+
+# --------------------------------------------------------------------- main
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    p, cfg = workload(args.workload)
+    import oracle
+    ads = oracle.problem_adapters(p)
+    n = min(args.ref_tokens, p.T)
+    X, ids = p.X[:n], p.ids[:n]
+    for _ in range(args.warmup):
+        oracle.lora_linear(X, p.W, ids, ads, p.max_adapters)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.lora_linear(X, p.W, ids, ads, p.max_adapters)
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    cores = oracle.num_threads()
+    cfg = dict(cfg, sample=f"{n} of {p.T} tokens per step")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": cfg,
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {p.T} tokens per step, {args.steps} steps"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="q_proj_decode")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-tokens", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="launch the kernels directly instead of replaying a captured CUDA graph")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import adapter_linear_gb300 as al
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+
+    p, cfg = workload(args.workload)
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
+    for slot, ad in p.adapters.items():
+        pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
+    pool.reserve(p.T)
+    X, W, ids = t(p.X), t(p.W), t(p.ids)
+    Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(dev)
+
+    def timed(call, steps, per_kernel=False):
+        """Cold-L2 device time per step (events around the call only)."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(steps)]
+        kt = []
+        for i in range(steps):
+            flush.fill_(float(i))
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+            if per_kernel:
+                kt.append(pool.kernel_times())
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev], kt
+
+    lora_call = lambda: pool.linear(X, W, ids, Y)  # noqa: E731
+    base_call = lambda: pool.base_linear(X, W, Y)  # noqa: E731
+
+    # warm-up (also grows scratch, encodes tensor maps, loads modules)
+    for _ in range(args.warmup):
+        lora_call()
+        base_call()
+    barrier()
+
+    def graph_of(call, timing):
+        """One step captured as a CUDA graph (the library's kernels, and with `timing`
+        its per-kernel event records); replayed in the timed loops."""
+        if args.no_graph:
+            pool.enable_timing(timing)
+            return call
+        pool.enable_timing(timing)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            call()
+        pool.enable_timing(False)
+        graphs.append(g)
+        return g.replay
+
+    graphs = []
+    lora_timed = graph_of(lora_call, True)
+    for _ in range(args.warmup):
+        lora_timed()
+    barrier()
+
+    # ---- timed region: K lora_linear steps, per-kernel events on the same stream
+    nvml = NvmlClockSampler(dev)
+    with ClockSampler(dev.index or 0) as clocks, nvml:
+        barrier()
+        step_ms, kts = timed(lora_timed, args.steps, per_kernel=True)
+        barrier()
+    pool.enable_timing(False)
+    total_ms = sum(step_ms)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    tokens = p.T * args.steps * ws
+    value = tokens / (total_ms / 1e3)
+
+    # ---- the same kernels without the per-kernel events, and base-only
+    lora_plain = graph_of(lora_call, False)
+    base_plain = graph_of(base_call, False)
+    for _ in range(args.warmup):
+        lora_plain()
+        base_plain()
+    plain_ms, _ = timed(lora_plain, args.steps)
+    base_ms, _ = timed(base_plain, args.steps)
+    base_timed = graph_of(base_call, True)
+    _, base_kts = timed(base_timed, args.steps, per_kernel=True)
+    pool.enable_timing(False)
+
+    # ---- e2e through the host entry point (pinned buffers, copies + sync inside)
+    Xh = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).pin_memory()
+    idh = torch.from_numpy(p.ids).pin_memory()
+    Yh = torch.empty((p.T, p.d_out), dtype=torch.bfloat16).pin_memory()
+    for _ in range(3):
+        pool.linear_host(Xh, W, idh, Yh)
+    e2e_s = 0.0
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        pool.linear_host(Xh, W, idh, Yh)
+        e2e_s += time.perf_counter() - t0
+    e2e_value = p.T * args.steps * ws / e2e_s
+    assert pool.check_errors() == al.LORA_OK
+    barrier()
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    def mean_of(kts, key):
+        return statistics.mean(k[key] for k in kts) if kts else 0.0
+
+    gemm_ms = mean_of(kts, "base_gemm")
+    shrink_ms = mean_of(kts, "shrink")
+    finish_ms = mean_of(kts, "finish_expand")
+    seg_ms = mean_of(kts, "segment_build")
+    ab = algorithmic_bytes(p)
+    hbm_peak, tf_peak, peak_src = measured_peaks()
+    decode = p.T <= 256
+    gemm_bytes = ab["w"] + ab["x"]
+    if decode:
+        achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+        roof = {"kernel": "gemm_decode_kernel", "bound": "hbm", "achieved": achieved,
+                "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                "traffic": profiled_traffic(), "algorithmic_bytes": gemm_bytes,
+                "peak_source": peak_src}
+    else:
+        gemm_flops = 2.0 * p.T * p.d_in * p.d_out
+        achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+        roof = {"kernel": "gemm_prefill_kernel", "bound": "tensor", "achieved": achieved,
+                "peak": tf_peak, "unit": "TFLOP/s", "frac": achieved / tf_peak, "traffic": None,
+                "algorithmic_flops": gemm_flops, "peak_source": peak_src}
+    adapter_bytes = ab["adapters"] + ab["x"] + ab["y"]  # shrink reads A + X; finish reads B, writes Y
+    adapter_gbs = adapter_bytes / ((shrink_ms + finish_ms) * 1e-3) / 1e9 if shrink_ms + finish_ms else None
+    overhead = statistics.mean(plain_ms) / statistics.mean(base_ms) - 1.0
+    floor = ab["adapters"] / (ab["w"] + ab["x"] + ab["y"])
+
+    cpu = None
+    if not args.no_cpu_baseline and ws >= 1:
+        rate, cores, sample = cpu_oracle_rate(p, args.cpu_seconds, max_tokens=16)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+
+    clk = nvml.summary() or dict(clocks.summary(), source="nvidia-smi")
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(cfg, l2="flushed before every timed step (2x L2 write, outside events)",
+                       launch="direct" if args.no_graph else "CUDA graph replay of one call",
+                       parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
+        "overhead_vs_base": overhead,
+        "overhead_floor": floor,
+        "base_only_ms": statistics.mean(base_ms),
+        "lora_ms_no_kernel_events": statistics.mean(plain_ms),
+        "adapter_path_gbs": adapter_gbs,
+        "kernel_ms": {"segment_build": seg_ms, "shrink": shrink_ms, "base_gemm": gemm_ms,
+                      "finish_expand": finish_ms},
+        "base_only_kernel_ms": {"base_gemm": mean_of(base_kts, "base_gemm"),
+                                "finish": mean_of(base_kts, "finish_expand")},
+        "roofline": roof,
+        "tflops": algorithmic_flops(p) / (statistics.mean(plain_ms) * 1e-3) / 1e12,
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": ab["x"] + ab["ids"],
+                "d2h_bytes_per_step": ab["y"]},
+        "gpu_launches": (2 if decode else 3) * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -207,6 +207,19 @@ lora_status lora_build_segments(lora_pool_t pool, const int32_t *ids, int T, int
 #define LORA_STATS_COUNT 7
 lora_status lora_pool_stats(lora_pool_t pool, int64_t *out);
 
+/*
+ * Measurement hook. While enabled, every lora_linear / lora_base_linear call
+ * records CUDA events on its stream around each kernel it launches.
+ * lora_pool_kernel_times waits for the last call and writes the device time
+ * of each of its kernels in milliseconds to ms[0..LORA_KERNEL_SLOTS):
+ *   0 segment builder, 1 shrink, 2 base GEMM (prefill: with the fused
+ *   expand), 3 decode finishing pass (split-K sum + expand).
+ * Slots a call did not use read 0.
+ */
+#define LORA_KERNEL_SLOTS 4
+lora_status lora_pool_enable_timing(lora_pool_t pool, int enable);
+lora_status lora_pool_kernel_times(lora_pool_t pool, float *ms);
+
 /* Force a kernel family (lora_path); LORA_PATH_AUTO restores the default. */
 lora_status lora_pool_set_path(lora_pool_t pool, int path);
 
