@@ -35,6 +35,7 @@ EXPORTS = (
     "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
     "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
+    "lora_base_linear_noalloc",
 )
 LORA_KERNEL_SLOTS = 4
 KERNEL_SLOT_NAMES = ("segment_build", "shrink", "base_gemm", "finish_expand")
@@ -80,6 +81,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_abi_version": [],
         "lora_pool_enable_timing": [vp, i32],
         "lora_pool_kernel_times": [vp, vp],
+        "lora_base_linear_noalloc": [vp, vp, i32, i32, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -151,6 +153,13 @@ def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream
 def lora_base_linear(pool: int, X, W_base, T: int, Y, stream=None) -> int:
     return load_library().lora_base_linear(pool, _ptr(X), _ptr(W_base), T, _ptr(Y),
                                            _stream(stream))
+
+
+def lora_base_linear_noalloc(X, W_base, T: int, d_in: int, d_out: int, Y, stream=None) -> int:
+    """Base product through the entry point that allocates no device memory (no pool):
+    for callers that may not call cudaMalloc."""
+    return load_library().lora_base_linear_noalloc(_ptr(X), _ptr(W_base), T, d_in, d_out, _ptr(Y),
+                                                   _stream(stream))
 
 
 def lora_pool_check_errors(pool: int) -> int:

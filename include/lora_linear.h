@@ -182,6 +182,35 @@ lora_status lora_base_linear(lora_pool_t pool, const void *X, const void *W_base
                              void *Y, lora_stream_t stream);
 
 /*
+ * Base product Y = X W_base^T for callers that cannot allocate device memory.
+ * The pages have no counterpart for this call: it exists for users of this
+ * library who may not call cudaMalloc (code living inside another framework's
+ * memory arena, plugins whose host forbids device allocation after start-up,
+ * callers that must never block on an allocator). It needs no pool and
+ * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call):
+ * the same decode kernels as lora_base_linear take their split-K scratch from
+ * a fixed __device__ array compiled into the library (16 MiB of partial sums
+ * plus a 256-byte head), which every GPU that loads the library holds until
+ * the process exits.
+ *   X: device bf16 T x d_in, W_base: device bf16 d_out x d_in, Y: device bf16
+ *   T x d_out; 0 <= T <= 256; d_in, d_out positive multiples of 8 up to
+ *   LORA_MAX_DIM. Asynchronous on `stream`.
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, once per device, with that device current): make
+ * that first call before any CUDA stream capture.
+ * Every call shares the one array and leaves its contents behind; calls that
+ * overlap on the GPU (other streams, or concurrent replays) race on it and
+ * must be serialised by the caller.
+ * Errors: ARG (null pointers, T outside [0, 256]), SHAPE (bad d_in / d_out,
+ * or T x d_out too large for the fixed scratch: the call needs
+ * 256 * T * G floats with G >= d_out / 128; T = 256 works up to d_out = 8192),
+ * UNSUPPORTED (device not compute capability 10.3), CUDA. A kernel wait that
+ * times out is not reported by this call.
+ */
+lora_status lora_base_linear_noalloc(const void *X, const void *W_base, int T, int d_in,
+                                     int d_out, void *Y, lora_stream_t stream);
+
+/*
  * Wait for the pool's last enqueued call, read and clear the device error
  * word. Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID or LORA_ERR_TIMEOUT (the
  * first of these present), or LORA_ERR_CUDA if the device reported an error.
