@@ -133,8 +133,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_arrive(kBarSetup, kThreads);  // barriers are ready; do not wait for TMEM
         if (lane == 0) {
             const uint64_t pol_w = policy_evict_first();  // W is read exactly once
-            int it = 0;
-            for (int u = u0; u < u1; ++u, ++it) {
+            // W is a weight: the first ring's worth of W tiles is requested before the
+            // previous kernel in the stream has finished; X (and everything the epilogue
+            // touches) only after the programmatic wait.
+            const int pre = (u1 - u0) < stages ? (u1 - u0) : stages;
+            for (int i = 0; i < pre; ++i) {
+                const int u = u0 + i, tile = u / p.KB, kb = u - tile * p.KB;
+                mbar_arrive_expect_tx(&full[i], stage_bytes);
+                tma_load_2d_hint(smem + (size_t)i * stage_bytes, &tmW, &full[i], kb * 64, tile * 128,
+                                 pol_w);
+            }
+            pdl_wait_prior();
+            for (int i = 0; i < pre; ++i) {
+                const int kb = (u0 + i) % p.KB;
+                tma_load_2d(smem + (size_t)i * stage_bytes + kWTileBytes, &tmX, &full[i], kb * 64, 0);
+            }
+            int it = pre;
+            for (int u = u0 + pre; u < u1; ++u, ++it) {
                 const int s = it % stages;
                 if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err)) break;
                 const int tile = u / p.KB, kb = u - tile * p.KB;
@@ -188,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(kBarSetup, kThreads);
         tc_fence_after_sync();
         const uint32_t tmem = *tmem_slot;
+        pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
         if (sa.ids != nullptr) {
             const int pairs = p.T * pool.max_pages;
             for (int u = c; u < pairs; u += p.G) {
@@ -225,22 +241,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-constexpr int kFinishThreads = 256;  // one thread per output column
-constexpr int kPrefetchPages = 8;    // B pages fetched before the GEMM has finished
+constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
+constexpr int kFinishCols = 8;
+constexpr int kPrefetchPages = 2;     // B pages fetched before the GEMM has finished
+
+__device__ __forceinline__ void add8(float (&acc)[kFinishCols], const float *src)
+{
+    const float4 a = *reinterpret_cast<const float4 *>(src);
+    const float4 b = *reinterpret_cast<const float4 *>(src + 4);
+    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+}
+
+// acc[c] += sum_jj v[jj] * page[n0 + c][jj], the 8 columns' 16-byte words in b[0..7]
+__device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *v, const uint4 (&b)[8])
+{
+#pragma unroll
+    for (int c = 0; c < kFinishCols; ++c) acc[c] = dot8_f32_bf16(v, b[c], acc[c]);
+}
 
 __global__ void __launch_bounds__(kFinishThreads)
     finish_decode_kernel(DecodePlan p, const float *__restrict__ partials,
                          const int32_t *__restrict__ ids, PoolDev pool, const float *__restrict__ V,
                          int ldv, uint16_t *__restrict__ Y, int *err)
 {
-    const int n = blockIdx.x * kFinishThreads + threadIdx.x;
+    const int n0 = (blockIdx.x * kFinishThreads + threadIdx.x) * kFinishCols;
     const int t = blockIdx.y;
-    const bool col_ok = n < pool.d_out;
+    const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
 
-    // ---- independent of the GEMM kernel: adapter of this token, its B values
+    // ---- independent of the GEMM kernel: this token's adapter and its first B words
     int np = 0;
     const int32_t *pages = nullptr;
-    uint4 b[kPrefetchPages];
     if (ids != nullptr) {
         const int id = ids[t];
         if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
@@ -251,46 +282,60 @@ __global__ void __launch_bounds__(kFinishThreads)
             atomicOr(err, kErrBadIdBit);  // strict: never a silent base fall-back
         }
     }
+    uint4 b[kPrefetchPages][8];
     if (col_ok) {
 #pragma unroll
         for (int q = 0; q < kPrefetchPages; ++q)
-            if (q < np) b[q] = ldg_nc_v4(pool.B_pages + ((size_t)pages[q] * pool.d_out + n) * kRankPage);
+            if (q < np) {
+                const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+#pragma unroll
+                for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
+            }
     }
-    const int tile = n >> 7, nl = n & 127;
-    const int kb_lo = tile * p.KB, kb_hi = kb_lo + p.KB;
     // contributors of this tile: CTAs c_lo..c_hi (contiguous k-ranges); only c_lo can
     // have started in the previous tile, in which case its partial for this tile is
-    // its second one
-    int c_lo = (int)(((long long)kb_lo * p.G) / p.U);
-    while (c_lo > 0 && cta_start(c_lo, p.U, p.G) > kb_lo) --c_lo;
-    while (cta_start(c_lo + 1, p.U, p.G) <= kb_lo) ++c_lo;
+    // its second one. (U < 2^20 and G < 2^11, so the products fit in 32 bits.)
+    const int tile = n0 >> 7, nl = n0 & 127;
+    const int kb_lo = tile * p.KB, kb_hi = kb_lo + p.KB;
+    int c_lo = (kb_lo * p.G) / p.U;
+    while (c_lo > 0 && (c_lo * p.U) / p.G > kb_lo) --c_lo;
+    while (((c_lo + 1) * p.U) / p.G <= kb_lo) ++c_lo;
     int c_hi = c_lo;
-    while (c_hi + 1 < p.G && cta_start(c_hi + 1, p.U, p.G) < kb_hi) ++c_hi;
-    const int seg_lo = cta_start(c_lo, p.U, p.G) < kb_lo ? 1 : 0;
+    while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < kb_hi) ++c_hi;
+    const int seg_lo = (c_lo * p.U) / p.G < kb_lo ? 1 : 0;
 
     // ---- partials and V are written by the GEMM kernel
     pdl_wait_prior();
+    pdl_launch_dependents();  // the next call's GEMM may start streaming its weights
     if (!col_ok) return;
 
-    float acc = partials[((size_t)(c_lo * 2 + seg_lo) * p.T + t) * 128 + nl];
-    for (int c = c_lo + 1; c <= c_hi; ++c) acc += partials[((size_t)(c * 2) * p.T + t) * 128 + nl];
+    float acc[kFinishCols] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    add8(acc, partials + ((size_t)(c_lo * 2 + seg_lo) * p.T + t) * 128 + nl);
+    for (int c = c_lo + 1; c <= c_hi; ++c) add8(acc, partials + ((size_t)(c * 2) * p.T + t) * 128 + nl);
     const float *vrow = V + (size_t)t * ldv;
     for (int q = 0; q < np; ++q) {
+        float v[8];
         const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
         const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
-        const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        uint4 bq;
+        v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+        v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
         if (q < kPrefetchPages) {
-#pragma unroll
-            for (int i = 0; i < kPrefetchPages; ++i)
-                if (i == q) bq = b[i];
+            if (q == 0) expand8(acc, v, b[0]);
+            else expand8(acc, v, b[1]);
         } else {
-            bq = ldg_nc_v4(pool.B_pages + ((size_t)pages[q] * pool.d_out + n) * kRankPage);
+            uint4 bq[8];
+            const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) bq[c] = ldg_nc_v4(src + c * kRankPage);
+            expand8(acc, v, bq);
         }
-        acc = dot8_f32_bf16(vv, bq, acc);
     }
-    __nv_bfloat16 h = __float2bfloat16_rn(acc);
-    Y[(size_t)t * pool.d_out + n] = *reinterpret_cast<uint16_t *>(&h);
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    *reinterpret_cast<uint4 *>(Y + (size_t)t * pool.d_out + n0) = o;
 }
 
 uint32_t pow2_cols(uint32_t n)
@@ -335,17 +380,30 @@ cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
     cudaError_t e = ensure_smem_attr((const void *)gemm_decode_kernel, plan.smem_bytes);
     if (e != cudaSuccess) return e;
     ShrinkArgs sa{X, ids, V, ldv};
-    gemm_decode_kernel<<<plan.G, kThreads, plan.smem_bytes, stream>>>(tmW, tmX, plan, partials, err,
-                                                                      pool, sa);
-    return cudaGetLastError();
+    // programmatic stream serialization: the prologue and the first W tiles overlap the
+    // previous kernel in the stream (the kernel waits before touching anything else)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(plan.G);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = plan.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel, tmW, tmX, plan, partials, err, pool, sa);
 }
 
 cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
                                  const int32_t *ids, const PoolDev &pool, const float *V,
                                  int ldv, uint16_t *Y, int *err, cudaStream_t stream)
 {
+    cudaError_t e = ensure_smem_attr((const void *)finish_decode_kernel, 0);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((pool.d_out + kFinishThreads - 1) / kFinishThreads, plan.T);
+    const int per_cta = kFinishThreads * kFinishCols;
+    cfg.gridDim = dim3((pool.d_out + per_cta - 1) / per_cta, plan.T);
     cfg.blockDim = dim3(kFinishThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;

@@ -99,9 +99,9 @@ cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, 
                                 int npages, const PoolDev &pool, uint16_t *A_pages,
                                 uint16_t *B_pages, cudaStream_t stream);
 
-// Host: raise a kernel's dynamic shared-memory limit to at least `bytes` on the
-// current device (remembered per kernel and device, so repeated launches do
-// not repeat the driver call).
+// Host: on the current device, give a kernel the largest shared-memory carveout
+// and raise its dynamic shared-memory limit to at least `bytes` (remembered
+// per kernel and device, so repeated launches do not repeat the driver calls).
 cudaError_t ensure_smem_attr(const void *kernel, size_t bytes);
 
 // Host: build a 2-D bf16 TMA descriptor with 128-byte swizzle over a row-major

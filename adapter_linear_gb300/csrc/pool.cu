@@ -599,6 +599,8 @@ cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, 
                                 int npages, const PoolDev &pool, uint16_t *A_pages,
                                 uint16_t *B_pages, cudaStream_t stream)
 {
+    cudaError_t e = ensure_smem_attr((const void *)pack_adapter_kernel, 0);
+    if (e != cudaSuccess) return e;
     const size_t total = (size_t)npages * kRankPage * (pool.d_in + pool.d_out);
     int grid = (int)std::min<size_t>((total + 255) / 256, 4096);
     pack_adapter_kernel<<<grid, 256, 0, stream>>>(A, B, rank, pages, npages, pool.d_in, pool.d_out,
@@ -626,7 +628,13 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t bytes)
             if (e == cudaSuccess) x.bytes = bytes;
             return e;
         }
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    // every kernel of the library asks for the largest shared-memory carveout, so an SM
+    // never has to drain and reconfigure between two of them and kernels launched with
+    // programmatic serialization can be resident beside the GEMM kernels
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess && bytes > 0)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e == cudaSuccess) done.push_back({kernel, dev, bytes});
     return e;
 }

@@ -4,8 +4,11 @@ One step = one lora_linear call (segment build, shrink, base GEMM, expand)
 over one batch of the Llama-2-7B q_proj decode workload: T=64 tokens,
 d_in=d_out=4096, 200 resident rank-16 adapters (alpha 32), ids uniform over
 0..199, synthetic seeded bf16 data. Inputs are resident in HBM when the timed
-region starts; L2 is flushed (a 2x-L2 buffer write, outside the events)
-before every timed step, so every step reads W and the adapters from HBM.
+region starts. The K steps run back to back (one CUDA graph) over R "layers",
+each with its own W and adapter pool, step k on layer k mod R; the layers
+together hold more than 3x the L2 size, so every step reads its weights and
+adapter pages from HBM. An isolated call (L2 flushed before it) is reported
+beside it.
 
 Prints ONE JSON line (rank 0). value = tokens/s over all ranks; e2e = the
 same metric through lora_linear_host (pinned host X/ids in, host Y out,
@@ -333,13 +336,29 @@ def main():
             return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
         return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
 
-    pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
-    for slot, ad in p.adapters.items():
-        pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
-    pool.reserve(p.T)
-    X, W, ids = t(p.X), t(p.W), t(p.ids)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = props.L2_cache_size
+    A_dev = {s: t(ad.A) for s, ad in p.adapters.items()}
+    B_dev = {s: t(ad.B) for s, ad in p.adapters.items()}
+
+    def new_layer(W):
+        pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
+        for slot, ad in p.adapters.items():
+            pool.load_adapter(slot, A_dev[slot], B_dev[slot], ad.rank, ad.alpha)
+        pool.reserve(p.T)
+        return pool, W
+
+    # R layers, each with its own W and its own adapter pool (like the layers of a
+    # model): step k runs layer k mod R, so every step reads its weights and adapter
+    # pages from HBM -- the layers' footprint is more than 3x L2, no flush needed.
+    W0 = t(p.W)
+    layers = [new_layer(W0)]
+    layer_bytes = W0.numel() * 2 + layers[0][0].stats()["bytes_held"]
+    R = max(2, min(32, -(-3 * l2 // layer_bytes)))
+    while len(layers) < R:
+        layers.append(new_layer(W0.clone()))
+    X, ids = t(p.X), t(p.ids)
     Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2 // 4 + 1024, dtype=torch.float32, device=dev)
 
     def barrier():
@@ -347,58 +366,55 @@ def main():
             torch.distributed.barrier()
         torch.cuda.synchronize(dev)
 
-    def timed(call, steps, per_kernel=False):
-        """Cold-L2 device time per step (events around the call only)."""
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(steps)]
-        kt = []
-        for i in range(steps):
-            flush.fill_(float(i))
-            ev[i][0].record(stream)
-            call()
-            ev[i][1].record(stream)
-            if per_kernel:
-                kt.append(pool.kernel_times())
-        torch.cuda.synchronize(dev)
-        return [a.elapsed_time(b) for a, b in ev], kt
+    def lora_step(k):
+        pool, W = layers[k % R]
+        pool.linear(X, W, ids, Y)
 
-    lora_call = lambda: pool.linear(X, W, ids, Y)  # noqa: E731
-    base_call = lambda: pool.base_linear(X, W, Y)  # noqa: E731
+    def base_step(k):
+        pool, W = layers[k % R]
+        pool.base_linear(X, W, Y)
 
-    # warm-up (also grows scratch, encodes tensor maps, loads modules)
-    for _ in range(args.warmup):
-        lora_call()
-        base_call()
-    barrier()
-
-    def graph_of(call, timing):
-        """One step captured as a CUDA graph (the library's kernels, and with `timing`
-        its per-kernel event records); replayed in the timed loops."""
-        if args.no_graph:
+    def program(step, n, timing=False):
+        """n consecutive steps captured as one CUDA graph (or a plain loop)."""
+        for pool, _ in layers:
             pool.enable_timing(timing)
-            return call
-        pool.enable_timing(timing)
+        run = lambda: [step(k) for k in range(n)]  # noqa: E731
+        if args.no_graph:
+            return run
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
-            call()
-        pool.enable_timing(False)
+            run()
+        for pool, _ in layers:
+            pool.enable_timing(False)
         graphs.append(g)
         return g.replay
 
+    def time_program(prog):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        prog()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    # warm-up: W plain steps of each kind (scratch, tensor maps, modules, graphs)
+    for k in range(max(args.warmup, R)):
+        lora_step(k)
+        base_step(k)
+    barrier()
     graphs = []
-    lora_timed = graph_of(lora_call, True)
-    for _ in range(args.warmup):
-        lora_timed()
+    lora_prog = program(lora_step, args.steps)
+    base_prog = program(base_step, args.steps)
+    warm_prog = program(lora_step, args.warmup)
+    warm_prog()
     barrier()
 
-    # ---- timed region: K lora_linear steps, per-kernel events on the same stream
+    # ---- timed region: exactly K lora_linear steps, back to back
     nvml = NvmlClockSampler(dev)
     with ClockSampler(dev.index or 0) as clocks, nvml:
         barrier()
-        step_ms, kts = timed(lora_timed, args.steps, per_kernel=True)
+        total_ms = time_program(lora_prog)
         barrier()
-    pool.enable_timing(False)
-    total_ms = sum(step_ms)
     if ws > 1:
         tt = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -406,33 +422,47 @@ def main():
     tokens = p.T * args.steps * ws
     value = tokens / (total_ms / 1e3)
 
-    # ---- the same kernels without the per-kernel events, and base-only
-    lora_plain = graph_of(lora_call, False)
-    base_plain = graph_of(base_call, False)
-    for _ in range(args.warmup):
-        lora_plain()
-        base_plain()
-    plain_ms, _ = timed(lora_plain, args.steps)
-    base_ms, _ = timed(base_plain, args.steps)
-    base_timed = graph_of(base_call, True)
-    _, base_kts = timed(base_timed, args.steps, per_kernel=True)
-    pool.enable_timing(False)
+    # ---- base-only reference, same structure
+    base_prog()
+    base_total_ms = time_program(base_prog)
+
+    # ---- per-kernel device time: one step per layer with the library's timing events
+    def kernel_samples(step):
+        prog = program(step, R, timing=True)
+        out = []
+        for _ in range(max(1, -(-args.steps // R))):
+            prog()
+            torch.cuda.synchronize(dev)
+            out += [pool.kernel_times() for pool, _ in layers]
+        return out[:args.steps]
+    kts = kernel_samples(lora_step)
+    base_kts = kernel_samples(base_step)
+
+    # ---- an isolated call: L2 flushed before it, one call per replay
+    iso_prog = program(lambda k: lora_step(0), 1)
+    iso = []
+    for i in range(args.steps):
+        flush.fill_(float(i))
+        iso.append(time_program(iso_prog))
+    iso_ms = statistics.median(iso)
 
     # ---- e2e through the host entry point (pinned buffers, copies + sync inside)
+    pool0, W = layers[0]
     Xh = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).pin_memory()
     idh = torch.from_numpy(p.ids).pin_memory()
     Yh = torch.empty((p.T, p.d_out), dtype=torch.bfloat16).pin_memory()
     for _ in range(3):
-        pool.linear_host(Xh, W, idh, Yh)
+        pool0.linear_host(Xh, W, idh, Yh)
     e2e_s = 0.0
     for i in range(args.steps):
         flush.fill_(float(i))
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
-        pool.linear_host(Xh, W, idh, Yh)
+        pool0.linear_host(Xh, W, idh, Yh)
         e2e_s += time.perf_counter() - t0
     e2e_value = p.T * args.steps * ws / e2e_s
-    assert pool.check_errors() == al.LORA_OK
+    for pool, _ in layers:
+        assert pool.check_errors() == al.LORA_OK
     barrier()
 
     if rank != 0:
@@ -465,7 +495,7 @@ def main():
                 "algorithmic_flops": gemm_flops, "peak_source": peak_src}
     adapter_bytes = ab["adapters"] + ab["x"] + ab["y"]  # shrink reads A + X; finish reads B, writes Y
     adapter_gbs = adapter_bytes / ((shrink_ms + finish_ms) * 1e-3) / 1e9 if shrink_ms + finish_ms else None
-    overhead = statistics.mean(plain_ms) / statistics.mean(base_ms) - 1.0
+    overhead = total_ms / base_total_ms - 1.0
     floor = ab["adapters"] / (ab["w"] + ab["x"] + ab["y"])
 
     cpu = None
@@ -478,20 +508,22 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(cfg, l2="flushed before every timed step (2x L2 write, outside events)",
-                       launch="direct" if args.no_graph else "CUDA graph replay of one call",
+        "config": dict(cfg, layers=R,
+                       l2=f"inputs larger than L2: {R} layers, each its own W and adapter pool "
+                          f"({R * layer_bytes / 1e6:.0f} MB cycled), step k uses layer k mod {R}",
+                       launch="direct" if args.no_graph else "one CUDA graph of the K steps",
                        parallelism=f"replicas x{ws}" if ws > 1 else "single GPU"),
         "overhead_vs_base": overhead,
         "overhead_floor": floor,
-        "base_only_ms": statistics.mean(base_ms),
-        "lora_ms_no_kernel_events": statistics.mean(plain_ms),
+        "base_only_ms_per_step": base_total_ms / args.steps,
+        "isolated_call_ms": iso_ms,
         "adapter_path_gbs": adapter_gbs,
         "kernel_ms": {"segment_build": seg_ms, "shrink": shrink_ms, "base_gemm": gemm_ms,
                       "finish_expand": finish_ms},
         "base_only_kernel_ms": {"base_gemm": mean_of(base_kts, "base_gemm"),
                                 "finish": mean_of(base_kts, "finish_expand")},
         "roofline": roof,
-        "tflops": algorithmic_flops(p) / (statistics.mean(plain_ms) * 1e-3) / 1e12,
+        "tflops": algorithmic_flops(p) / (total_ms / args.steps * 1e-3) / 1e12,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": ab["x"] + ab["ids"],
                 "d2h_bytes_per_step": ab["y"]},
