@@ -182,6 +182,18 @@ __device__ __forceinline__ uint64_t policy_evict_last()
     return p;
 }
 
+// 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Make generic-proxy shared-memory writes visible to the async proxy
 // (tensor cores / TMA) before signalling them.
 __device__ __forceinline__ void fence_proxy_async_smem()
@@ -265,6 +277,21 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t smem_addr)
     d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
     d |= (uint64_t)2 << 61;                         // swizzle: 128 B
     return d;
+}
+
+// Shared-memory matrix descriptor for a K-major operand without swizzle: core
+// matrices of 8 rows x 16 bytes (128 contiguous bytes), `lbo` bytes between the
+// core matrices that follow each other along K, `sbo` bytes between 8-row groups
+// along M/N. The interleaved B pages ([n][8 rank rows] per page) are exactly
+// this layout with sbo = 128 and lbo = the distance between two page slices.
+__device__ __forceinline__ uint64_t sdesc_k_none(uint32_t smem_addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = 0;
+    d |= (uint64_t)((smem_addr & 0x3FFFFu) >> 4);  // start address
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;   // leading (K) byte offset
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;   // stride (M/N) byte offset
+    d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
+    return d;                                       // swizzle: none
 }
 
 // 32 TMEM lanes x 32 bit, N consecutive columns -> N registers per thread,

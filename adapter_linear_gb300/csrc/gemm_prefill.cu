@@ -1,21 +1,30 @@
-// gemm_prefill.cu -- base product with the low-rank expand fused into the
-// epilogue, for prefill-sized batches (compute bound: a 16384 x 14336 x 4096
-// GEMM is ~2 TFLOP).
+// gemm_prefill.cu -- base product with the low-rank expand, for prefill-sized
+// batches (compute bound: a 16384 x 14336 x 4096 GEMM is ~2 TFLOP).
 //
 // Persistent kernel, one CTA per SM, output tiles of 128 tokens x 256 columns
-// walked in a grouped order (16 token-tiles share one sweep over the columns,
+// walked in a grouped order (16 token tiles share one sweep over the columns,
 // so their X rows stay in L2 while W streams).
 //  * warp 8: TMA producer. Per 64-wide k-block it loads X[128 x 64] and
 //    W[256 x 64] (128-byte swizzle) into a 4-stage ring (48 KB per stage).
 //  * warp 9: MMA issuer. tcgen05.mma M=128 N=256 K=16, four per k-block, into
 //    one of two TMEM accumulators (2 x 256 columns = all 512), so the
 //    epilogue of tile i overlaps the MMAs of tile i+1.
+//  * The expand Y += s_i (X A_i) B_i runs on the tensor cores too: when every
+//    token of a tile with an adapter uses the same adapter (always, for
+//    sequences of one adapter that start on a 128-token boundary), the
+//    producer appends ceil(pages/4) k-blocks, each holding 32 rank columns: the
+//    shrink's bf16 hi/lo pairs s*V = hi + lo of the tile's tokens (one TMA box
+//    of 64 columns = [hi 32 | lo 32]; rows of base-only tokens are zero) and
+//    four 4 KB slices of the adapter's interleaved B pages (bulk copies; a B
+//    page is already a K-major no-swizzle operand: 8 columns x 16 bytes per
+//    core matrix). Four MMAs per such block: hi and lo against the same B.
+//    The product is accumulated in fp32 with the base product, so Y is rounded
+//    once. Expand work: 2 * 32 / 64 = one k-block per 32 rank columns.
 //  * warps 0-7: epilogue. Warp w reads TMEM lanes 32*(w%4).. (its 32 token
-//    rows) and columns 128*(w/4).. in chunks of 32 with tcgen05.ld; for a row
-//    whose token has an adapter it adds sum_j V[t,j] B_i[j,n] (V carries s_i;
-//    B pages are interleaved so one 16-byte load gives 8 rank rows of one
-//    column, and rows of the same adapter hit the same addresses), rounds
-//    once to bf16 and stores Y. Y is written exactly once.
+//    rows) and columns 128*(w/4).. in chunks of 32 with tcgen05.ld, rounds to
+//    bf16 and stores Y. For a tile whose tokens use more than one adapter the
+//    expand is added here instead, on CUDA cores (B pages read 16 bytes = 8
+//    rank rows per column), before the rounding.
 #include "device_common.cuh"
 
 namespace lora {
@@ -31,13 +40,16 @@ constexpr int kStages = 4;
 constexpr int kGroupM = 16;
 constexpr int kEpiWarps = 8;
 constexpr uint32_t kTmemCols = 512;
+constexpr int kPagesPerBlock = 4;            // 32 rank columns per expand k-block
+constexpr int kPageSliceBytes = kBN * 16;    // 256 columns x 8 rank rows of bf16
 
 struct PrefillArgs {
     int T, d_in, d_out;
     int KB, tiles_m, tiles_n, num_tiles;
     const int32_t *ids;
-    const float *V;
-    int ldv;
+    const int32_t *tile_info;
+    const uint16_t *Vhl;
+    int ldh;
     uint16_t *Y;
     int *err;
 };
@@ -53,9 +65,36 @@ __device__ __forceinline__ void tile_coords(int tile, const PrefillArgs &a, int 
     n = local / gm;
 }
 
+// Adapter use of one token tile (from the segment builder's tile table): mode 0 =
+// no token has an adapter, 1 = one adapter (slot), 2 = several adapters (expand
+// on CUDA cores).
+struct TileLora {
+    int mode, slot, npages, blocks;
+    const int32_t *pages;
+};
+
+__device__ __forceinline__ TileLora tile_lora(int m, const PrefillArgs &a, const PoolDev &pool)
+{
+    TileLora r{0, -1, 0, 0, nullptr};
+    if (a.tile_info == nullptr) return r;
+    const int ti = a.tile_info[m];
+    if (ti == kTileNoAdapter) return r;
+    if (ti == kTileMixed) {
+        r.mode = 2;
+        return r;
+    }
+    const int32_t *row = pool.slots + (size_t)ti * pool.slot_stride;
+    r.mode = 1;
+    r.slot = ti;
+    r.npages = row[SLOT_NPAGES];
+    r.blocks = (r.npages + kPagesPerBlock - 1) / kPagesPerBlock;
+    r.pages = row + SLOT_PAGES;
+    return r;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
-                        PrefillArgs a, PoolDev pool)
+                        const __grid_constant__ CUtensorMap tmV, PrefillArgs a, PoolDev pool)
 {
     extern __shared__ uint8_t pre_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -90,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 8 && lane == 0) {
         tma_prefetch_map(&tmX);
         tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmV);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -104,14 +144,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x) {
                 int m, n;
                 tile_coords(tile, a, m, n);
-                for (int kb = 0; kb < a.KB; ++kb, ++it) {
+                const TileLora tl = tile_lora(m, a, pool);
+                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
+                const int n0 = n * kBN;
+                const uint32_t slice_bytes = (uint32_t)min(kBN, a.d_out - n0) * 16u;
+                for (int kb = 0; kb < steps; ++kb, ++it) {
                     const int s = it % kStages;
                     ok = mbar_wait(&empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &abort_flag, a.err);
                     if (!ok) break;
                     uint8_t *xs = smem + (size_t)s * kStageBytes;
-                    mbar_arrive_expect_tx(&full[s], kStageBytes);
-                    tma_load_2d(xs, &tmX, &full[s], kb * kBK, m * kBM);
-                    tma_load_2d(xs + kXTileBytes, &tmW, &full[s], kb * kBK, n * kBN);
+                    if (kb < a.KB) {
+                        mbar_arrive_expect_tx(&full[s], kStageBytes);
+                        tma_load_2d(xs, &tmX, &full[s], kb * kBK, m * kBM);
+                        tma_load_2d(xs + kXTileBytes, &tmW, &full[s], kb * kBK, n0);
+                    } else {
+                        const int e = kb - a.KB;
+                        mbar_arrive_expect_tx(&full[s], kXTileBytes + kPagesPerBlock * slice_bytes);
+                        tma_load_2d(xs, &tmV, &full[s], e * 64, m * kBM);
+                        for (int i = 0; i < kPagesPerBlock; ++i) {
+                            const int q = e * kPagesPerBlock + i;
+                            const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
+                            bulk_load(xs + kXTileBytes + i * kPageSliceBytes,
+                                      pool.B_pages + ((size_t)page * a.d_out + n0) * kRankPage,
+                                      slice_bytes, &full[s]);
+                        }
+                    }
                 }
             }
             for (int i = 0; i < kStages && i < it; ++i) {
@@ -128,22 +185,37 @@ __global__ void __launch_bounds__(kThreads, 1)
             int it = 0, tc = 0;
             bool ok = true;
             for (int tile = blockIdx.x; tile < a.num_tiles && ok; tile += gridDim.x, ++tc) {
+                int m, n;
+                tile_coords(tile, a, m, n);
+                const TileLora tl = tile_lora(m, a, pool);
+                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
                 const int buf = tc & 1;
                 ok = mbar_wait(&acc_empty[buf], ((uint32_t)(tc >> 1) & 1u) ^ 1u, &abort_flag, a.err);
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
-                for (int kb = 0; kb < a.KB; ++kb, ++it) {
+                for (int kb = 0; kb < steps; ++kb, ++it) {
                     const int s = it % kStages;
                     ok = mbar_wait(&full[s], (uint32_t)(it / kStages) & 1u, &abort_flag, a.err);
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t xa = smem_u32(smem + (size_t)s * kStageBytes);
                     const uint32_t wa = xa + kXTileBytes;
+                    if (kb < a.KB) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32), idesc,
-                                    (kb | kk) != 0);
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32),
+                                        idesc, (kb | kk) != 0);
+                    } else {
+                        // A: [hi j0..15 | hi j16..31 | lo j0..15 | lo j16..31]; B: page slices
+                        // (0,1) hold j0..15, (2,3) hold j16..31
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32),
+                                        sdesc_k_none(wa + (kk & 1) * 2 * kPageSliceBytes,
+                                                     kPageSliceBytes, 128),
+                                        idesc, 1u);
+                    }
                     mma_commit(&empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[buf]);
@@ -160,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int tile = blockIdx.x; tile < a.num_tiles; tile += gridDim.x, ++tc) {
             int m, n;
             tile_coords(tile, a, m, n);
+            const TileLora tl = tile_lora(m, a, pool);
             const int buf = tc & 1;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(tc >> 1) & 1u, &abort_flag, a.err);
@@ -171,14 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool row_ok = t < a.T;
             int np = 0;
             const int32_t *pages = nullptr;
-            const float *vrow = nullptr;
-            if (row_ok && a.ids != nullptr) {
+            const uint16_t *hrow = nullptr;
+            if (tl.mode == 2 && row_ok) {  // several adapters: this row's own expand
                 const int id = a.ids[t];
                 if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
                     const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
                     np = row[SLOT_NPAGES];
                     pages = row + SLOT_PAGES;
-                    vrow = a.V + (size_t)t * a.ldv;
+                    hrow = a.Vhl + (size_t)t * a.ldh;
                 }
             }
             uint16_t *yrow = a.Y + (size_t)t * a.d_out;
@@ -192,9 +265,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
                 for (int q = 0; q < np; ++q) {
-                    const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
-                    const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
-                    const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                    const uint16_t *g = hrow + (q / 4) * 64 + (q % 4) * 8;
+                    const uint4 h = *reinterpret_cast<const uint4 *>(g);
+                    const uint4 l = *reinterpret_cast<const uint4 *>(g + 32);
+                    const float vv[8] = {bf16_lo(h.x) + bf16_lo(l.x), bf16_hi(h.x) + bf16_hi(l.x),
+                                         bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
+                                         bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
+                                         bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
                     const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
@@ -234,9 +311,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, int T,
-                                const int32_t *ids, const PoolDev &pool, const float *V, int ldv,
-                                uint16_t *Y, int num_sms, int *err, cudaStream_t stream)
+cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                const CUtensorMap &tmV, int T, const int32_t *ids,
+                                const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
+                                int num_sms, int *err, cudaStream_t stream)
 {
     PrefillArgs a{};
     a.T = T;
@@ -247,8 +325,9 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, 
     a.tiles_n = (pool.d_out + kBN - 1) / kBN;
     a.num_tiles = a.tiles_m * a.tiles_n;
     a.ids = ids;
-    a.V = V;
-    a.ldv = ldv;
+    a.tile_info = tile_info;
+    a.Vhl = Vhl;
+    a.ldh = ldh;
     a.Y = Y;
     a.err = err;
     if (a.num_tiles == 0) return cudaSuccess;
@@ -256,7 +335,7 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, 
     cudaError_t e = ensure_smem_attr((const void *)gemm_prefill_kernel, smem);
     if (e != cudaSuccess) return e;
     const int grid = a.num_tiles < num_sms ? a.num_tiles : num_sms;
-    gemm_prefill_kernel<<<grid, kThreads, smem, stream>>>(tmX, tmW, a, pool);
+    gemm_prefill_kernel<<<grid, kThreads, smem, stream>>>(tmX, tmW, tmV, a, pool);
     return cudaGetLastError();
 }
 

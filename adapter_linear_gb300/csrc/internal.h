@@ -45,7 +45,12 @@ struct SegTables {
     int32_t *seg_start;  // [max_seg + 1]
     int32_t *seg_slot;   // [max_seg]
     int32_t *seg_ublk;   // [max_seg + 1]  prefix of ceil(len / kShrinkRows)
+    int32_t *tile_info;  // [ceil(T / 128)]  adapters of each 128-token tile in token
+                         // order: the slot if all its tokens with an adapter share one,
+                         // kTileNoAdapter, or kTileMixed
 };
+constexpr int kTileNoAdapter = -1;
+constexpr int kTileMixed = -2;
 
 struct PoolDev {
     const uint16_t *A_pages;  // bf16 bits
@@ -63,13 +68,10 @@ size_t seg_build_smem_bytes(int max_adapters);
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
                              int *err, cudaStream_t stream);
 
-// Decode shrink (CUDA cores): V[t, 8q+jj] = s_i * X[t,:] . A_i[:, 8q+jj]
-cudaError_t launch_shrink_simt(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs,
-                               float *V, int ldv, cudaStream_t stream);
-
-// Prefill shrink (tcgen05): same result, 128-token units per segment.
+// Prefill shrink (tcgen05), 128-token units per segment: writes s_i X[t,:] A_i as
+// bf16 hi/lo pairs grouped per 32 rank columns (see shrink.cu) into Vhl [T][ldh].
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
-                             int T, const PoolDev &pool, SegTables tabs, float *V, int ldv,
+                             int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
                              int num_sms, int *err, cudaStream_t stream);
 
 struct DecodePlan {
@@ -90,9 +92,12 @@ cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
                                  const int32_t *ids, const PoolDev &pool, const float *V,
                                  int ldv, uint16_t *Y, int *err, cudaStream_t stream);
 
-cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW, int T,
-                                const int32_t *ids, const PoolDev &pool, const float *V, int ldv,
-                                uint16_t *Y, int num_sms, int *err, cudaStream_t stream);
+// Prefill GEMM with the expand: tmV is a TMA map of Vhl [T x ldh] (box 128 x 64);
+// tile_info from the segment builder; ids == nullptr: base product only.
+cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
+                                const CUtensorMap &tmV, int T, const int32_t *ids,
+                                const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
+                                int num_sms, int *err, cudaStream_t stream);
 
 // Pack a row-major A (d_in x rank) and B (rank x d_out) into pool pages.
 cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,

@@ -34,7 +34,8 @@ struct lora_pool {
     int max_pages = 0;   // pages per adapter at max_rank
     int num_pages = 0;   // arena pages, page 0 = zero page
     int slot_stride = 0;
-    int ldv = 0;         // fp32 row stride of the low-rank intermediate
+    int ldv = 0;         // fp32 row stride of the decode path's low-rank intermediate
+    int ldh = 0;         // bf16 row stride of the prefill path's hi/lo intermediate
     uint16_t *A_pages = nullptr, *B_pages = nullptr;
     int32_t *d_slots = nullptr;
     std::vector<int32_t> h_slots;
@@ -48,8 +49,9 @@ struct lora_pool {
     // per-call scratch, sized for cap_T tokens
     int cap_T = 0;
     int32_t *order = nullptr, *hdr = nullptr, *seg_start = nullptr, *seg_slot = nullptr,
-            *seg_ublk = nullptr;
+            *seg_ublk = nullptr, *tile_info = nullptr;
     float *V = nullptr;
+    uint16_t *Vhl = nullptr;
     float *partials = nullptr;
     size_t partials_floats = 0;
     // device staging of lora_linear_host
@@ -122,7 +124,11 @@ void free_scratch(lora_pool *p)
     free_dev(p, p->seg_start, sizeof(int32_t) * seg_entries(p, T));
     free_dev(p, p->seg_slot, sizeof(int32_t) * seg_entries(p, T));
     free_dev(p, p->seg_ublk, sizeof(int32_t) * seg_entries(p, T));
+    free_dev(p, p->tile_info, sizeof(int32_t) * (size_t)((T + 127) / 128));
+    p->tile_info = nullptr;
     free_dev(p, p->V, sizeof(float) * (size_t)T * p->ldv);
+    free_dev(p, p->Vhl, sizeof(uint16_t) * (size_t)T * p->ldh);
+    p->Vhl = nullptr;
     free_dev(p, p->partials, sizeof(float) * p->partials_floats);
     p->order = p->hdr = p->seg_start = p->seg_slot = p->seg_ublk = nullptr;
     p->V = p->partials = nullptr;
@@ -144,7 +150,9 @@ lora_status ensure_scratch(lora_pool *p, int T)
         (st = alloc_dev(p, (void **)&p->seg_start, sizeof(int32_t) * se)) ||
         (st = alloc_dev(p, (void **)&p->seg_slot, sizeof(int32_t) * se)) ||
         (st = alloc_dev(p, (void **)&p->seg_ublk, sizeof(int32_t) * se)) ||
+        (st = alloc_dev(p, (void **)&p->tile_info, sizeof(int32_t) * (size_t)((T + 127) / 128))) ||
         (st = alloc_dev(p, (void **)&p->V, sizeof(float) * (size_t)T * p->ldv)) ||
+        (st = alloc_dev(p, (void **)&p->Vhl, sizeof(uint16_t) * (size_t)T * p->ldh)) ||
         (st = alloc_dev(p, (void **)&p->partials, sizeof(float) * pf))) {
         p->cap_T = T;
         p->partials_floats = pf;
@@ -164,6 +172,7 @@ SegTables seg_tables(const lora_pool *p)
     t.seg_start = p->seg_start;
     t.seg_slot = p->seg_slot;
     t.seg_ublk = p->seg_ublk;
+    t.tile_info = p->tile_info;
     return t;
 }
 
@@ -265,13 +274,18 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (!mark(0)) return LORA_ERR_CUDA;
         const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, 128);
         const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 256);
-        if (!tmW || !tmX) return LORA_ERR_ARG;
-        if (with_lora)
-            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, Xb, T, pd, tabs, p->V, p->ldv, p->num_sms,
+        const CUtensorMap *tmV = tmap_for(p, p->Vhl, p->ldh, T, 64, 128);
+        if (!tmW || !tmX || !tmV) return LORA_ERR_ARG;
+        if (with_lora) {
+            // rows of tokens without an adapter must read as zero in the expand
+            CUDA_TRY(cudaMemsetAsync(p->Vhl, 0, sizeof(uint16_t) * (size_t)T * p->ldh, stream));
+            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
                                       p->d_err, stream));
+        }
         if (!mark(1)) return LORA_ERR_CUDA;
-        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, T, with_lora ? ids : nullptr, pd, p->V, p->ldv,
-                                     Yb, p->num_sms, p->d_err, stream));
+        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, *tmV, T, with_lora ? ids : nullptr,
+                                     with_lora ? p->tile_info : nullptr, pd, p->Vhl, p->ldh, Yb,
+                                     p->num_sms, p->d_err, stream));
         if (!mark(2)) return LORA_ERR_CUDA;
     }
     p->n_calls += 1;
@@ -332,6 +346,7 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
     p->num_pages = max_adapters * p->max_pages + 1;
     p->slot_stride = ((SLOT_PAGES + p->max_pages + 3) / 4) * 4;
     p->ldv = ((p->max_pages * kRankPage + 15) / 16) * 16;
+    p->ldh = 2 * (((p->max_pages * kRankPage + 31) / 32) * 32);
     p->h_slots.assign((size_t)max_adapters * p->slot_stride, 0);
     p->free_pages.reserve(p->num_pages - 1);
     for (int pg = p->num_pages - 1; pg >= 1; --pg) p->free_pages.push_back(pg);

@@ -172,6 +172,29 @@ __global__ void __launch_bounds__(kSegThreads, 1)
         }
         __syncwarp();
     }
+
+    // ---- D: adapters of each 128-token tile (in token order), for the prefill GEMM
+    const int ntile = (T + 127) / 128;
+    for (int tile = warp; tile < ntile; tile += kSegWarps) {
+        int lo = 0x7fffffff, hi = -1;
+        for (int i = lane; i < 128; i += 32) {
+            const int t = tile * 128 + i;
+            if (t < T) {
+                bool unused = false;
+                const int key = cache_keys ? keys[t] : token_key(ids[t], pool, unused);
+                if (key > 0) {
+                    lo = min(lo, key - 1);
+                    hi = max(hi, key - 1);
+                }
+            }
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+        if (lane == 0) tabs.tile_info[tile] = hi < 0 ? kTileNoAdapter : (lo == hi ? hi : kTileMixed);
+    }
 }
 
 }  // namespace

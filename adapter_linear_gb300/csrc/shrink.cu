@@ -1,114 +1,25 @@
-// shrink.cu -- the low-rank "shrink" V = s_i * X[t,:] A_i for every token with
-// an adapter: the low-dimensional intermediate that the LoRA-Land blog
-// (核心实现解析 / 2) forms first, so that the extra work stays a small
-// fraction of the base product. V is fp32 [T][ldv], indexed by token; the
-// scale s_i = alpha_i / r_i is folded in here. Columns of the pages beyond an
-// adapter's rank come out as exact zeros (zero-padded pages).
+// shrink.cu -- the prefill path's low-rank "shrink" V = s_i * X[t,:] A_i for
+// every token with an adapter: the low-dimensional intermediate that the
+// LoRA-Land blog (核心实现解析 / 2) forms first, so that the extra work stays a
+// small fraction of the base product. (The decode path computes it inside its
+// GEMM kernel.) The scale s_i = alpha_i / r_i is folded in here.
 //
-// Two kernels compute the same V:
-//  * shrink_simt_kernel (decode batches): one CTA per (segment, page). The
-//    A page (8 x d_in bf16) is read once with 128-bit loads and applied to
-//    every token of the segment, four tokens at a time; the 32 partial dot
-//    products per thread are reduced with a warp transpose-reduce and one
-//    shared-memory pass.
-//  * shrink_tc_kernel (prefill batches): persistent; one unit = up to 128
-//    tokens of one segment. tcgen05 MMA M=128 (tokens) x N=16..256 (rank rows,
-//    padded with the zero page) x K=d_in, operands staged by TMA (X rows when
-//    the segment's tokens are contiguous, else gathered by the producer warp
-//    into the same 128-byte-swizzled layout), fp32 accumulator in TMEM,
-//    double-buffered so one unit's epilogue overlaps the next unit's MMAs.
+// shrink_tc_kernel: persistent; one unit = up to 128 tokens of one segment
+// (tokens grouped by adapter). tcgen05 MMA M=128 (tokens) x N=16..256 (rank
+// rows, padded with the zero page) x K=d_in, operands staged by TMA (X rows
+// when the segment's tokens are contiguous, else gathered by the producer warp
+// into the same 128-byte-swizzled layout), fp32 accumulator in TMEM,
+// double-buffered so one unit's epilogue overlaps the next unit's MMAs.
+//
+// Output Vhl, bf16 [T][ldh], row = token: each fp32 value v is stored as the
+// pair hi = bf16(v), lo = bf16(v - hi) (hi + lo carries about 16 significant
+// bits), grouped per 32 rank columns as [hi 0..31 | lo 0..31] [hi 32..63 | ...],
+// so a 64-column TMA box is exactly the A operand of four MMA K-steps of the
+// expand in the prefill GEMM. Columns past an adapter's rank, up to its last
+// 32-column group, are written as zeros.
 #include "device_common.cuh"
 
 namespace lora {
-
-// ============================================================ CUDA-core shrink
-
-namespace {
-
-constexpr int kSimtThreads = 256;
-constexpr int kTokGroup = 4;
-
-__global__ void __launch_bounds__(kSimtThreads)
-    shrink_simt_kernel(const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
-                       float *__restrict__ V, int ldv)
-{
-    const int q = blockIdx.x % pool.max_pages;
-    const int s = blockIdx.x / pool.max_pages;
-    if (s >= tabs.hdr[HDR_NUMSEG]) return;
-    const int slot = tabs.seg_slot[s];
-    const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
-    const int npages = row[SLOT_NPAGES];
-    if (q >= npages) return;
-    const float scale = __int_as_float(row[SLOT_SCALE]);
-    const int page = row[SLOT_PAGES + q];
-    const int d_in = pool.d_in;
-    const uint16_t *Ap = pool.A_pages + (size_t)page * kRankPage * d_in;
-    const int p0 = tabs.seg_start[s], p1 = tabs.seg_start[s + 1];
-    const int nchunk = d_in / 8;  // 16-byte chunks along k
-
-    __shared__ float red[kSimtThreads / 32][32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-    for (int pb = p0; pb < p1; pb += kTokGroup) {
-        const int nt = min(kTokGroup, p1 - pb);
-        int tok[kTokGroup];
-#pragma unroll
-        for (int i = 0; i < kTokGroup; ++i) tok[i] = tabs.order[pb + min(i, nt - 1)];
-
-        float v[kTokGroup * kRankPage];
-#pragma unroll
-        for (int i = 0; i < kTokGroup * kRankPage; ++i) v[i] = 0.f;
-
-        for (int c = threadIdx.x; c < nchunk; c += kSimtThreads) {
-            uint4 a[kRankPage];
-#pragma unroll
-            for (int jj = 0; jj < kRankPage; ++jj) a[jj] = ldg_nc_v4(Ap + (size_t)jj * d_in + c * 8);
-            uint4 x[kTokGroup];
-#pragma unroll
-            for (int i = 0; i < kTokGroup; ++i)
-                x[i] = (i < nt) ? ldg_nc_v4(X + (size_t)tok[i] * d_in + c * 8) : make_uint4(0, 0, 0, 0);
-#pragma unroll
-            for (int i = 0; i < kTokGroup; ++i)
-#pragma unroll
-                for (int jj = 0; jj < kRankPage; ++jj)
-                    v[i * kRankPage + jj] = dot8_bf16(x[i], a[jj], v[i * kRankPage + jj]);
-        }
-
-        // warp transpose-reduce: afterwards lane l holds the warp sum of v[l]
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            const bool upper = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < o; ++i) {
-                const float send = upper ? v[i] : v[i + o];
-                const float keep = upper ? v[i + o] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-        }
-        red[warp][lane] = v[0];
-        __syncthreads();
-        if (warp == 0) {
-            float tot = 0.f;
-#pragma unroll
-            for (int w = 0; w < kSimtThreads / 32; ++w) tot += red[w][lane];
-            const int i = lane / kRankPage, jj = lane % kRankPage;
-            if (i < nt) V[(size_t)tok[i] * ldv + q * kRankPage + jj] = scale * tot;
-        }
-        __syncthreads();
-    }
-}
-
-}  // namespace
-
-cudaError_t launch_shrink_simt(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs,
-                               float *V, int ldv, cudaStream_t stream)
-{
-    const int max_seg = T < pool.max_adapters ? T : pool.max_adapters;
-    const int grid = max_seg * pool.max_pages;
-    if (grid == 0) return cudaSuccess;
-    shrink_simt_kernel<<<grid, kSimtThreads, 0, stream>>>(X, pool, tabs, V, ldv);
-    return cudaGetLastError();
-}
 
 // ========================================================== tensor-core shrink
 
@@ -148,7 +59,7 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const 
 __global__ void __launch_bounds__(kTcThreads, 1)
     shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
                      const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
-                     float *__restrict__ V, int ldv, int nmax, int stages, uint32_t tmem_cols,
+                     uint16_t *__restrict__ Vhl, int ldh, int nmax, int stages, uint32_t tmem_cols,
                      int *err)
 {
     extern __shared__ uint8_t shrink_smem_raw[];
@@ -300,21 +211,36 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int p = ui.p0 + r;
             const bool valid = p < ui.p1;
             const int tok = valid ? tabs.order[p] : 0;
-            float *vrow = V + (size_t)tok * ldv;
+            // s * (X A) as a bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi)), grouped
+            // per 32 rank columns: [hi 0..31 | lo 0..31] [hi 32..63 | lo 32..63] ...
+            uint16_t *hrow = Vhl + (size_t)tok * ldh;
             for (int col = 0; col < ui.n; col += 16) {
                 uint32_t v[16];
                 tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * nmax + col), v);
                 if (valid) {
+                    uint32_t hi[8], lo[8];
 #pragma unroll
-                    for (int j = 0; j < 16; j += 4) {
-                        float4 o;
-                        o.x = ui.scale * __uint_as_float(v[j + 0]);
-                        o.y = ui.scale * __uint_as_float(v[j + 1]);
-                        o.z = ui.scale * __uint_as_float(v[j + 2]);
-                        o.w = ui.scale * __uint_as_float(v[j + 3]);
-                        *reinterpret_cast<float4 *>(vrow + col + j) = o;
+                    for (int j = 0; j < 16; j += 2) {
+                        const float a0 = ui.scale * __uint_as_float(v[j]);
+                        const float a1 = ui.scale * __uint_as_float(v[j + 1]);
+                        const uint32_t h = pack_bf16x2(a0, a1);
+                        hi[j / 2] = h;
+                        lo[j / 2] = pack_bf16x2(a0 - bf16_lo(h), a1 - bf16_hi(h));
                     }
+                    uint16_t *dst = hrow + (col / 32) * 64 + (col % 32);
+                    *reinterpret_cast<uint4 *>(dst) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                    *reinterpret_cast<uint4 *>(dst + 8) = make_uint4(hi[4], hi[5], hi[6], hi[7]);
+                    *reinterpret_cast<uint4 *>(dst + 32) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    *reinterpret_cast<uint4 *>(dst + 40) = make_uint4(lo[4], lo[5], lo[6], lo[7]);
                 }
+            }
+            if (valid && (ui.n % 32) != 0) {  // the rest of the last 32-column group: zeros
+                uint16_t *dst = hrow + (ui.n / 32) * 64 + 16;
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(dst) = z;
+                *reinterpret_cast<uint4 *>(dst + 8) = z;
+                *reinterpret_cast<uint4 *>(dst + 32) = z;
+                *reinterpret_cast<uint4 *>(dst + 40) = z;
             }
             tc_fence_before_sync();
             __syncwarp();
@@ -340,7 +266,7 @@ uint32_t pow2_cols(uint32_t n)
 }  // namespace
 
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
-                             int T, const PoolDev &pool, SegTables tabs, float *V, int ldv,
+                             int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
                              int num_sms, int *err, cudaStream_t stream)
 {
     const int nmax = ((pool.max_pages * kRankPage + 15) / 16) * 16;
@@ -356,7 +282,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, con
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
-    shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, X, pool, tabs, V, ldv, nmax,
+    shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, X, pool, tabs, Vhl, ldh, nmax,
                                                           stages, tmem_cols, err);
     return cudaGetLastError();
 }

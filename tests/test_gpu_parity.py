@@ -311,3 +311,28 @@ def test_pool_management_errors():
     got = run(pool, prob, 0)
     ref, _ = ref_of(prob)
     assert_parity(got, ref, "host-loaded adapter")
+
+
+def test_prefill_expand_tile_modes():
+    """Tiles with one adapter (the tensor-core expand, incl. base-only rows inside them),
+    a tile with several adapters (the CUDA-core expand), ranks that are not multiples
+    of 32, a d_out tail shorter than the 256-column tile and a ragged last token tile."""
+    d_in, d_out, seed, T = 136, 200, 57, 350
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d_in), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.1)
+    ranks = [5, 40, 13, 8]
+    ads = {i: L.make_adapter(seed, i, d_in, d_out, r, 2.0 * r, std=0.2) for i, r in enumerate(ranks)}
+    ids = np.full(T, -1, np.int32)
+    ids[0:128] = 0
+    ids[5:9] = -1                  # base rows inside a single-adapter tile
+    ids[128:256] = 1
+    g = L.rng_for(seed, L.ROLE_IDS)
+    ids[256:] = g.integers(-1, 4, size=T - 256)   # mixed, ragged tile
+    prob = L.Problem("tile_modes", d_in, d_out, X, W, ids, ads, 4, 40, seed)
+    pool = load_pool(al, prob)
+    got = run(pool, prob, PATHS["prefill"])
+    ref, base = ref_of(prob)
+    assert_parity(got, ref, "prefill tile modes")
+    assert_routing(got, ref, base, ids, "prefill tile modes")
+    got_d = run(pool, prob, PATHS["decode"]) if T <= 256 else None
+    assert got_d is None
