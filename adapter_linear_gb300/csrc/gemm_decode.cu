@@ -6,13 +6,13 @@
 //    * operands swapped: D[n, t] = sum_k W[n,k] X[t,k], so the long d_out side
 //      is the MMA's M (128 rows of W per tile) and the T tokens are its N
 //      (T rounded up to 16; rows past T read as zero from TMA);
-//    * stream-K: the (tile, 64-wide k-block) iteration space is cut into G
+//    * stream-K: the (tile, 128-wide k-block) iteration space is cut into G
 //      equal contiguous ranges, one per CTA (G = number of SMs, or fewer for
 //      small problems), so every SM streams the same share of W. A range
 //      touches at most two tiles; each touched tile gets its own TMEM
 //      accumulator and is written as an fp32 partial sum [cta][0|1][T][128];
-//    * warp roles: warp 4 issues TMA loads (W tile 128x64, X tile T'x64,
-//      128-byte swizzle) into a multi-stage ring and starts before TMEM is
+//    * warp roles: warp 4 issues TMA loads (per stage two W boxes 128x64 and two
+//      X boxes T'x64, 128-byte swizzle) into a multi-stage ring and starts before TMEM is
 //      allocated; warp 5 allocates TMEM and issues tcgen05 MMAs (M=128, N=T',
 //      K=16); warps 0-3, idle until the accumulators are ready, first compute
 //      the low-rank shrink V[t, 8q..8q+7] = s_i X[t,:] A_i[:, 8q..8q+7] for
@@ -34,7 +34,11 @@ namespace lora {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr int kWTileBytes = 128 * 128;  // 128 rows x 64 bf16
+constexpr int kWTileBytes = 128 * 128;  // one TMA box of W: 128 rows x 64 bf16
+// Two 64-wide boxes per stage (k-block = 128 columns): half the barrier round
+// trips per byte and longer runs per W row than one box, measured ~2.5 us
+// faster per q_proj decode step; four boxes were no faster.
+constexpr int kBoxes = 2;
 constexpr uint32_t kBarSetup = 1;       // named barrier: all six warps, setup done
 constexpr uint32_t kBarShrink = 2;      // named barrier: the four epilogue warps
 
@@ -94,8 +98,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     extern __shared__ uint8_t dec_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(dec_smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t x_bytes = (uint32_t)p.ntok * 128;
-    const uint32_t stage_bytes = kWTileBytes + x_bytes;
+    const uint32_t x_box = (uint32_t)p.ntok * 128;  // one TMA box of X
+    const uint32_t w_bytes = kBoxes * kWTileBytes;
+    const uint32_t stage_bytes = w_bytes + kBoxes * x_box;
     const int stages = p.stages;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
     uint64_t *empty = full + stages;
@@ -140,13 +145,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < pre; ++i) {
                 const int u = u0 + i, tile = u / p.KB, kb = u - tile * p.KB;
                 mbar_arrive_expect_tx(&full[i], stage_bytes);
-                tma_load_2d_hint(smem + (size_t)i * stage_bytes, &tmW, &full[i], kb * 64, tile * 128,
-                                 pol_w);
+                for (int b = 0; b < kBoxes; ++b)
+                    tma_load_2d_hint(smem + (size_t)i * stage_bytes + b * kWTileBytes, &tmW, &full[i],
+                                     (kb * kBoxes + b) * 64, tile * 128, pol_w);
             }
             pdl_wait_prior();
             for (int i = 0; i < pre; ++i) {
                 const int kb = (u0 + i) % p.KB;
-                tma_load_2d(smem + (size_t)i * stage_bytes + kWTileBytes, &tmX, &full[i], kb * 64, 0);
+                for (int b = 0; b < kBoxes; ++b)
+                    tma_load_2d(smem + (size_t)i * stage_bytes + w_bytes + b * x_box, &tmX, &full[i],
+                                (kb * kBoxes + b) * 64, 0);
             }
             int it = pre;
             for (int u = u0 + pre; u < u1; ++u, ++it) {
@@ -155,8 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int tile = u / p.KB, kb = u - tile * p.KB;
                 uint8_t *ws = smem + (size_t)s * stage_bytes;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
-                tma_load_2d_hint(ws, &tmW, &full[s], kb * 64, tile * 128, pol_w);
-                tma_load_2d(ws + kWTileBytes, &tmX, &full[s], kb * 64, 0);
+                for (int b = 0; b < kBoxes; ++b) {
+                    tma_load_2d_hint(ws + b * kWTileBytes, &tmW, &full[s], (kb * kBoxes + b) * 64,
+                                     tile * 128, pol_w);
+                    tma_load_2d(ws + w_bytes + b * x_box, &tmX, &full[s], (kb * kBoxes + b) * 64, 0);
+                }
             }
             for (int i = 0; i < stages && i < it; ++i) {
                 const int j = it - 1 - i;
@@ -184,12 +195,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int seg = tile - tile0;
                 const uint32_t d = tmem + (uint32_t)(seg * p.ntok);
                 const uint32_t wa = smem_u32(smem + (size_t)s * stage_bytes);
-                const uint32_t xa = wa + kWTileBytes;
+                const uint32_t xa = wa + w_bytes;
                 const bool first = (kb == 0) || (u == u0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_ss(d, sdesc_k_sw128(wa + kk * 32), sdesc_k_sw128(xa + kk * 32), idesc,
-                                (first && kk == 0) ? 0u : 1u);
+                for (int b = 0; b < kBoxes; ++b)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(d, sdesc_k_sw128(wa + b * kWTileBytes + kk * 32),
+                                    sdesc_k_sw128(xa + b * x_box + kk * 32), idesc,
+                                    (first && b == 0 && kk == 0) ? 0u : 1u);
                 mma_commit(&empty[s]);
                 if (u == u1 - 1 || kb == p.KB - 1) mma_commit(&acc_full[seg]);
             }
@@ -353,14 +367,14 @@ DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms)
     p.T = T;
     p.ntok = ((T + 15) / 16) * 16;
     if (p.ntok < 16) p.ntok = 16;
-    p.KB = (d_in + 63) / 64;
+    p.KB = (d_in + 64 * kBoxes - 1) / (64 * kBoxes);
     p.n_tiles = (d_out + 127) / 128;
     p.U = p.n_tiles * p.KB;
     int G = num_sms;
     if (G > p.U) G = p.U;
     if (G < p.n_tiles) G = p.n_tiles;  // ranges never span more than two tiles
     p.G = G;
-    const size_t stage_bytes = kWTileBytes + (size_t)p.ntok * 128;
+    const size_t stage_bytes = kBoxes * (kWTileBytes + (size_t)p.ntok * 128);
     int stages = (int)((200 * 1024) / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
