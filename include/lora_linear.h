@@ -141,9 +141,11 @@ lora_status lora_unload_adapter(lora_pool_t pool, int slot);
 /*
  * The hot path. For every token t: Y[t] = X[t] W_base^T + s_i (X[t] A_i) B_i
  * with i = token_adapter_ids[t]; id -1 gives the base product only (the vLLM
- * tutorial's 按请求切换 LoRA: no adapter -> pure base). The batch is grouped
- * by adapter with a stable sort ("Grouped Multi-LoRA Execution", LoRA-Land
- * blog section 2); the low-rank intermediate X A_i is kept in fp32 and the
+ * tutorial's 按请求切换 LoRA: no adapter -> pure base). Prefill-sized batches
+ * are grouped by adapter with a stable sort ("Grouped Multi-LoRA Execution",
+ * LoRA-Land blog section 2); decode-sized batches (T <= 256) gather each
+ * token's adapter pages directly. The low-rank intermediate X A_i is kept in
+ * fp32 (decode) or as an fp32-accurate bf16 hi + lo pair (prefill), and the
  * result is rounded to bf16 once.
  *   X: device bf16 T x d_in.  W_base: device bf16 d_out x d_in.
  *   token_adapter_ids: device int32[T].  Y: device bf16 T x d_out (written
