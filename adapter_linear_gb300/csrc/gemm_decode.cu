@@ -258,6 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
 constexpr int kFinishCols = 8;
 constexpr int kPrefetchPages = 2;     // B pages fetched before the GEMM has finished
+constexpr int kFinishBatch = 8;       // partial loads in flight per thread
 
 __device__ __forceinline__ void add8(float (&acc)[kFinishCols], const float *src)
 {
@@ -325,7 +326,25 @@ __global__ void __launch_bounds__(kFinishThreads)
 
     float acc[kFinishCols] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     add8(acc, partials + ((size_t)(c_lo * 2 + seg_lo) * p.T + t) * 128 + nl);
-    for (int c = c_lo + 1; c <= c_hi; ++c) add8(acc, partials + ((size_t)(c * 2) * p.T + t) * 128 + nl);
+    // the other contributors' first partials, kFinishBatch loads in flight at a time
+    // (summed in CTA order all the same)
+    const size_t stride = (size_t)2 * p.T * 128;
+    const float *src = partials + ((size_t)(c_lo + 1) * 2 * p.T + t) * 128 + nl;
+    for (int c0 = c_lo + 1; c0 <= c_hi; c0 += kFinishBatch, src += kFinishBatch * stride) {
+        float4 b[kFinishBatch][2];
+#pragma unroll
+        for (int i = 0; i < kFinishBatch; ++i)
+            if (c0 + i <= c_hi) {
+                b[i][0] = *reinterpret_cast<const float4 *>(src + i * stride);
+                b[i][1] = *reinterpret_cast<const float4 *>(src + i * stride + 4);
+            }
+#pragma unroll
+        for (int i = 0; i < kFinishBatch; ++i)
+            if (c0 + i <= c_hi) {
+                acc[0] += b[i][0].x; acc[1] += b[i][0].y; acc[2] += b[i][0].z; acc[3] += b[i][0].w;
+                acc[4] += b[i][1].x; acc[5] += b[i][1].y; acc[6] += b[i][1].z; acc[7] += b[i][1].w;
+            }
+    }
     const float *vrow = V + (size_t)t * ldv;
     for (int q = 0; q < np; ++q) {
         float v[8];
