@@ -280,6 +280,10 @@ __global__ void __launch_bounds__(kFinishThreads)
                          const int32_t *__restrict__ ids, PoolDev pool, const float *__restrict__ V,
                          int ldv, uint16_t *__restrict__ Y, int *err)
 {
+    // The next call's GEMM may launch now: its CTAs take an SM as soon as this call's
+    // GEMM CTA leaves it and stream their first W tiles; everything they write comes
+    // after their own wait for this kernel.
+    pdl_launch_dependents();
     const int n0 = (blockIdx.x * kFinishThreads + threadIdx.x) * kFinishCols;
     const int t = blockIdx.y;
     const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
@@ -321,7 +325,6 @@ __global__ void __launch_bounds__(kFinishThreads)
 
     // ---- partials and V are written by the GEMM kernel
     pdl_wait_prior();
-    pdl_launch_dependents();  // the next call's GEMM may start streaming its weights
     if (!col_ok) return;
 
     float acc[kFinishCols] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
