@@ -27,6 +27,9 @@ namespace {
 
 constexpr int kTcThreads = 192;          // warps 0-3 epilogue, 4 producer, 5 MMA
 constexpr int kXTileBytes = 128 * 128;   // 128 rows x 64 bf16
+// Two 64-column boxes per pipeline stage (k-block = 128 columns): fewer barrier
+// round trips per byte and twice the bytes in flight per stage.
+constexpr int kSBoxes = 2;
 
 struct UnitInfo {
     int p0, p1;       // positions in `order`
@@ -65,8 +68,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     extern __shared__ uint8_t shrink_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(shrink_smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t p_bytes = (uint32_t)nmax * 128;
-    const uint32_t stage_bytes = kXTileBytes + p_bytes;
+    const uint32_t p_bytes = (uint32_t)nmax * 128;  // one box of the A pages
+    const uint32_t x_bytes = kSBoxes * kXTileBytes;
+    const uint32_t stage_bytes = x_bytes + kSBoxes * p_bytes;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
     uint64_t *empty = full + stages;
     uint64_t *acc_full = empty + stages;  // [2]
@@ -78,7 +82,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = tabs.hdr[HDR_UNITS];
     const int d_in = pool.d_in;
-    const int KB = (d_in + 63) / 64;
+    const int KB = (d_in + 64 * kSBoxes - 1) / (64 * kSBoxes);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < stages; ++i) {
@@ -117,7 +121,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 contiguous &= (tabs.order[ui.p0 + r] == row0 + r);
             contiguous = __all_sync(0xffffffffu, contiguous);
             const int npad = ui.n / kRankPage;
-            const uint32_t bytes = (uint32_t)npad * 1024u + (contiguous ? kXTileBytes : 0u);
+            const uint32_t bytes = kSBoxes * ((uint32_t)npad * 1024u + (contiguous ? kXTileBytes : 0u));
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++kb, ++it) {
                 const int s = it % stages;
@@ -126,29 +130,35 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) break;
                 uint8_t *xs = smem + (size_t)s * stage_bytes;
-                uint8_t *ps = xs + kXTileBytes;
+                uint8_t *ps = xs + x_bytes;
                 if (!contiguous) {
-                    // gather 128 rows x 64 bf16 into the 128-byte-swizzled layout
+                    // gather 128 rows x 64 bf16 per box into the 128-byte-swizzled layout
                     for (int r = lane; r < 128; r += 32) {
                         const int p = ui.p0 + r;
                         const int tok = (p < ui.p1) ? tabs.order[p] : -1;
 #pragma unroll
-                        for (int c = 0; c < 8; ++c) {
-                            const int k = kb * 64 + c * 8;
-                            uint4 val = make_uint4(0, 0, 0, 0);
-                            if (tok >= 0 && k < d_in) val = ldg_nc_v4(X + (size_t)tok * d_in + k);
-                            *reinterpret_cast<uint4 *>(xs + r * 128 + ((c ^ (r & 7)) << 4)) = val;
-                        }
+                        for (int b = 0; b < kSBoxes; ++b)
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const int k = (kb * kSBoxes + b) * 64 + c * 8;
+                                uint4 val = make_uint4(0, 0, 0, 0);
+                                if (tok >= 0 && k < d_in) val = ldg_nc_v4(X + (size_t)tok * d_in + k);
+                                *reinterpret_cast<uint4 *>(xs + b * kXTileBytes + r * 128 +
+                                                           ((c ^ (r & 7)) << 4)) = val;
+                            }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                 }
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&full[s], bytes);
-                    if (contiguous) tma_load_2d(xs, &tmX, &full[s], kb * 64, row0);
-                    for (int q = 0; q < npad; ++q) {
-                        const int page = q < ui.npages ? ui.pages[q] : 0;
-                        tma_load_2d(ps + q * 1024, &tmA, &full[s], kb * 64, page * kRankPage);
+                    for (int b = 0; b < kSBoxes; ++b) {
+                        const int k0 = (kb * kSBoxes + b) * 64;
+                        if (contiguous) tma_load_2d(xs + b * kXTileBytes, &tmX, &full[s], k0, row0);
+                        for (int q = 0; q < npad; ++q) {
+                            const int page = q < ui.npages ? ui.pages[q] : 0;
+                            tma_load_2d(ps + b * p_bytes + q * 1024, &tmA, &full[s], k0, page * kRankPage);
+                        }
                     }
                 }
                 __syncwarp();
@@ -182,11 +192,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     if (!ok) break;
                     tc_fence_after_sync();
                     const uint32_t xa = smem_u32(smem + (size_t)s * stage_bytes);
-                    const uint32_t pa = xa + kXTileBytes;
+                    const uint32_t pa = xa + x_bytes;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(pa + kk * 32),
-                                    idesc, (kb | kk) != 0);
+                    for (int b = 0; b < kSBoxes; ++b)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss(d, sdesc_k_sw128(xa + b * kXTileBytes + kk * 32),
+                                        sdesc_k_sw128(pa + b * p_bytes + kk * 32), idesc,
+                                        (kb | b | kk) != 0);
                     mma_commit(&empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[buf]);
@@ -270,7 +283,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, con
                              int num_sms, int *err, cudaStream_t stream)
 {
     const int nmax = ((pool.max_pages * kRankPage + 15) / 16) * 16;
-    const size_t stage_bytes = kXTileBytes + (size_t)nmax * 128;
+    const size_t stage_bytes = kSBoxes * (kXTileBytes + (size_t)nmax * 128);
     int stages = (int)((200 * 1024) / stage_bytes);
     if (stages > 6) stages = 6;
     if (stages < 2) stages = 2;
