@@ -35,8 +35,9 @@ EXPORTS = (
     "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
     "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
-    "lora_base_linear_noalloc",
+    "lora_base_linear_noalloc", "lora_linear_grouped",
 )
+LORA_MAX_GROUP = 8
 LORA_KERNEL_SLOTS = 4
 KERNEL_SLOT_NAMES = ("segment_build", "shrink", "base_gemm", "finish_expand")
 
@@ -82,6 +83,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_pool_enable_timing": [vp, i32],
         "lora_pool_kernel_times": [vp, vp],
         "lora_base_linear_noalloc": [vp, vp, i32, i32, i32, vp, vp],
+        "lora_linear_grouped": [i32, vp, vp, vp, vp, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -148,6 +150,18 @@ def lora_linear(pool: int, X, W_base, ids, T: int, Y, stream=None) -> int:
 def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream=None) -> int:
     return load_library().lora_linear_host(pool, _ptr(X_host), _ptr(W_base), _ptr(ids_host), T,
                                            _ptr(Y_host), _stream(stream))
+
+
+def lora_linear_grouped(pools, X, W_base, ids, T: int, Y, stream=None) -> int:
+    """n layers that share the token ids in one decode launch chain: pools, X, W_base and Y
+    are equal-length sequences (pool handles and tensors / device pointers)."""
+    n = len(pools)
+    arr = ctypes.c_void_p * max(n, 1)
+    ph = arr(*[int(p) if p else None for p in pools])
+    xs = arr(*[_ptr(x) for x in X])
+    ws = arr(*[_ptr(w) for w in W_base])
+    ys = arr(*[_ptr(y) for y in Y])
+    return load_library().lora_linear_grouped(n, ph, xs, ws, _ptr(ids), T, ys, _stream(stream))
 
 
 def lora_base_linear(pool: int, X, W_base, T: int, Y, stream=None) -> int:
@@ -256,6 +270,18 @@ class LoraPool:
         _check(lora_linear_host(self.handle, X_host, W, ids_host, X_host.shape[0], Y_host, stream),
                "lora_linear_host")
         return Y_host
+
+    @staticmethod
+    def linear_grouped(pools, Xs, Ws, ids, Ys=None, stream=None):
+        """Y_m = lora_linear of pools[m] on (Xs[m], Ws[m]) for all m, with one set of ids,
+        in one launch chain on the decode path (one call per layer above 256 tokens)."""
+        import torch
+        T = ids.shape[0]
+        if Ys is None:
+            Ys = [torch.empty((T, p.d_out), dtype=torch.bfloat16, device=ids.device) for p in pools]
+        _check(lora_linear_grouped([p.handle for p in pools], Xs, Ws, ids, T, Ys, stream),
+               "lora_linear_grouped")
+        return Ys
 
     def base_linear(self, X, W, Y=None, stream=None):
         import torch

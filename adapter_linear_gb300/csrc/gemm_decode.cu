@@ -1,32 +1,38 @@
-// gemm_decode.cu -- the decode path (T <= 256): two kernels.
+// gemm_decode.cu -- the decode path (T <= 256): two kernels per call, for one
+// layer or for a group of layers that share the token ids (e.g. the target
+// modules of one transformer layer), described by one problem table.
 //
-// 1. gemm_decode_kernel: base product + the per-token low-rank shrink.
+// 1. gemm_decode_kernel: base products + the per-token low-rank shrink.
 //    At decode sizes the base GEMM is bound by reading W_base once from HBM, so
 //    the layout is chosen to stream W at full bandwidth on every SM:
 //    * operands swapped: D[n, t] = sum_k W[n,k] X[t,k], so the long d_out side
 //      is the MMA's M (128 rows of W per tile) and the T tokens are its N
 //      (T rounded up to 16; rows past T read as zero from TMA);
-//    * stream-K: the (tile, 128-wide k-block) iteration space is cut into G
-//      equal contiguous ranges, one per CTA (G = number of SMs, or fewer for
-//      small problems), so every SM streams the same share of W. A range
-//      touches at most two tiles; each touched tile gets its own TMEM
-//      accumulator and is written as an fp32 partial sum [cta][0|1][T][128];
+//    * stream-K: the problems' (tile, 128-wide k-block) units, concatenated in
+//      problem order, are cut into G equal contiguous ranges, one per CTA
+//      (G = number of SMs, or fewer for small problems), so every SM streams
+//      the same share of all the weights of the group. Every tile a range
+//      touches (a "segment" of the range) gets a TMEM accumulator from a small
+//      ring and is written out as an fp32 partial sum [cta][segment][T][128];
 //    * warp roles: warp 4 issues TMA loads (per stage two W boxes 128x64 and two
-//      X boxes T'x64, 128-byte swizzle) into a multi-stage ring and starts before TMEM is
-//      allocated; warp 5 allocates TMEM and issues tcgen05 MMAs (M=128, N=T',
-//      K=16); warps 0-3, idle until the accumulators are ready, first compute
-//      the low-rank shrink V[t, 8q..8q+7] = s_i X[t,:] A_i[:, 8q..8q+7] for
-//      the (token, page) pairs dealt to this CTA round-robin (a BGMV-style
-//      per-token gather: each pair reads one 8 x d_in A page with 128-bit
+//      X boxes T'x64, 128-byte swizzle) into a multi-stage ring -- the first
+//      ring's worth of W (a weight) before the wait on the previous kernel;
+//      warp 5 allocates TMEM and issues tcgen05 MMAs (M=128, N=T', K=16);
+//      warps 0-3, idle until the accumulators are ready, first compute the
+//      low-rank shrink V[t, 8q..8q+7] = s_i X[t,:] A_i[:, 8q..8q+7] for the
+//      (problem, token, page) triples dealt to this CTA round-robin (a
+//      BGMV-style per-token gather: each reads one 8 x d_in A page with 128-bit
 //      loads), so the adapter reads overlap the W stream; then they read the
 //      accumulators back with tcgen05.ld (TMEM lane = output row n) and store
 //      the partials.
 // 2. finish_decode_kernel (launched with programmatic stream serialization, so
-//    it is resident and has prefetched its B pages before the GEMM ends): per
+//    it is resident and has loaded its B pages before the GEMM ends): per
 //    output element, the partials of the CTAs that covered its tile are summed
 //    in CTA order (deterministic), the low-rank expand s_i V[t,:] B_i[:,n] is
 //    added from the interleaved B pages (one 16-byte load = 8 rank rows of one
 //    column; V already carries s_i), and the sum is rounded once to bf16.
+#include <utility>
+
 #include "device_common.cuh"
 
 namespace lora {
@@ -47,22 +53,42 @@ __host__ __device__ __forceinline__ int cta_start(int c, int U, int G)
     return (int)(((long long)c * U) / G);
 }
 
-struct ShrinkArgs {
-    const uint16_t *X;
-    const int32_t *ids;  // nullptr: base product only
-    float *V;
-    int ldv;
-};
+// Index into a plan's problem table: a compile-time 0 for a one-problem plan, so
+// its fields are read at fixed parameter offsets.
+template <int NP>
+__host__ __device__ __forceinline__ int pick(int m)
+{
+    return NP == 1 ? 0 : m;
+}
+
+// The problem that unit u belongs to: the last m whose first unit is <= u.
+template <class Plan>
+__host__ __device__ __forceinline__ int unit_problem(const Plan &p, int u)
+{
+    if (Plan::kNP == 1) return 0;
+    int m = 0;
+    for (int k = 1; k < p.n; ++k)
+        if (p.prob[k].u_begin <= u) m = k;
+    return m;
+}
+
+// Index of unit u's tile in the problems' concatenated tile order.
+template <class Plan>
+__host__ __device__ __forceinline__ int unit_tile(const Plan &p, int u)
+{
+    const DecodeProblem &q = p.prob[pick<Plan::kNP>(unit_problem(p, u))];
+    return q.g_begin + (u - q.u_begin) / q.KB;
+}
 
 // One (token, page) pair of the shrink, computed by the 128 threads of warps 0-3.
-__device__ __forceinline__ void shrink_pair(int t, int page, float scale, const PoolDev &pool,
-                                            const ShrinkArgs &sa, int q, float (*red)[8])
+__device__ __forceinline__ void shrink_pair(int t, int page, float scale, const DecodeProblem &pr,
+                                            int q, float (*red)[8])
 {
     const int tid = threadIdx.x;  // 0..127
     const int warp = tid >> 5, lane = tid & 31;
-    const int d_in = pool.d_in;
-    const uint16_t *Ap = pool.A_pages + (size_t)page * kRankPage * d_in;
-    const uint16_t *xr = sa.X + (size_t)t * d_in;
+    const int d_in = pr.pool.d_in;
+    const uint16_t *Ap = pr.pool.A_pages + (size_t)page * kRankPage * d_in;
+    const uint16_t *xr = pr.X + (size_t)t * d_in;
     float acc[kRankPage];
 #pragma unroll
     for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = 0.f;
@@ -85,15 +111,37 @@ __device__ __forceinline__ void shrink_pair(int t, int page, float scale, const 
     named_bar_sync(kBarShrink, 128);
     if (tid < kRankPage) {
         const float s = red[0][tid] + red[1][tid] + red[2][tid] + red[3][tid];
-        sa.V[(size_t)t * sa.ldv + q * kRankPage + tid] = scale * s;
+        pr.V[(size_t)t * pr.ldv + q * kRankPage + tid] = scale * s;
     }
     named_bar_sync(kBarShrink, 128);
 }
 
+// The current problem's unit bookkeeping, kept in registers while a loop walks
+// its units in order (reloaded when the walk crosses into the next problem).
+struct UnitCursor {
+    int m, ub, KB, gb, next_ub;
+    template <class Plan>
+    __device__ __forceinline__ void load(const Plan &p, int mm)
+    {
+        m = pick<Plan::kNP>(mm);
+        const DecodeProblem &q = p.prob[m];
+        ub = q.u_begin;
+        KB = q.KB;
+        gb = q.g_begin;
+        next_ub = Plan::kNP > 1 && m + 1 < p.n ? p.prob[pick<Plan::kNP>(m + 1)].u_begin : 0x7fffffff;
+    }
+    template <class Plan>
+    __device__ __forceinline__ void seek(const Plan &p, int u)
+    {
+        while (u >= next_ub) load(p, m + 1);
+    }
+};
+
+template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_decode_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       DecodePlan p, float *__restrict__ partials, int *err, PoolDev pool,
-                       ShrinkArgs sa)
+    gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
+                       const __grid_constant__ DecodePlanT<NP> p, const int32_t *__restrict__ ids,
+                       float *__restrict__ partials, int *err)
 {
     extern __shared__ uint8_t dec_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -101,11 +149,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t x_box = (uint32_t)p.ntok * 128;  // one TMA box of X
     const uint32_t w_bytes = kBoxes * kWTileBytes;
     const uint32_t stage_bytes = w_bytes + kBoxes * x_box;
-    const int stages = p.stages;
+    const int stages = p.stages, n_acc = p.n_acc;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)stages * stage_bytes);
     uint64_t *empty = full + stages;
-    uint64_t *acc_full = empty + stages;  // [2]
-    uint64_t *drain = acc_full + 2;
+    uint64_t *acc_full = empty + stages;     // [n_acc]
+    uint64_t *acc_empty = acc_full + n_acc;  // [n_acc]
+    uint64_t *drain = acc_empty + n_acc;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
     __shared__ int abort_flag;
     __shared__ float red[4][kRankPage];
@@ -116,8 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
     const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
-    const int tile0 = u0 / p.KB;
-    const int nseg = (u1 > u0) ? (u1 - 1) / p.KB - tile0 + 1 : 0;
+    const int g0 = unit_tile(p, u0);  // the tile of segment 0
+    const int nseg = u1 > u0 ? unit_tile(p, u1 - 1) - g0 + 1 : 0;
 
     if (warp == 4) {
         // ------------------------------------------------------------ producer
@@ -126,13 +175,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_init(&full[i], 1);
                 mbar_init(&empty[i], 1);
             }
-            mbar_init(&acc_full[0], 1);
-            mbar_init(&acc_full[1], 1);
+            for (int i = 0; i < n_acc; ++i) {
+                mbar_init(&acc_full[i], 1);
+                mbar_init(&acc_empty[i], 4);
+            }
             mbar_init(drain, 1);
             abort_flag = 0;
             fence_mbar_init();
-            tma_prefetch_map(&tmW);
-            tma_prefetch_map(&tmX);
+            for (int m = 0; m < p.n; ++m) {
+                tma_prefetch_map(&maps.W[m]);
+                tma_prefetch_map(&maps.X[m]);
+            }
         }
         __syncwarp();
         named_bar_arrive(kBarSetup, kThreads);  // barriers are ready; do not wait for TMEM
@@ -142,33 +195,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             // previous kernel in the stream has finished; X (and everything the epilogue
             // touches) only after the programmatic wait.
             const int pre = (u1 - u0) < stages ? (u1 - u0) : stages;
+            UnitCursor cur;
+            cur.load(p, unit_problem(p, u0));
             for (int i = 0; i < pre; ++i) {
-                const int u = u0 + i, tile = u / p.KB, kb = u - tile * p.KB;
+                const int u = u0 + i;
+                cur.seek(p, u);
+                const int lu = u - cur.ub, tile = lu / cur.KB, kb = lu - tile * cur.KB;
                 mbar_arrive_expect_tx(&full[i], stage_bytes);
                 for (int b = 0; b < kBoxes; ++b)
-                    tma_load_2d_hint(smem + (size_t)i * stage_bytes + b * kWTileBytes, &tmW, &full[i],
-                                     (kb * kBoxes + b) * 64, tile * 128, pol_w);
+                    tma_load_2d_hint(smem + (size_t)i * stage_bytes + b * kWTileBytes, &maps.W[cur.m],
+                                     &full[i], (kb * kBoxes + b) * 64, tile * 128, pol_w);
             }
             pdl_wait_prior();
+            cur.load(p, unit_problem(p, u0));
             for (int i = 0; i < pre; ++i) {
-                const int kb = (u0 + i) % p.KB;
+                const int u = u0 + i;
+                cur.seek(p, u);
+                const int kb = (u - cur.ub) % cur.KB;
                 for (int b = 0; b < kBoxes; ++b)
-                    tma_load_2d(smem + (size_t)i * stage_bytes + w_bytes + b * x_box, &tmX, &full[i],
-                                (kb * kBoxes + b) * 64, 0);
+                    tma_load_2d(smem + (size_t)i * stage_bytes + w_bytes + b * x_box, &maps.X[cur.m],
+                                &full[i], (kb * kBoxes + b) * 64, 0);
             }
             int it = pre;
             for (int u = u0 + pre; u < u1; ++u, ++it) {
                 const int s = it % stages;
                 if (!mbar_wait(&empty[s], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err)) break;
-                const int tile = u / p.KB, kb = u - tile * p.KB;
+                cur.seek(p, u);
+                const int lu = u - cur.ub, tile = lu / cur.KB, kb = lu - tile * cur.KB;
                 uint8_t *ws = smem + (size_t)s * stage_bytes;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 for (int b = 0; b < kBoxes; ++b) {
-                    tma_load_2d_hint(ws + b * kWTileBytes, &tmW, &full[s], (kb * kBoxes + b) * 64,
-                                     tile * 128, pol_w);
-                    tma_load_2d(ws + w_bytes + b * x_box, &tmX, &full[s], (kb * kBoxes + b) * 64, 0);
+                    tma_load_2d_hint(ws + b * kWTileBytes, &maps.W[cur.m], &full[s],
+                                     (kb * kBoxes + b) * 64, tile * 128, pol_w);
+                    tma_load_2d(ws + w_bytes + b * x_box, &maps.X[cur.m], &full[s],
+                                (kb * kBoxes + b) * 64, 0);
                 }
             }
+            // do not leave while copies into this CTA's shared memory are in flight
             for (int i = 0; i < stages && i < it; ++i) {
                 const int j = it - 1 - i;
                 int dummy = 0;
@@ -187,25 +250,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             const uint32_t idesc = idesc_bf16_f32(128, p.ntok);
             int it = 0;
+            UnitCursor cur;
+            cur.load(p, unit_problem(p, u0));
+            uint32_t d = tmem;
             for (int u = u0; u < u1; ++u, ++it) {
+                cur.seek(p, u);
+                const int KB = cur.KB, lu = u - cur.ub;
+                const int tile = lu / KB, kb = lu - tile * KB;
+                const int seg = cur.gb + tile - g0;
+                const bool seg_first = (kb == 0) || (u == u0);
+                if (seg_first) {
+                    // the ring slot's previous tile must have been read out
+                    const int a = seg % n_acc;
+                    if (!mbar_wait(&acc_empty[a], ((uint32_t)(seg / n_acc) & 1u) ^ 1u, &abort_flag, err))
+                        break;
+                    tc_fence_after_sync();
+                    d = tmem + (uint32_t)(a * p.ntok);
+                }
                 const int s = it % stages;
                 if (!mbar_wait(&full[s], (uint32_t)(it / stages) & 1u, &abort_flag, err)) break;
                 tc_fence_after_sync();
-                const int tile = u / p.KB, kb = u - tile * p.KB;
-                const int seg = tile - tile0;
-                const uint32_t d = tmem + (uint32_t)(seg * p.ntok);
                 const uint32_t wa = smem_u32(smem + (size_t)s * stage_bytes);
                 const uint32_t xa = wa + w_bytes;
-                const bool first = (kb == 0) || (u == u0);
 #pragma unroll
                 for (int b = 0; b < kBoxes; ++b)
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16_ss(d, sdesc_k_sw128(wa + b * kWTileBytes + kk * 32),
                                     sdesc_k_sw128(xa + b * x_box + kk * 32), idesc,
-                                    (first && b == 0 && kk == 0) ? 0u : 1u);
+                                    (seg_first && b == 0 && kk == 0) ? 0u : 1u);
                 mma_commit(&empty[s]);
-                if (u == u1 - 1 || kb == p.KB - 1) mma_commit(&acc_full[seg]);
+                if (u == u1 - 1 || kb == KB - 1) mma_commit(&acc_full[seg % n_acc]);
             }
             mma_commit(drain);
             int dummy = 0;
@@ -218,32 +293,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         const uint32_t tmem = *tmem_slot;
         pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
-        if (sa.ids != nullptr) {
-            const int pairs = p.T * pool.max_pages;
-            for (int u = c; u < pairs; u += p.G) {
-                const int t = u / pool.max_pages, q = u - t * pool.max_pages;
-                const int id = sa.ids[t];
-                if (!slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) continue;
-                const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+        if (ids != nullptr) {
+            int m = 0;
+            for (int u = c; u < p.pairs; u += p.G) {
+                while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
+                const DecodeProblem &pr = p.prob[pick<NP>(m)];
+                const int lp = u - pr.pair_begin;
+                const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
+                const int id = ids[t];
+                if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
+                const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
                 if (q >= row[SLOT_NPAGES]) continue;
-                shrink_pair(t, row[SLOT_PAGES + q], __int_as_float(row[SLOT_SCALE]), pool, sa, q,
-                            red);
+                shrink_pair(t, row[SLOT_PAGES + q], __int_as_float(row[SLOT_SCALE]), pr, q, red);
             }
         }
         for (int seg = 0; seg < nseg; ++seg) {
+            const int a = seg % n_acc;
             bool ok = true;
-            if (lane == 0) ok = mbar_wait(&acc_full[seg], 0, &abort_flag, err);
+            if (lane == 0) ok = mbar_wait(&acc_full[a], (uint32_t)(seg / n_acc) & 1u, &abort_flag, err);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             tc_fence_after_sync();
-            float *out = partials + (size_t)(c * 2 + seg) * p.T * 128 + warp * 32 + lane;
+            float *out = partials + ((size_t)c * p.max_seg + seg) * p.T * 128 + warp * 32 + lane;
             for (int col = 0; col < p.ntok; col += 16) {
                 uint32_t v[16];
-                tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(seg * p.ntok + col), v);
+                tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * p.ntok + col), v);
 #pragma unroll
                 for (int j = 0; j < 16; ++j)
                     if (col + j < p.T) out[(size_t)(col + j) * 128] = __uint_as_float(v[j]);
             }
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[a]);
         }
     }
 
@@ -257,16 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
 constexpr int kFinishCols = 8;
-constexpr int kPrefetchPages = 2;     // B pages fetched before the GEMM has finished
-constexpr int kFinishBatch = 8;       // partial loads in flight per thread
-
-__device__ __forceinline__ void add8(float (&acc)[kFinishCols], const float *src)
-{
-    const float4 a = *reinterpret_cast<const float4 *>(src);
-    const float4 b = *reinterpret_cast<const float4 *>(src + 4);
-    acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-    acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
-}
+constexpr int kFinishBlockCols = kFinishThreads * kFinishCols;
+constexpr int kPrefetchPages = 2;     // B pages loaded into registers before the GEMM ends
+// partial loads in flight per thread (fewer beside the LoRA variant's B words)
+template <bool LORA>
+constexpr int finish_batch() { return LORA ? 4 : 8; }
 
 // acc[c] += sum_jj v[jj] * page[n0 + c][jj], the 8 columns' 16-byte words in b[0..7]
 __device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *v, const uint4 (&b)[8])
@@ -275,34 +351,45 @@ __device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *
     for (int c = 0; c < kFinishCols; ++c) acc[c] = dot8_f32_bf16(v, b[c], acc[c]);
 }
 
-__global__ void __launch_bounds__(kFinishThreads)
-    finish_decode_kernel(DecodePlan p, const float *__restrict__ partials,
-                         const int32_t *__restrict__ ids, PoolDev pool, const float *__restrict__ V,
-                         int ldv, uint16_t *__restrict__ Y, int *err)
+// LORA = false: the base-only variant (no adapter state, few registers).
+// At most 168 registers a thread (the bound for 3 CTAs): two finishing CTAs then
+// fit on an SM beside the GEMM CTA (192 threads x 112 registers) and have their
+// B words in registers when the GEMM ends.
+template <int NP, bool LORA>
+__global__ void __launch_bounds__(kFinishThreads, 3)
+    finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
+                         const int32_t *__restrict__ ids)
 {
     // The next call's GEMM may launch now: its CTAs take an SM as soon as this call's
     // GEMM CTA leaves it and stream their first W tiles; everything they write comes
     // after their own wait for this kernel.
     pdl_launch_dependents();
-    const int n0 = (blockIdx.x * kFinishThreads + threadIdx.x) * kFinishCols;
+    int m = 0;
+    for (int k = 1; NP > 1 && k < p.n; ++k)
+        if (p.prob[pick<NP>(k)].col_blk_begin <= (int)blockIdx.x) m = k;
+    const DecodeProblem &pr = p.prob[pick<NP>(m)];
+    const PoolDev &pool = pr.pool;
+    const int n0 = ((blockIdx.x - pr.col_blk_begin) * kFinishThreads + threadIdx.x) * kFinishCols;
     const int t = blockIdx.y;
     const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
 
-    // ---- independent of the GEMM kernel: this token's adapter and its first B words
+    // ---- independent of the GEMM kernel: this token's adapter and its B words (the
+    // 8 columns' 16-byte words of a page are one 128-byte line): the first pages into
+    // registers, the rest into L2
     int np = 0;
     const int32_t *pages = nullptr;
-    if (ids != nullptr) {
+    if (LORA && pool.slots != nullptr) {
         const int id = ids[t];
         if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
             const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
             np = row[SLOT_NPAGES];
             pages = row + SLOT_PAGES;
-        } else if (id != -1 && threadIdx.x == 0 && blockIdx.x == 0) {
-            atomicOr(err, kErrBadIdBit);  // strict: never a silent base fall-back
+        } else if (id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin) {
+            atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
         }
     }
     uint4 b[kPrefetchPages][8];
-    if (col_ok) {
+    if (LORA && col_ok) {
 #pragma unroll
         for (int q = 0; q < kPrefetchPages; ++q)
             if (q < np) {
@@ -310,45 +397,55 @@ __global__ void __launch_bounds__(kFinishThreads)
 #pragma unroll
                 for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
             }
+        for (int q = kPrefetchPages; q < np; ++q)
+            prefetch_l2(pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage);
     }
-    // contributors of this tile: CTAs c_lo..c_hi (contiguous k-ranges); only c_lo can
-    // have started in the previous tile, in which case its partial for this tile is
-    // its second one. (U < 2^20 and G < 2^11, so the products fit in 32 bits.)
+    // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
+    // can have started before the tile; its partial for the tile is its segment
+    // (tile - its first tile), the others' is their segment 0. (U * G < 2^31 is
+    // checked on the host, so the products fit in 32 bits.)
     const int tile = n0 >> 7, nl = n0 & 127;
-    const int kb_lo = tile * p.KB, kb_hi = kb_lo + p.KB;
-    int c_lo = (kb_lo * p.G) / p.U;
-    while (c_lo > 0 && (c_lo * p.U) / p.G > kb_lo) --c_lo;
-    while (((c_lo + 1) * p.U) / p.G <= kb_lo) ++c_lo;
+    const int ub = pr.u_begin + tile * pr.KB, ue = ub + pr.KB;
+    int c_lo = (ub * p.G) / p.U;
+    while (c_lo > 0 && (c_lo * p.U) / p.G > ub) --c_lo;
+    while (((c_lo + 1) * p.U) / p.G <= ub) ++c_lo;
     int c_hi = c_lo;
-    while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < kb_hi) ++c_hi;
-    const int seg_lo = (c_lo * p.U) / p.G < kb_lo ? 1 : 0;
+    while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < ue) ++c_hi;
+    const int seg_lo = pr.g_begin + tile - unit_tile(p, (c_lo * p.U) / p.G);
 
     // ---- partials and V are written by the GEMM kernel
     pdl_wait_prior();
     if (!col_ok) return;
 
-    float acc[kFinishCols] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    add8(acc, partials + ((size_t)(c_lo * 2 + seg_lo) * p.T + t) * 128 + nl);
+    float acc[kFinishCols];
+    {
+        const float *src = partials + (((size_t)c_lo * p.max_seg + seg_lo) * p.T + t) * 128 + nl;
+        const float4 a0 = *reinterpret_cast<const float4 *>(src);
+        const float4 a1 = *reinterpret_cast<const float4 *>(src + 4);
+        acc[0] = a0.x; acc[1] = a0.y; acc[2] = a0.z; acc[3] = a0.w;
+        acc[4] = a1.x; acc[5] = a1.y; acc[6] = a1.z; acc[7] = a1.w;
+    }
     // the other contributors' first partials, kFinishBatch loads in flight at a time
     // (summed in CTA order all the same)
-    const size_t stride = (size_t)2 * p.T * 128;
-    const float *src = partials + ((size_t)(c_lo + 1) * 2 * p.T + t) * 128 + nl;
+    const size_t stride = (size_t)p.max_seg * p.T * 128;
+    const float *src = partials + ((size_t)(c_lo + 1) * p.max_seg * p.T + t) * 128 + nl;
+    constexpr int kFinishBatch = finish_batch<LORA>();
     for (int c0 = c_lo + 1; c0 <= c_hi; c0 += kFinishBatch, src += kFinishBatch * stride) {
-        float4 b[kFinishBatch][2];
+        float4 v[kFinishBatch][2];
 #pragma unroll
         for (int i = 0; i < kFinishBatch; ++i)
             if (c0 + i <= c_hi) {
-                b[i][0] = *reinterpret_cast<const float4 *>(src + i * stride);
-                b[i][1] = *reinterpret_cast<const float4 *>(src + i * stride + 4);
+                v[i][0] = *reinterpret_cast<const float4 *>(src + i * stride);
+                v[i][1] = *reinterpret_cast<const float4 *>(src + i * stride + 4);
             }
 #pragma unroll
         for (int i = 0; i < kFinishBatch; ++i)
             if (c0 + i <= c_hi) {
-                acc[0] += b[i][0].x; acc[1] += b[i][0].y; acc[2] += b[i][0].z; acc[3] += b[i][0].w;
-                acc[4] += b[i][1].x; acc[5] += b[i][1].y; acc[6] += b[i][1].z; acc[7] += b[i][1].w;
+                acc[0] += v[i][0].x; acc[1] += v[i][0].y; acc[2] += v[i][0].z; acc[3] += v[i][0].w;
+                acc[4] += v[i][1].x; acc[5] += v[i][1].y; acc[6] += v[i][1].z; acc[7] += v[i][1].w;
             }
     }
-    const float *vrow = V + (size_t)t * ldv;
+    const float *vrow = pr.V + (size_t)t * pr.ldv;
     for (int q = 0; q < np; ++q) {
         float v[8];
         const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
@@ -360,9 +457,9 @@ __global__ void __launch_bounds__(kFinishThreads)
             else expand8(acc, v, b[1]);
         } else {
             uint4 bq[8];
-            const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+            const uint16_t *bsrc = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) bq[c] = ldg_nc_v4(src + c * kRankPage);
+            for (int c = 0; c < 8; ++c) bq[c] = ldg_nc_v4(bsrc + c * kRankPage);
             expand8(acc, v, bq);
         }
     }
@@ -371,7 +468,7 @@ __global__ void __launch_bounds__(kFinishThreads)
     o.y = pack_bf16x2(acc[2], acc[3]);
     o.z = pack_bf16x2(acc[4], acc[5]);
     o.w = pack_bf16x2(acc[6], acc[7]);
-    *reinterpret_cast<uint4 *>(Y + (size_t)t * pool.d_out + n0) = o;
+    *reinterpret_cast<uint4 *>(pr.Y + (size_t)t * pool.d_out + n0) = o;
 }
 
 uint32_t pow2_cols(uint32_t n)
@@ -381,74 +478,147 @@ uint32_t pow2_cols(uint32_t n)
     return c;
 }
 
+// programmatic stream serialization: the kernel's prologue (and, for the GEMM,
+// its first W tiles) overlaps the previous kernel in the stream; each kernel
+// waits (griddepcontrol.wait) before it touches anything the stream wrote
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace
 
-DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms)
+bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max_pages, int max_G,
+                 DecodePlan *out)
 {
+    if (n < 1 || n > kMaxGroup || T < 1 || T > kDecodeMaxT || max_G < 1) return false;
     DecodePlan p{};
+    p.n = n;
     p.T = T;
     p.ntok = ((T + 15) / 16) * 16;
-    if (p.ntok < 16) p.ntok = 16;
-    p.KB = (d_in + 64 * kBoxes - 1) / (64 * kBoxes);
-    p.n_tiles = (d_out + 127) / 128;
-    p.U = p.n_tiles * p.KB;
-    int G = num_sms;
-    if (G > p.U) G = p.U;
-    if (G < p.n_tiles) G = p.n_tiles;  // ranges never span more than two tiles
-    p.G = G;
+    long long U = 0, pairs = 0, cols = 0;
+    int g = 0;
+    for (int m = 0; m < n; ++m) {
+        DecodeProblem &q = p.prob[m];
+        q.KB = (d_in[m] + 64 * kBoxes - 1) / (64 * kBoxes);
+        q.n_tiles = (d_out[m] + 127) / 128;
+        q.u_begin = (int)U;
+        q.g_begin = g;
+        q.pair_begin = (int)pairs;
+        q.col_blk_begin = (int)cols;
+        U += (long long)q.n_tiles * q.KB;
+        g += q.n_tiles;
+        pairs += (long long)T * max_pages[m];
+        cols += (d_out[m] + kFinishBlockCols - 1) / kFinishBlockCols;
+    }
+    long long G = max_G < U ? max_G : U;
+    // the finishing pass computes c * U in 32 bits
+    if (U * G >= (1ll << 31) || pairs >= (1ll << 31) || cols >= (1ll << 31)) return false;
+    p.U = (int)U;
+    p.G = (int)G;
+    p.pairs = (int)pairs;
+    p.col_blocks = (int)cols;
+    int max_seg = 1;
+    for (int c = 0; c < p.G; ++c) {
+        const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
+        const int s = unit_tile(p, u1 - 1) - unit_tile(p, u0) + 1;
+        if (s > max_seg) max_seg = s;
+    }
+    p.max_seg = max_seg;
+    // accumulators: one per segment of a range, within the 512 TMEM columns
+    int n_acc = 512 / p.ntok;
+    if (n_acc > max_seg) n_acc = max_seg;
+    p.n_acc = n_acc;
     const size_t stage_bytes = kBoxes * (kWTileBytes + (size_t)p.ntok * 128);
     int stages = (int)((200 * 1024) / stage_bytes);
     if (stages > 8) stages = 8;
     if (stages < 2) stages = 2;
     p.stages = stages;
-    p.smem_bytes = 1024 + stages * stage_bytes + (2 * stages + 3) * 8 + 16;
-    p.tmem_cols = pow2_cols(2 * p.ntok);
-    return p;
+    p.smem_bytes = 1024 + stages * stage_bytes + (2 * stages + 2 * n_acc + 1) * 8 + 16;
+    p.tmem_cols = pow2_cols((uint32_t)(n_acc * p.ntok));
+    *out = p;
+    return true;
 }
 
-size_t decode_partials_floats(const DecodePlan &p) { return (size_t)p.G * 2 * p.T * 128; }
+size_t decode_partials_floats(const DecodePlan &p) { return (size_t)p.G * p.max_seg * p.T * 128; }
 
-cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
-                               const DecodePlan &plan, const PoolDev &pool, const uint16_t *X,
-                               const int32_t *ids, float *V, int ldv, float *partials, int *err,
-                               cudaStream_t stream)
+namespace {
+
+template <int NP>
+DecodePlanT<NP> narrow_plan(const DecodePlan &p)
 {
-    cudaError_t e = ensure_smem_attr((const void *)gemm_decode_kernel, plan.smem_bytes);
-    if (e != cudaSuccess) return e;
-    ShrinkArgs sa{X, ids, V, ldv};
-    // programmatic stream serialization: the prologue and the first W tiles overlap the
-    // previous kernel in the stream (the kernel waits before touching anything else)
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(plan.G);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = plan.smem_bytes;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_decode_kernel, tmW, tmX, plan, partials, err, pool, sa);
+    DecodePlanT<NP> q;
+    q.n = p.n;
+    q.T = p.T;
+    q.ntok = p.ntok;
+    q.U = p.U;
+    q.G = p.G;
+    q.max_seg = p.max_seg;
+    q.n_acc = p.n_acc;
+    q.stages = p.stages;
+    q.pairs = p.pairs;
+    q.col_blocks = p.col_blocks;
+    q.tmem_cols = p.tmem_cols;
+    q.smem_bytes = p.smem_bytes;
+    for (int m = 0; m < NP; ++m) q.prob[m] = p.prob[m];
+    return q;
 }
 
-cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
-                                 const int32_t *ids, const PoolDev &pool, const float *V,
-                                 int ldv, uint16_t *Y, int *err, cudaStream_t stream)
+template <int NP>
+cudaError_t launch_gemm_decode_n(const DecodeMaps &maps, const DecodePlan &plan, const int32_t *ids,
+                                 float *partials, int *err, cudaStream_t stream)
 {
-    cudaError_t e = ensure_smem_attr((const void *)finish_decode_kernel, 0);
+    cudaError_t e = ensure_smem_attr((const void *)gemm_decode_kernel<NP>, plan.smem_bytes);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    const int per_cta = kFinishThreads * kFinishCols;
-    cfg.gridDim = dim3((pool.d_out + per_cta - 1) / per_cta, plan.T);
-    cfg.blockDim = dim3(kFinishThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, finish_decode_kernel, plan, partials, ids, pool, V, ldv, Y, err);
+    DecodeMapsT<NP> m;
+    for (int i = 0; i < NP; ++i) {
+        m.W[i] = maps.W[i];
+        m.X[i] = maps.X[i];
+    }
+    return launch_pdl(gemm_decode_kernel<NP>, dim3(plan.G), dim3(kThreads), plan.smem_bytes, stream, m,
+                      narrow_plan<NP>(plan), ids, partials, err);
+}
+
+template <int NP, bool LORA>
+cudaError_t launch_finish_decode_n(const DecodePlan &plan, const float *partials, const int32_t *ids,
+                                   cudaStream_t stream)
+{
+    cudaError_t e = ensure_smem_attr((const void *)finish_decode_kernel<NP, LORA>, 0);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(finish_decode_kernel<NP, LORA>, dim3(plan.col_blocks, plan.T),
+                      dim3(kFinishThreads), 0, stream, narrow_plan<NP>(plan), partials, ids);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_decode(const DecodeMaps &maps, const DecodePlan &plan, const int32_t *ids,
+                               float *partials, int *err, cudaStream_t stream)
+{
+    if (plan.n == 1) return launch_gemm_decode_n<1>(maps, plan, ids, partials, err, stream);
+    return launch_gemm_decode_n<kMaxGroup>(maps, plan, ids, partials, err, stream);
+}
+
+cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, const int32_t *ids,
+                                 cudaStream_t stream)
+{
+    if (ids == nullptr) {
+        if (plan.n == 1) return launch_finish_decode_n<1, false>(plan, partials, ids, stream);
+        return launch_finish_decode_n<kMaxGroup, false>(plan, partials, ids, stream);
+    }
+    if (plan.n == 1) return launch_finish_decode_n<1, true>(plan, partials, ids, stream);
+    return launch_finish_decode_n<kMaxGroup, true>(plan, partials, ids, stream);
 }
 
 }  // namespace lora

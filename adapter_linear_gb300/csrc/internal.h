@@ -74,23 +74,66 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, con
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
                              int num_sms, int *err, cudaStream_t stream);
 
-struct DecodePlan {
-    int T, ntok, KB, n_tiles, U, G, stages;
-    size_t smem_bytes;
-    uint32_t tmem_cols;
+// ---------------------------------------------------------------- decode path
+// One decode call covers 1..kMaxGroup problems that share the token ids (one
+// lora_linear call, or the layers of one grouped call); their (tile, k-block)
+// units are concatenated in problem order for the stream-K split.
+constexpr int kMaxGroup = 8;
+
+struct DecodeProblem {
+    PoolDev pool;           // pool.slots == nullptr: no adapters (base product only)
+    const uint16_t *X;      // [T][d_in]
+    float *V;               // shrink output [T][ldv]
+    int ldv;
+    uint16_t *Y;            // [T][d_out]
+    int *err;               // the pool's error word (bad ids)
+    int KB;                 // 128-column k-blocks
+    int n_tiles;            // 128-row tiles of d_out
+    int u_begin;            // first unit of this problem
+    int g_begin;            // first tile in the concatenated tile order
+    int pair_begin;         // first shrink (token, page) pair
+    int col_blk_begin;      // first block of the finishing grid
 };
-DecodePlan plan_decode(int T, int d_in, int d_out, int num_sms);
+
+// The plan of one decode call. Kernels take a copy sized for the problems it
+// holds (NP = 1 for a single layer, kMaxGroup otherwise) to keep their
+// parameter block small.
+template <int NP>
+struct DecodePlanT {
+    static constexpr int kNP = NP;
+    int n, T, ntok;
+    int U, G;               // units, CTAs (stream-K ranges)
+    int max_seg;            // most tiles one range touches (partials per CTA)
+    int n_acc;              // TMEM accumulators in the ring
+    int stages;
+    int pairs;              // shrink pairs of all problems
+    int col_blocks;         // finishing grid.x
+    uint32_t tmem_cols;
+    size_t smem_bytes;
+    DecodeProblem prob[NP];
+};
+using DecodePlan = DecodePlanT<kMaxGroup>;
+
+template <int NP>
+struct DecodeMapsT {
+    CUtensorMap W[NP];  // W_m [d_out][d_in], box 64 x 128
+    CUtensorMap X[NP];  // X_m [T][d_in], box 64 x ntok
+};
+using DecodeMaps = DecodeMapsT<kMaxGroup>;
+
+// Shapes and the stream-K split (pointers left for the caller to fill);
+// max_G bounds the number of ranges. False when the shapes are out of range.
+bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max_pages, int max_G,
+                 DecodePlan *out);
 size_t decode_partials_floats(const DecodePlan &p);
-// Base product (stream-K partials) + the per-token shrink V (ids == nullptr: no shrink).
-cudaError_t launch_gemm_decode(const CUtensorMap &tmW, const CUtensorMap &tmX,
-                               const DecodePlan &plan, const PoolDev &pool, const uint16_t *X,
-                               const int32_t *ids, float *V, int ldv, float *partials, int *err,
-                               cudaStream_t stream);
-// Y = bf16(sum of split-K partials + s_i V[t] B_i); ids == nullptr: no branch.
+// Base products (stream-K partials) + the per-token shrink of every problem with a
+// pool (ids == nullptr: no shrink). err takes the timeout bit.
+cudaError_t launch_gemm_decode(const DecodeMaps &maps, const DecodePlan &plan, const int32_t *ids,
+                               float *partials, int *err, cudaStream_t stream);
+// Y_m = bf16(sum of split-K partials + s_i V_m[t] B_i); ids == nullptr: no branch.
 // Launched with programmatic stream serialization after launch_gemm_decode.
-cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials,
-                                 const int32_t *ids, const PoolDev &pool, const float *V,
-                                 int ldv, uint16_t *Y, int *err, cudaStream_t stream);
+cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, const int32_t *ids,
+                                 cudaStream_t stream);
 
 // Prefill GEMM with the expand: tmV is a TMA map of Vhl [T x ldh] (box 128 x 64);
 // tile_info from the segment builder; ids == nullptr: base product only.

@@ -21,7 +21,7 @@
 namespace lora {
 namespace {
 
-// Split-K partial sums (G * 2 * T * 128 floats per call): 16 MiB, after a
+// Split-K partial sums (G * max_seg * T * 128 floats per call): 16 MiB, after a
 // 256-byte reserved head whose first word takes the kernels' timeout bit.
 constexpr size_t kNoallocReserved = 64;
 constexpr size_t kNoallocScratchFloats = ((size_t)4 << 20) + kNoallocReserved;
@@ -80,32 +80,37 @@ extern "C" lora_status lora_base_linear_noalloc(const void *X, const void *W_bas
     lora_status st = setup_current_device(&dev);
     if (st != LORA_OK) return st;
 
-    DecodePlan plan = plan_decode(T, d_in, d_out, dev->num_sms);
+    // fewer stream-K ranges when the partial sums would not fit the fixed scratch
     const size_t avail = kNoallocScratchFloats - kNoallocReserved;
-    if (decode_partials_floats(plan) > avail) {
-        // fewer stream-K ranges (never fewer than the tiles) to fit the fixed scratch
-        const size_t fit = avail / ((size_t)2 * 128 * T);
-        plan.G = (int)(fit > (size_t)plan.n_tiles ? fit : (size_t)plan.n_tiles);
-        if (decode_partials_floats(plan) > avail) return LORA_ERR_SHAPE;
+    const int no_pages = 0;
+    DecodePlan plan;
+    int max_G = dev->num_sms;
+    for (;;) {
+        if (!plan_decode(1, T, &d_in, &d_out, &no_pages, max_G, &plan)) return LORA_ERR_SHAPE;
+        const size_t need = decode_partials_floats(plan);
+        if (need <= avail) break;
+        const size_t per_cta = (size_t)plan.max_seg * T * 128;
+        const int fit = (int)(avail / per_cta);
+        if (plan.G <= 1) return LORA_ERR_SHAPE;
+        max_G = fit < plan.G ? (fit > 1 ? fit : 1) : plan.G - 1;
     }
 
-    CUtensorMap tmW, tmX;
-    if (!make_tmap_bf16_2d(&tmW, W_base, d_in, d_out, (uint64_t)d_in * 2, 64, 128) ||
-        !make_tmap_bf16_2d(&tmX, X, d_in, T, (uint64_t)d_in * 2, 64, plan.ntok))
+    DecodeMaps maps;
+    if (!make_tmap_bf16_2d(&maps.W[0], W_base, d_in, d_out, (uint64_t)d_in * 2, 64, 128) ||
+        !make_tmap_bf16_2d(&maps.X[0], X, d_in, T, (uint64_t)d_in * 2, 64, plan.ntok))
         return LORA_ERR_ARG;
-    PoolDev none{};
-    none.d_in = d_in;
-    none.d_out = d_out;
     // the partials need no clearing: every slot the finishing pass reads is
     // written by this call's GEMM kernel first
     int *err = reinterpret_cast<int *>(dev->scratch);
     float *partials = dev->scratch + kNoallocReserved;
+    DecodeProblem &q = plan.prob[0];
+    q.pool.d_in = d_in;
+    q.pool.d_out = d_out;
+    q.X = static_cast<const uint16_t *>(X);
+    q.Y = static_cast<uint16_t *>(Y);
+    q.err = err;
     cudaStream_t s = (cudaStream_t)stream;
-    if (launch_gemm_decode(tmW, tmX, plan, none, static_cast<const uint16_t *>(X), nullptr, nullptr,
-                           0, partials, err, s) != cudaSuccess)
-        return LORA_ERR_CUDA;
-    if (launch_finish_decode(plan, partials, nullptr, none, nullptr, 0, static_cast<uint16_t *>(Y),
-                             err, s) != cudaSuccess)
-        return LORA_ERR_CUDA;
+    if (launch_gemm_decode(maps, plan, nullptr, partials, err, s) != cudaSuccess) return LORA_ERR_CUDA;
+    if (launch_finish_decode(plan, partials, nullptr, s) != cudaSuccess) return LORA_ERR_CUDA;
     return LORA_OK;
 }

@@ -142,8 +142,11 @@ lora_status ensure_scratch(lora_pool *p, int T)
     CUDA_TRY(cudaDeviceSynchronize());  // earlier calls may still read the old scratch
     free_scratch(p);
     const size_t se = seg_entries(p, T);
-    const DecodePlan plan = plan_decode(std::min(T, kDecodeMaxT), p->d_in, p->d_out, p->num_sms);
-    const size_t pf = decode_partials_floats(plan);
+    DecodePlan plan;
+    if (!plan_decode(1, std::max(1, std::min(T, kDecodeMaxT)), &p->d_in, &p->d_out, &p->max_pages,
+                     p->num_sms, &plan))
+        return LORA_ERR_SHAPE;
+    const size_t pf = std::max(decode_partials_floats(plan), p->partials_floats);
     lora_status st;
     if ((st = alloc_dev(p, (void **)&p->order, sizeof(int32_t) * T)) ||
         (st = alloc_dev(p, (void **)&p->hdr, sizeof(int32_t) * 4)) ||
@@ -227,6 +230,86 @@ __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16
 
 bool dims_ok(int d) { return d > 0 && d <= LORA_MAX_DIM && d % 8 == 0; }
 
+// Split-K partials of a grouped decode call (held by its first pool): grown on
+// first use of a larger group, like the rest of the scratch.
+lora_status ensure_partials(lora_pool *p, size_t floats)
+{
+    if (floats <= p->partials_floats) return LORA_OK;
+    CUDA_TRY(cudaDeviceSynchronize());  // earlier calls may still read the old buffer
+    free_dev(p, p->partials, sizeof(float) * p->partials_floats);
+    p->partials = nullptr;
+    p->partials_floats = 0;
+    lora_status st = alloc_dev(p, (void **)&p->partials, sizeof(float) * floats);
+    if (st == LORA_OK) p->partials_floats = floats;
+    return st;
+}
+
+// Measurement hook of one call: event k+1 closes kernel slot k (inside a graph
+// capture the records become event nodes replayed with the graph).
+struct CallMarks {
+    lora_pool *p;
+    cudaStream_t stream;
+    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
+    bool begin()
+    {
+        if (!p->timing) return true;
+        for (bool &u : p->ev_used) u = false;
+        if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return false;
+        return mark(-1);
+    }
+    bool mark(int slot)
+    {
+        if (!p->timing) return true;
+        if (slot >= 0) p->ev_used[slot] = true;
+        p->ev_last = slot + 1;
+        const unsigned flags =
+            capture == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+        return cudaEventRecordWithFlags(p->ev[slot + 1], stream, flags) == cudaSuccess;
+    }
+};
+
+// The decode path for n problems that share the ids (scratch already sized for T
+// on every pool). Per-token (BGMV-style) shrink fused into the GEMM kernel: no
+// segment tables.
+lora_status run_decode(lora_pool *const *pools, int n, const void *const *X, const void *const *W,
+                       const int32_t *ids, int T, void *const *Y, cudaStream_t stream, bool with_lora,
+                       CallMarks &marks)
+{
+    lora_pool *p0 = pools[0];
+    int d_in[kMaxGroup], d_out[kMaxGroup], pages[kMaxGroup];
+    for (int m = 0; m < n; ++m) {
+        d_in[m] = pools[m]->d_in;
+        d_out[m] = pools[m]->d_out;
+        pages[m] = with_lora ? pools[m]->max_pages : 0;
+    }
+    DecodePlan plan;
+    if (!plan_decode(n, T, d_in, d_out, pages, p0->num_sms, &plan)) return LORA_ERR_SHAPE;
+    lora_status st = ensure_partials(p0, decode_partials_floats(plan));
+    if (st != LORA_OK) return st;
+    DecodeMaps maps;
+    for (int m = 0; m < n; ++m) {
+        lora_pool *p = pools[m];
+        const CUtensorMap *tmW = tmap_for(p, W[m], p->d_in, p->d_out, 64, 128);
+        const CUtensorMap *tmX = tmap_for(p, X[m], p->d_in, T, 64, plan.ntok);
+        if (!tmW || !tmX) return LORA_ERR_ARG;
+        maps.W[m] = *tmW;
+        maps.X[m] = *tmX;
+        DecodeProblem &q = plan.prob[m];
+        q.pool = pool_view(p);
+        q.X = static_cast<const uint16_t *>(X[m]);
+        q.V = p->V;
+        q.ldv = p->ldv;
+        q.Y = static_cast<uint16_t *>(Y[m]);
+        q.err = p->d_err;
+    }
+    const int32_t *tids = with_lora ? ids : nullptr;
+    CUDA_TRY(launch_gemm_decode(maps, plan, tids, p0->partials, p0->d_err, stream));
+    if (!marks.mark(2)) return LORA_ERR_CUDA;
+    CUDA_TRY(launch_finish_decode(plan, p0->partials, tids, stream));
+    if (!marks.mark(3)) return LORA_ERR_CUDA;
+    return LORA_OK;
+}
+
 lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t *ids, int T,
                        void *Y, cudaStream_t stream, bool with_lora)
 {
@@ -240,35 +323,16 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
 
     const PoolDev pd = pool_view(p);
     const SegTables tabs = seg_tables(p);
-    // measurement hook: event k+1 closes kernel slot k
-    for (bool &u : p->ev_used) u = false;
-    cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
-    if (p->timing && cudaStreamIsCapturing(stream, &capture) != cudaSuccess) return LORA_ERR_CUDA;
-    auto mark = [&](int slot) -> bool {
-        if (!p->timing) return true;
-        if (slot >= 0) p->ev_used[slot] = true;
-        p->ev_last = slot + 1;
-        // inside a graph capture the records become event nodes replayed with the graph
-        const unsigned flags =
-            capture == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
-        return cudaEventRecordWithFlags(p->ev[slot + 1], stream, flags) == cudaSuccess;
-    };
-    if (!mark(-1)) return LORA_ERR_CUDA;
+    CallMarks marks{p, stream};
+    if (!marks.begin()) return LORA_ERR_CUDA;
+    auto mark = [&](int slot) { return marks.mark(slot); };
     const uint16_t *Xb = static_cast<const uint16_t *>(X);
     uint16_t *Yb = static_cast<uint16_t *>(Y);
 
     if (path == LORA_PATH_DECODE) {
-        // per-token (BGMV-style) shrink fused into the GEMM kernel: no segment tables
-        const DecodePlan plan = plan_decode(T, p->d_in, p->d_out, p->num_sms);
-        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 128);
-        const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, plan.ntok);
-        if (!tmW || !tmX) return LORA_ERR_ARG;
-        CUDA_TRY(launch_gemm_decode(*tmW, *tmX, plan, pd, Xb, with_lora ? ids : nullptr, p->V,
-                                    p->ldv, p->partials, p->d_err, stream));
-        if (!mark(2)) return LORA_ERR_CUDA;
-        CUDA_TRY(launch_finish_decode(plan, p->partials, with_lora ? ids : nullptr, pd, p->V,
-                                      p->ldv, Yb, p->d_err, stream));
-        if (!mark(3)) return LORA_ERR_CUDA;
+        lora_pool *pools[1] = {p};
+        st = run_decode(pools, 1, &X, &W, ids, T, &Y, stream, with_lora, marks);
+        if (st != LORA_OK) return st;
     } else {
         if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
         if (!mark(0)) return LORA_ERR_CUDA;
@@ -482,6 +546,43 @@ lora_status lora_base_linear(lora_pool_t p, const void *X, const void *W_base, i
                              lora_stream_t stream)
 {
     return run_linear(p, X, W_base, nullptr, T, Y, (cudaStream_t)stream, false);
+}
+
+lora_status lora_linear_grouped(int n, const lora_pool_t *pools, const void *const *X,
+                                const void *const *W_base, const int32_t *token_adapter_ids, int T,
+                                void *const *Y, lora_stream_t stream)
+{
+    if (n < 1 || n > LORA_MAX_GROUP || !pools || !X || !W_base || !token_adapter_ids || !Y || T < 0)
+        return LORA_ERR_ARG;
+    for (int m = 0; m < n; ++m) {
+        if (!pools[m] || !X[m] || !W_base[m] || !Y[m]) return LORA_ERR_ARG;
+        if (pools[m]->device != pools[0]->device) return LORA_ERR_ARG;
+        for (int k = 0; k < m; ++k)
+            if (pools[k] == pools[m]) return LORA_ERR_ARG;  // each problem uses its pool's scratch
+    }
+    if (T == 0) return LORA_OK;
+    cudaStream_t s = (cudaStream_t)stream;
+    int path = pools[0]->path;
+    if (path == LORA_PATH_AUTO) path = T <= kDecodeMaxT ? LORA_PATH_DECODE : LORA_PATH_PREFILL;
+    if (path == LORA_PATH_DECODE && T > kDecodeMaxT) return LORA_ERR_ARG;
+    if (path == LORA_PATH_PREFILL) {
+        // prefill-sized batches: the layers one after another, each on its own path
+        for (int m = 0; m < n; ++m) {
+            lora_status st = run_linear(pools[m], X[m], W_base[m], token_adapter_ids, T, Y[m], s, true);
+            if (st != LORA_OK) return st;
+        }
+        return LORA_OK;
+    }
+    for (int m = 0; m < n; ++m) {
+        lora_status st = ensure_scratch(pools[m], T);
+        if (st != LORA_OK) return st;
+    }
+    CallMarks marks{pools[0], s};
+    if (!marks.begin()) return LORA_ERR_CUDA;
+    lora_status st = run_decode(pools, n, X, W_base, token_adapter_ids, T, Y, s, true, marks);
+    if (st != LORA_OK) return st;
+    for (int m = 0; m < n; ++m) pools[m]->n_calls += 1;
+    return LORA_OK;
 }
 
 lora_status lora_linear_host(lora_pool_t p, const void *X_host, const void *W_base,

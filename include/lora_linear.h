@@ -73,6 +73,7 @@ typedef enum {
 #define LORA_MAX_RANK 256         /* largest rank a pool can hold              */
 #define LORA_MAX_DIM 65536        /* largest d_in / d_out                      */
 #define LORA_RANK_PAGE 8          /* rank rows per pool page                   */
+#define LORA_MAX_GROUP 8          /* layers of one lora_linear_grouped call    */
 
 /* Which kernel family lora_linear uses. AUTO picks DECODE for T <= 256 and
  * PREFILL above; DECODE accepts T <= 256 only. Both compute the same result. */
@@ -163,6 +164,38 @@ lora_status lora_unload_adapter(lora_pool_t pool, int slot);
 lora_status lora_linear(lora_pool_t pool, const void *X, const void *W_base,
                         const int32_t *token_adapter_ids, int T, void *Y,
                         lora_stream_t stream);
+
+/*
+ * Several LoRA linear layers that share one batch of token ids, in one launch
+ * chain: for m = 0..n-1, Y[m] = lora_linear(pools[m], X[m], W_base[m], ids).
+ * The layers are typically the target modules of one transformer layer (q, k,
+ * v, o, gate, up, down), each module's adapters held in its own pool under the
+ * same slot ids. The pages train one adapter over these seven projections
+ * ("多 LoRA 热插拔: 一模型服多租户" (vLLM tutorial), sections "训练出 vLLM
+ * 兼容的 LoRA" (target_modules) and "性能注意事项" (one target set for the
+ * whole batch); icman.com.cn Multi-LoRA article, section 3.2); running them
+ * in one launch chain answers the per-call dispatch cost that the same
+ * article's section 4.2 names.
+ *   n: 1..LORA_MAX_GROUP.  pools, X, W_base, Y: HOST arrays of n entries
+ *   (pool handles and device pointers with the lora_linear layouts of each
+ *   pool's d_in / d_out); the pools must be distinct and on one device.
+ *   token_adapter_ids: device int32[T], shared by all layers.
+ * Decode-sized batches (T <= 256, or pools[0] forced to DECODE) run all layers
+ * in the same two kernels: one stream-K split over all the layers' weights, so
+ * the device streams them as one workload. Larger batches run the layers one
+ * after another, each as lora_linear would (pools[0]'s path setting applies).
+ * Results equal those of n separate lora_linear calls up to the order of the
+ * fp32 split-K sums. Bad ids are reported per pool (lora_pool_check_errors of
+ * the layer's pool); a kernel timeout in pools[0]'s error word. Scratch: each
+ * pool's per-token scratch, and pools[0] holds the call's split-K partial
+ * sums (grown on first use of a larger group, after a device synchronise).
+ * Errors returned at once: ARG (n out of range, null pointers, repeated or
+ * cross-device pools, T < 0, T > 256 with a forced DECODE path), SHAPE, OOM,
+ * CUDA.
+ */
+lora_status lora_linear_grouped(int n, const lora_pool_t *pools, const void *const *X,
+                                const void *const *W_base, const int32_t *token_adapter_ids,
+                                int T, void *const *Y, lora_stream_t stream);
 
 /*
  * Same as lora_linear, but X, token_adapter_ids and Y are HOST pointers

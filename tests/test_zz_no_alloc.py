@@ -29,7 +29,10 @@ def _cuda():
     torch.cuda.set_device(0)
 
 
-@pytest.mark.parametrize("T,d_in,d_out", [(64, 4096, 4096), (37, 72, 136), (256, 4096, 8192)])
+# (256, 4096, 16384): the partial sums of the full stream-K split do not fit the
+# fixed array, so the call runs with fewer CTAs (each covering more tiles)
+@pytest.mark.parametrize("T,d_in,d_out", [(64, 4096, 4096), (37, 72, 136), (256, 4096, 8192),
+                                          (256, 4096, 16384)])
 def test_noalloc_matches_pool_entry_twice(T, d_in, d_out):
     seed = 41
     W = to_dev(L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 1.0 / 64))
@@ -47,10 +50,15 @@ def test_noalloc_matches_pool_entry_twice(T, d_in, d_out):
 
 
 def test_noalloc_rejects_what_does_not_fit():
+    # 512 tiles of 128 output rows x 256 tokens of fp32 partials exceed the array
+    # whatever the number of CTAs
+    Ww = torch.zeros((65536, 64), dtype=torch.bfloat16, device="cuda")
+    Xw = torch.zeros((256, 64), dtype=torch.bfloat16, device="cuda")
+    Yw = torch.empty((256, 65536), dtype=torch.bfloat16, device="cuda")
+    assert al.lora_base_linear_noalloc(Xw, Ww, 256, 64, 65536, Yw) == al.LORA_ERR_SHAPE
     W = torch.zeros((16384, 4096), dtype=torch.bfloat16, device="cuda")
     X = torch.zeros((256, 4096), dtype=torch.bfloat16, device="cuda")
     Y = torch.empty((256, 16384), dtype=torch.bfloat16, device="cuda")
-    assert al.lora_base_linear_noalloc(X, W, 256, 4096, 16384, Y) == al.LORA_ERR_SHAPE
     assert al.lora_base_linear_noalloc(X, W, 257, 4096, 16384, Y) == al.LORA_ERR_ARG
     assert al.lora_base_linear_noalloc(X, W, 8, 4090, 16384, Y) == al.LORA_ERR_SHAPE
     assert al.lora_base_linear_noalloc(None, W, 8, 4096, 16384, Y) == al.LORA_ERR_ARG
