@@ -264,6 +264,221 @@ def cpu_oracle_rate(p, seconds: float, max_tokens: int):
     return done / el, oracle.num_threads(), f"{n} of {p.T} tokens per pass, {done} tokens in {el:.1f} s"
 
 
+# ------------------------------------------------------- grouped layer (7 modules)
+
+def run_grouped_layer(args):
+    """A Llama-3-8B decoder layer's seven target modules (q,k,v,o,gate,up,down; T = 32,
+    32 adapters r16 per module, one id vector) per step: one lora_linear_grouped call,
+    against seven lora_linear calls and seven base-only calls of the same layer."""
+    import torch
+    import adapter_linear_gb300 as al
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    probs = L.llama3_7mod()
+    T = probs[0].T
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    Xs = [t(p.X) for p in probs]
+    ids = t(probs[0].ids)
+    Ys = [torch.empty((T, p.d_out), dtype=torch.bfloat16, device=dev) for p in probs]
+
+    def new_layer():
+        pools, Ws = [], []
+        for p in probs:
+            pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
+            for slot, ad in p.adapters.items():
+                pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
+            pool.reserve(T)
+            pools.append(pool)
+            Ws.append(t(p.W))
+        return pools, Ws
+
+    layers = [new_layer()]
+    layer_bytes = sum(w.numel() * 2 for w in layers[0][1]) + \
+        sum(pl.stats()["bytes_held"] for pl in layers[0][0])
+    R = max(2, -(-3 * l2 // layer_bytes))
+    while len(layers) < R:
+        layers.append(new_layer())
+
+    def grouped_step(k):
+        pools, Ws = layers[k % R]
+        al.LoraPool.linear_grouped(pools, Xs, Ws, ids, Ys)
+
+    def separate_step(k):
+        pools, Ws = layers[k % R]
+        for m, pool in enumerate(pools):
+            pool.linear(Xs[m], Ws[m], ids, Ys[m])
+
+    def base_step(k):
+        pools, Ws = layers[k % R]
+        for m, pool in enumerate(pools):
+            pool.base_linear(Xs[m], Ws[m], Ys[m])
+
+    no_ids = torch.full_like(ids, -1)
+
+    def grouped_base_step(k):  # the same grouped call with every token on the base path
+        pools, Ws = layers[k % R]
+        al.LoraPool.linear_grouped(pools, Xs, Ws, no_ids, Ys)
+
+    graphs = []
+
+    def program(step, n, timing=False):
+        for pools, _ in layers:
+            for pool in pools:
+                pool.enable_timing(timing)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for k in range(n):
+                step(k)
+        for pools, _ in layers:
+            for pool in pools:
+                pool.enable_timing(False)
+        graphs.append(g)
+        return g.replay
+
+    def time_program(prog):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        prog()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1)
+
+    for k in range(max(args.warmup, R)):
+        grouped_step(k)
+        separate_step(k)
+        base_step(k)
+        grouped_base_step(k)
+    torch.cuda.synchronize(dev)
+    g_prog = program(grouped_step, args.steps)
+    gb_prog = program(grouped_base_step, args.steps)
+    s_prog = program(separate_step, args.steps)
+    b_prog = program(base_step, args.steps)
+    program(grouped_step, args.warmup)()
+    torch.cuda.synchronize(dev)
+
+    nvml = NvmlClockSampler(dev)
+    with ClockSampler(dev.index or 0) as clocks, nvml:
+        torch.cuda.synchronize(dev)
+        total_ms = time_program(g_prog)
+        torch.cuda.synchronize(dev)
+    if ws > 1:
+        tt = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    sep_ms = time_program(s_prog)
+    base_ms = time_program(b_prog)
+    gbase_ms = time_program(gb_prog)
+
+    # per-kernel device time of the grouped call (events of the first module's pool)
+    kprog = program(grouped_step, R, timing=True)
+    kts = []
+    for _ in range(max(1, -(-args.steps // R))):
+        kprog()
+        torch.cuda.synchronize(dev)
+        kts += [pools[0].kernel_times() for pools, _ in layers]
+    gemm_ms = statistics.mean(k["base_gemm"] for k in kts)
+    finish_ms = statistics.mean(k["finish_expand"] for k in kts)
+
+    # e2e: pinned host inputs copied in, the grouped call, outputs copied back
+    Xh = [x.cpu().pin_memory() for x in Xs]
+    idh = ids.cpu().pin_memory()
+    Yh = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for y in Ys]
+    Xd = [torch.empty_like(x) for x in Xs]
+    idd = torch.empty_like(ids)
+    pools0, Ws0 = layers[0]
+
+    def e2e_once():
+        for a, b in zip(Xd, Xh):
+            a.copy_(b, non_blocking=True)
+        idd.copy_(idh, non_blocking=True)
+        al.LoraPool.linear_grouped(pools0, Xd, Ws0, idd, Ys)
+        for a, b in zip(Yh, Ys):
+            a.copy_(b, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    for _ in range(3):
+        e2e_once()
+    e2e_s = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        e2e_once()
+        e2e_s += time.perf_counter() - t0
+    for pools, _ in layers:
+        for pool in pools:
+            assert pool.check_errors() == al.LORA_OK
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    abs_ = [algorithmic_bytes(p) for p in probs]
+    w_b = sum(a["w"] for a in abs_)
+    x_b = sum(a["x"] for a in abs_)
+    y_b = sum(a["y"] for a in abs_)
+    ad_a = sum(a["adapter_A"] for a in abs_)
+    ad_all = sum(a["adapters"] for a in abs_)
+    hbm_peak, _, peak_src = measured_peaks()
+    gemm_bytes = w_b + x_b + ad_a
+    achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        n, done, t0 = 2, 0, time.perf_counter()
+        ads = [oracle.problem_adapters(p) for p in probs]
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            for p, a in zip(probs, ads):
+                oracle.lora_linear(p.X[:n], p.W, p.ids[:n], a, p.max_adapters)
+            done += n
+        el = time.perf_counter() - t0
+        cpu = {"value": done / el, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+               "sample": f"{n} of {T} tokens through all 7 modules per pass, {done} tokens in {el:.1f} s"}
+    clk = nvml.summary() or dict(clocks.summary(), source="nvidia-smi")
+    out = {
+        "metric": METRIC, "value": T * args.steps * ws / (total_ms / 1e3), "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "Llama-3-8B decoder layer, 7 target modules in one grouped call",
+                   "T": T, "modules": [p.name.split("/")[1] for p in probs], "adapters": 32,
+                   "rank": 16, "layers": R,
+                   "l2": f"inputs larger than L2: {R} layers of 7 modules, each its own W and "
+                         f"pools ({R * layer_bytes / 1e6:.0f} MB cycled)",
+                   "launch": "one CUDA graph of the K steps",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "separate_calls_ms_per_step": sep_ms / args.steps,
+        "base_only_ms_per_step": gbase_ms / args.steps,
+        "base_only_separate_calls_ms_per_step": base_ms / args.steps,
+        "overhead_vs_base": total_ms / gbase_ms - 1.0,
+        "overhead_floor": ad_all / (w_b + x_b + y_b),
+        "kernel_ms": {"base_gemm": gemm_ms, "finish_expand": finish_ms},
+        "roofline": {"kernel": "gemm_decode_kernel", "bound": "hbm", "achieved": achieved,
+                     "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
+                     "traffic": None, "algorithmic_bytes": gemm_bytes, "peak_source": peak_src},
+        "clocks": clk,
+        "e2e": {"value": T * args.steps * ws / e2e_s, "unit": UNIT, "h2d_bytes_per_step": x_b + T * 4,
+                "d2h_bytes_per_step": y_b},
+        "gpu_launches": 2 * args.steps,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(out), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
 # --------------------------------------------------------------------- main
 
 def dist_env():
@@ -320,6 +535,8 @@ def main():
 
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "llama3_layer":
+        return run_grouped_layer(args)
 
     import torch
     import adapter_linear_gb300 as al
