@@ -14,7 +14,7 @@ from __future__ import annotations
 import ctypes
 import os
 import subprocess
-from typing import Dict, Optional, Tuple
+from typing import Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
@@ -61,6 +61,9 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.oracle_segments.restype = ctypes.c_int
     lib.oracle_lora_linear.argtypes = [vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, vp, vp]
     lib.oracle_lora_linear.restype = ctypes.c_int
+    lib.oracle_lora_linear_chains.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, vp,
+                                              vp]
+    lib.oracle_lora_linear_chains.restype = ctypes.c_int
     if path == LIB:
         _lib = lib
     return lib
@@ -110,6 +113,18 @@ def lora_linear(X: np.ndarray, W: np.ndarray, ids: np.ndarray,
     T, d_in = X.shape
     d_out = W.shape[0]
     assert W.shape[1] == d_in and ids.shape[0] == T
+    A_ptrs, B_ptrs, ranks, alphas, keep = _slot_arrays(adapters, n_slots, d_in, d_out)
+    Y = np.empty((T, d_out), np.float64)
+    rc = lib.oracle_lora_linear(_ptr(X), _ptr(W), _ptr(ids), T, d_in, d_out, n_slots,
+                                ctypes.cast(A_ptrs, ctypes.c_void_p),
+                                ctypes.cast(B_ptrs, ctypes.c_void_p), _ptr(ranks), _ptr(alphas),
+                                _ptr(Y))
+    if rc != OK:
+        raise OracleError(rc)
+    return Y
+
+
+def _slot_arrays(adapters, n_slots, d_in, d_out):
     n = max(n_slots, 1)
     A_ptrs = (ctypes.c_void_p * n)()
     B_ptrs = (ctypes.c_void_p * n)()
@@ -126,14 +141,49 @@ def lora_linear(X: np.ndarray, W: np.ndarray, ids: np.ndarray,
         B_ptrs[slot] = B.ctypes.data
         ranks[slot] = r
         alphas[slot] = alpha
+    return A_ptrs, B_ptrs, ranks, alphas, keep
+
+
+def lora_linear_chains(X: np.ndarray, W: np.ndarray, token_lists: Sequence[Sequence[int]],
+                       adapters: Dict[int, Tuple[np.ndarray, np.ndarray, int, float]],
+                       n_slots: int, lib=None) -> np.ndarray:
+    """Y (float64) = X W^T + sum over token t's listed adapters c of s_c (X A_c) B_c.
+
+    token_lists[t]: the adapter slots applied to token t (empty: base only). Same
+    adapter tuples as ``lora_linear``.
+    """
+    lib = lib or load()
+    X = np.ascontiguousarray(X, dtype=np.uint16)
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    T, d_in = X.shape
+    d_out = W.shape[0]
+    assert W.shape[1] == d_in and len(token_lists) == T
+    off = np.zeros(T + 1, np.int32)
+    off[1:] = np.cumsum([len(lst) for lst in token_lists])
+    flat = np.array([c for lst in token_lists for c in lst] or [0], np.int32)
+    A_ptrs, B_ptrs, ranks, alphas, keep = _slot_arrays(adapters, n_slots, d_in, d_out)
     Y = np.empty((T, d_out), np.float64)
-    rc = lib.oracle_lora_linear(_ptr(X), _ptr(W), _ptr(ids), T, d_in, d_out, n_slots,
-                                ctypes.cast(A_ptrs, ctypes.c_void_p),
-                                ctypes.cast(B_ptrs, ctypes.c_void_p), _ptr(ranks), _ptr(alphas),
-                                _ptr(Y))
+    rc = lib.oracle_lora_linear_chains(_ptr(X), _ptr(W), _ptr(off), _ptr(flat), T, d_in, d_out,
+                                       n_slots, ctypes.cast(A_ptrs, ctypes.c_void_p),
+                                       ctypes.cast(B_ptrs, ctypes.c_void_p), _ptr(ranks),
+                                       _ptr(alphas), _ptr(Y))
     if rc != OK:
         raise OracleError(rc)
     return Y
+
+
+def chain_lists(ids: np.ndarray, chains: Dict[int, Sequence[int]]) -> List[List[int]]:
+    """Per-token adapter lists for ids that may name chain slots: a chain slot stands for
+    its members, a plain slot for itself, -1 for nothing."""
+    out = []
+    for i in np.asarray(ids).tolist():
+        if i == -1:
+            out.append([])
+        elif i in chains:
+            out.append(list(chains[i]))
+        else:
+            out.append([i])
+    return out
 
 
 def problem_adapters(problem) -> Dict[int, Tuple[np.ndarray, np.ndarray, int, float]]:

@@ -195,3 +195,80 @@ int oracle_lora_linear(const uint16_t *X, const uint16_t *W, const int32_t *ids,
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------------ adapter chains */
+
+/*
+ * Several adapters on one token. Token t applies the adapters
+ * list[off[t]] .. list[off[t+1] - 1] (an empty range: the base output only);
+ * their low-rank branches add:
+ *
+ *   Y[t,n] = sum_k X[t,k] W[n,k]
+ *          + sum over listed c of  s_c * sum_j ( sum_k X[t,k] A_c[k,j] ) B_c[j,n]
+ *
+ * Source: "LoRA-Land: 将大模型变成操作系统..." (blog), section 技术方案 item 3
+ * (动态加载与组合: several adapters are combined like a pipeline and applied to
+ * the kernel in order) and section 核心实现解析 / 3. 热插拔 API 与组合
+ * (set_adaptive_chain). Applying the members' weight updates to one linear
+ * layer one after another gives W + dW_a + dW_b, so at the layer the branches
+ * add and their order does not change the result.
+ * Same slot arrays as oracle_lora_linear; off has T + 1 entries, off[0] = 0,
+ * non-decreasing. Returns ORACLE_ERR_BAD_ADAPTER_ID (writing nothing) if a
+ * listed id is not a loaded slot, ORACLE_ERR_ARG for malformed offsets.
+ */
+int oracle_lora_linear_chains(const uint16_t *X, const uint16_t *W, const int32_t *off,
+                              const int32_t *list, int64_t T, int64_t d_in, int64_t d_out,
+                              int32_t n_slots, const uint16_t *const *A,
+                              const uint16_t *const *B, const int32_t *rank,
+                              const double *alpha, double *Y)
+{
+    if (T < 0 || d_in <= 0 || d_out <= 0 || off[0] != 0) return ORACLE_ERR_ARG;
+    for (int64_t t = 0; t < T; ++t) {
+        if (off[t + 1] < off[t]) return ORACLE_ERR_ARG;
+        for (int32_t e = off[t]; e < off[t + 1]; ++e) {
+            const int32_t c = list[e];
+            if (c < 0 || c >= n_slots || A[c] == NULL || B[c] == NULL || rank[c] <= 0)
+                return ORACLE_ERR_BAD_ADAPTER_ID;
+        }
+    }
+    int64_t max_r = 1;
+    for (int32_t c = 0; c < n_slots; ++c)
+        if (A[c] && rank[c] > max_r) max_r = rank[c];
+
+#pragma omp parallel
+    {
+        double *low = (double *)malloc(sizeof(double) * (size_t)max_r);
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t t = 0; t < T; ++t) {
+            const uint16_t *xt = X + t * d_in;
+            double *yt = Y + t * d_out;
+            /* the base row */
+            for (int64_t n = 0; n < d_out; ++n) {
+                double acc = 0.0;
+                for (int64_t k = 0; k < d_in; ++k)
+                    acc += bf16_value(xt[k]) * bf16_value(W[n * d_in + k]);
+                yt[n] = acc;
+            }
+            /* each listed adapter's branch, added on */
+            for (int32_t e = off[t]; e < off[t + 1]; ++e) {
+                const int32_t c = list[e];
+                const int64_t rc = rank[c];
+                const double sc = alpha[c] / (double)rc;
+                for (int64_t j = 0; j < rc; ++j) {
+                    double acc = 0.0;
+                    for (int64_t k = 0; k < d_in; ++k)
+                        acc += bf16_value(xt[k]) * bf16_value(A[c][k * rc + j]);
+                    low[j] = acc;
+                }
+                for (int64_t n = 0; n < d_out; ++n) {
+                    double branch = 0.0;
+                    for (int64_t j = 0; j < rc; ++j)
+                        branch += low[j] * bf16_value(B[c][j * d_out + n]);
+                    yt[n] += sc * branch;
+                }
+            }
+        }
+        free(low);
+    }
+    return ORACLE_OK;
+}

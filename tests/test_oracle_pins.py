@@ -15,6 +15,11 @@ itself. Nothing here re-types the oracle's formula; each check is one of:
   changes nothing (the vLLM tutorial's 性能注意事项 says mixed ranks get
   aligned to the largest one), permuting tokens permutes rows, linearity in X;
 * strict mode (icman.com.cn article section 4.1): an unknown id is an error;
+* adapter chains (LoRA-Land blog, 技术方案 item 3 and 3. 热插拔 API 与组合:
+  set_adaptive_chain): a token's listed adapters equal the merged weight
+  W + sum_c s_c (A_c B_c)^T applied with numpy, and a chain of two adapters
+  with one scale equals the single adapter whose A and B are the members'
+  concatenated; the order of the members does not matter;
 * exhaustive brute force for the segment builder on every id vector of
   length <= 5 over {-1, 0, 1, 2}: the output must be a permutation, sorted by
   id, stable, with maximal segments.
@@ -225,9 +230,64 @@ def pin_segments_bruteforce(lib):
         check_segments_properties(ids, oracle.segments(ids, 50, lib=lib))
 
 
+def chain_problem(seed, T=10, d_in=20, d_out=18):
+    X, W, _, ads = small_problem(seed, T=T, d_in=d_in, d_out=d_out, ranks=(3, 8, 5, 4))
+    g = L.rng_for(seed, 61)
+    lists = []
+    for t in range(T):
+        n = int(g.integers(0, 4))
+        lists.append([int(c) for c in g.choice(4, size=n, replace=False)])
+    return X, W, lists, ads
+
+
+def pin_chain_merge_mode(lib):
+    """Each token's listed adapters equal the merged weight W + sum_c s_c (A_c B_c)^T."""
+    X, W, lists, ads = chain_problem(21)
+    assert any(len(lst) >= 2 for lst in lists) and any(len(lst) == 0 for lst in lists)
+    Y = oracle.lora_linear_chains(X, W, lists, ads, 4, lib=lib)
+    Xv, Wv = val(X), val(W)
+    for t, lst in enumerate(lists):
+        Wm = Wv.copy()
+        for c in lst:
+            A, B, r, alpha = ads[c]
+            Wm = Wm + (alpha / r) * (val(A) @ val(B)).T
+        np.testing.assert_allclose(Y[t], Xv[t] @ Wm.T, rtol=1e-12, atol=1e-12)
+
+
+def pin_chain_concatenation(lib):
+    """A chain of two adapters with one scale s is the rank r_a + r_b adapter with
+    A = [A_a | A_b], B = [B_a ; B_b] and alpha = s (r_a + r_b), through the single-adapter
+    entry point."""
+    X, W, _, _ = small_problem(22)
+    d_in, d_out = X.shape[1], W.shape[0]
+    a = L.make_adapter(22, 0, d_in, d_out, 3, 6.0, std=0.5)    # s = 2
+    b = L.make_adapter(22, 1, d_in, d_out, 5, 10.0, std=0.5)   # s = 2
+    ads = {0: (a.A, a.B, 3, 6.0), 1: (b.A, b.B, 5, 10.0)}
+    cat = {0: (np.concatenate([a.A, b.A], axis=1), np.concatenate([a.B, b.B], axis=0), 8, 16.0)}
+    T = X.shape[0]
+    Yc = oracle.lora_linear_chains(X, W, [[0, 1]] * T, ads, 2, lib=lib)
+    Ys = oracle.lora_linear(X, W, np.zeros(T, np.int32), cat, 1, lib=lib)
+    np.testing.assert_allclose(Yc, Ys, rtol=1e-12, atol=1e-12)
+
+
+def pin_chain_order_and_reduction(lib):
+    X, W, lists, ads = chain_problem(23)
+    Y = oracle.lora_linear_chains(X, W, lists, ads, 4, lib=lib)
+    Yr = oracle.lora_linear_chains(X, W, [lst[::-1] for lst in lists], ads, 4, lib=lib)
+    np.testing.assert_allclose(Y, Yr, rtol=1e-12, atol=1e-12)
+    # lists of at most one adapter: the single-adapter entry point
+    ids = np.array([lst[0] if lst else -1 for lst in lists], np.int32)
+    Y1 = oracle.lora_linear_chains(X, W, [[i] if i >= 0 else [] for i in ids], ads, 4, lib=lib)
+    np.testing.assert_allclose(Y1, oracle.lora_linear(X, W, ids, ads, 4, lib=lib),
+                               rtol=1e-12, atol=1e-12)
+    with pytest.raises(oracle.OracleError):
+        oracle.lora_linear_chains(X, W, [[0, 7]] + lists[1:], ads, 4, lib=lib)
+
+
 PINS = [pin_golden, pin_basis_rows, pin_base_rows_match_numpy, pin_zero_B_is_base,
         pin_merge_mode, pin_rank_padding, pin_permutation, pin_linearity, pin_scale,
-        pin_strict_ids, pin_segments_bruteforce]
+        pin_strict_ids, pin_segments_bruteforce, pin_chain_merge_mode, pin_chain_concatenation,
+        pin_chain_order_and_reduction]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -252,6 +312,14 @@ MUTATIONS = {
                       "if (a->index != b->index) return a->index < b->index ? 1 : -1;"),
     "base_last": ("if (a->key != b->key) return a->key < b->key ? -1 : 1;",
                   "if (a->key != b->key) return (uint32_t)a->key < (uint32_t)b->key ? -1 : 1;"),
+    "chain_last_member_only": ("yt[n] += sc * branch;",
+                               "yt[n] = (e + 1 == off[t + 1]) ? yt[n] + sc * branch : yt[n];"),
+    "chain_shared_scale": ("const double sc = alpha[c] / (double)rc;",
+                           "const double sc = alpha[list[off[t]]] / (double)rank[list[off[t]]];"),
+    "chain_B_transposed": ("branch += low[j] * bf16_value(B[c][j * d_out + n]);",
+                           "branch += low[j] * bf16_value(B[c][n * rc + j]);"),
+    "chain_W_transposed": ("acc += bf16_value(xt[k]) * bf16_value(W[n * d_in + k]);",
+                           "acc += bf16_value(xt[k]) * bf16_value(W[k * d_out + n]);"),
     "lenient_segment_ids": ("if (ids[t] < -1 || ids[t] >= n_slots) return ORACLE_ERR_BAD_ADAPTER_ID;",
                             "if (ids[t] < -1) return ORACLE_ERR_BAD_ADAPTER_ID;"),
 }
