@@ -23,6 +23,7 @@ STATUS_NAMES = {
     4: "LORA_ERR_SLOT_OCCUPIED", 5: "LORA_ERR_SLOT_EMPTY", 6: "LORA_ERR_RANK",
     7: "LORA_ERR_BAD_ADAPTER_ID", 8: "LORA_ERR_CUDA", 9: "LORA_ERR_OOM", 10: "LORA_ERR_TIMEOUT",
     11: "LORA_ERR_UNSUPPORTED",
+    12: "LORA_ERR_IN_USE",
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 LORA_PATH_AUTO, LORA_PATH_DECODE, LORA_PATH_PREFILL = 0, 1, 2
@@ -35,7 +36,7 @@ EXPORTS = (
     "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
     "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
-    "lora_base_linear_noalloc", "lora_linear_grouped",
+    "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
 )
 LORA_MAX_GROUP = 8
 LORA_KERNEL_SLOTS = 4
@@ -84,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_pool_kernel_times": [vp, vp],
         "lora_base_linear_noalloc": [vp, vp, i32, i32, i32, vp, vp],
         "lora_linear_grouped": [i32, vp, vp, vp, vp, i32, vp, vp],
+        "lora_define_chain": [vp, i32, vp, i32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -150,6 +152,11 @@ def lora_linear(pool: int, X, W_base, ids, T: int, Y, stream=None) -> int:
 def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream=None) -> int:
     return load_library().lora_linear_host(pool, _ptr(X_host), _ptr(W_base), _ptr(ids_host), T,
                                            _ptr(Y_host), _stream(stream))
+
+
+def lora_define_chain(pool: int, chain_slot: int, member_slots) -> int:
+    members = (ctypes.c_int * max(len(member_slots), 1))(*member_slots)
+    return load_library().lora_define_chain(pool, chain_slot, members, len(member_slots))
 
 
 def lora_linear_grouped(pools, X, W_base, ids, T: int, Y, stream=None) -> int:
@@ -254,6 +261,9 @@ class LoraPool:
 
     def unload_adapter(self, slot: int):
         _check(lora_unload_adapter(self.handle, slot), "lora_unload_adapter")
+
+    def define_chain(self, chain_slot: int, member_slots):
+        _check(lora_define_chain(self.handle, chain_slot, list(member_slots)), "lora_define_chain")
 
     def set_path(self, path: int):
         _check(lora_pool_set_path(self.handle, path), "lora_pool_set_path")

@@ -304,7 +304,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
                 const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
                 if (q >= row[SLOT_NPAGES]) continue;
-                shrink_pair(t, row[SLOT_PAGES + q], __int_as_float(row[SLOT_SCALE]), pr, q, red);
+                shrink_pair(t, row[SLOT_PAGES + q],
+                            __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]), pr, q, red);
             }
         }
         for (int seg = 0; seg < nseg; ++seg) {

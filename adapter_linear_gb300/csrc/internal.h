@@ -19,10 +19,16 @@ namespace lora {
 constexpr int kRankPage = 8;
 
 // Slot table: int32 [max_adapters][slot_stride]
-constexpr int SLOT_RANK = 0;    // rank (0 = empty slot)
-constexpr int SLOT_NPAGES = 1;  // ceil(rank / 8)
-constexpr int SLOT_SCALE = 2;   // alpha / rank as fp32 bits
-constexpr int SLOT_PAGES = 4;   // page ids, npages entries
+constexpr int SLOT_RANK = 0;     // rank (0 = empty slot); a chain: the members' ranks summed
+constexpr int SLOT_NPAGES = 1;   // pages: ceil(rank / 8); a chain: the members' pages
+constexpr int SLOT_SCALE = 2;    // alpha / rank as fp32 bits (a chain: its first member's)
+constexpr int SLOT_MEMBERS = 3;  // a chain's member adapters (0: an adapter's own pages)
+constexpr int SLOT_PAGES = 4;    // page ids, npages entries (up to max_pages), then one
+                                 // fp32 scale per page at slot_page_scale(max_pages, q)
+__host__ __device__ constexpr int slot_page_scale(int max_pages, int q)
+{
+    return SLOT_PAGES + max_pages + q;
+}
 
 // Segment-table header (int32 [4])
 constexpr int HDR_NBASE = 0;    // tokens with id -1 (and invalid ids)

@@ -12,6 +12,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <map>
 #include <vector>
 
 #include <cudaTypedefs.h>
@@ -40,6 +41,8 @@ struct lora_pool {
     int32_t *d_slots = nullptr;
     std::vector<int32_t> h_slots;
     std::vector<int32_t> free_pages;  // stack; back() is taken first
+    std::vector<int32_t> chain_refs;  // per slot: chains that list it as a member
+    std::map<int, std::vector<int>> chain_members;  // chain slot -> member slots
     int *d_err = nullptr;
     uint16_t *stage_A = nullptr, *stage_B = nullptr;
     int32_t *d_page_list = nullptr;
@@ -379,6 +382,7 @@ const char *lora_status_string(lora_status s)
     case LORA_ERR_OOM: return "out of device memory";
     case LORA_ERR_TIMEOUT: return "a kernel wait timed out";
     case LORA_ERR_UNSUPPORTED: return "device is not compute capability 10.3";
+    case LORA_ERR_IN_USE: return "a chain still lists this adapter";
     }
     return "unknown status";
 }
@@ -408,10 +412,13 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
     p->d_out = d_out;
     p->max_pages = (max_rank + kRankPage - 1) / kRankPage;
     p->num_pages = max_adapters * p->max_pages + 1;
-    p->slot_stride = ((SLOT_PAGES + p->max_pages + 3) / 4) * 4;
+    // page ids, then one scale per page, and one more readable scale entry (the
+    // tensor-core shrink reads the scale of the zero page that pads an odd count)
+    p->slot_stride = ((slot_page_scale(p->max_pages, p->max_pages) + 1 + 3) / 4) * 4;
     p->ldv = ((p->max_pages * kRankPage + 15) / 16) * 16;
     p->ldh = 2 * (((p->max_pages * kRankPage + 31) / 32) * 32);
     p->h_slots.assign((size_t)max_adapters * p->slot_stride, 0);
+    p->chain_refs.assign(max_adapters, 0);
     p->free_pages.reserve(p->num_pages - 1);
     for (int pg = p->num_pages - 1; pg >= 1; --pg) p->free_pages.push_back(pg);
 
@@ -501,7 +508,10 @@ lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void
     new_row[SLOT_NPAGES] = npages;
     const float scale = alpha / (float)rank;
     std::memcpy(&new_row[SLOT_SCALE], &scale, sizeof(float));
-    for (int q = 0; q < npages; ++q) new_row[SLOT_PAGES + q] = pages[q];
+    for (int q = 0; q < npages; ++q) {
+        new_row[SLOT_PAGES + q] = pages[q];
+        std::memcpy(&new_row[slot_page_scale(p->max_pages, q)], &scale, sizeof(float));
+    }
     ok = ok &&
          cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, new_row.data(),
                          sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice, s) == cudaSuccess;
@@ -522,6 +532,7 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
     if (slot < 0 || slot >= p->max_adapters) return LORA_ERR_SLOT_RANGE;
     int32_t *row = &p->h_slots[(size_t)slot * p->slot_stride];
     if (row[SLOT_RANK] == 0) return LORA_ERR_SLOT_EMPTY;
+    if (p->chain_refs[slot] > 0) return LORA_ERR_IN_USE;  // a chain still lists it
     CUDA_TRY(cudaDeviceSynchronize());
     std::vector<int32_t> zero(p->slot_stride, 0);
     if (cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, zero.data(),
@@ -530,9 +541,59 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
         cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
         return LORA_ERR_CUDA;
     const int npages = row[SLOT_NPAGES];
-    for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
+    if (row[SLOT_MEMBERS] > 0) {
+        // a chain owns no pages: release its members
+        for (int m : p->chain_members[slot]) p->chain_refs[m] -= 1;
+        p->chain_members.erase(slot);
+    } else {
+        for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
+    }
     std::fill(row, row + p->slot_stride, 0);
     p->n_unloads += 1;
+    return LORA_OK;
+}
+
+lora_status lora_define_chain(lora_pool_t p, int chain_slot, const int *member_slots, int n)
+{
+    if (!p || !member_slots || n < 1) return LORA_ERR_ARG;
+    if (chain_slot < 0 || chain_slot >= p->max_adapters) return LORA_ERR_SLOT_RANGE;
+    int32_t *row = &p->h_slots[(size_t)chain_slot * p->slot_stride];
+    if (row[SLOT_RANK] != 0) return LORA_ERR_SLOT_OCCUPIED;
+    std::vector<int32_t> new_row(p->slot_stride, 0);
+    int rank = 0, npages = 0;
+    for (int e = 0; e < n; ++e) {
+        const int m = member_slots[e];
+        if (m < 0 || m >= p->max_adapters) return LORA_ERR_SLOT_RANGE;
+        const int32_t *mrow = &p->h_slots[(size_t)m * p->slot_stride];
+        if (mrow[SLOT_RANK] == 0) return LORA_ERR_SLOT_EMPTY;
+        if (mrow[SLOT_MEMBERS] > 0 || m == chain_slot) return LORA_ERR_ARG;  // members are adapters
+        for (int k = 0; k < e; ++k)
+            if (member_slots[k] == m) return LORA_ERR_ARG;  // each member once
+        const int mp = mrow[SLOT_NPAGES];
+        if (npages + mp > p->max_pages) return LORA_ERR_RANK;  // the chain's pages fit one row
+        for (int q = 0; q < mp; ++q) {
+            new_row[SLOT_PAGES + npages + q] = mrow[SLOT_PAGES + q];
+            new_row[slot_page_scale(p->max_pages, npages + q)] =
+                mrow[slot_page_scale(p->max_pages, q)];
+        }
+        npages += mp;
+        rank += mrow[SLOT_RANK];
+    }
+    new_row[SLOT_RANK] = rank;
+    new_row[SLOT_NPAGES] = npages;
+    new_row[SLOT_SCALE] = p->h_slots[(size_t)member_slots[0] * p->slot_stride + SLOT_SCALE];
+    new_row[SLOT_MEMBERS] = n;
+    // calls already enqueued keep seeing the old table
+    CUDA_TRY(cudaDeviceSynchronize());
+    if (cudaMemcpyAsync(p->d_slots + (size_t)chain_slot * p->slot_stride, new_row.data(),
+                        sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice,
+                        p->copy_stream) != cudaSuccess ||
+        cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    std::copy(new_row.begin(), new_row.end(), row);
+    std::vector<int> &members = p->chain_members[chain_slot];
+    members.assign(member_slots, member_slots + n);
+    for (int m : members) p->chain_refs[m] += 1;
     return LORA_OK;
 }
 

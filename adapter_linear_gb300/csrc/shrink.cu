@@ -35,8 +35,8 @@ struct UnitInfo {
     int p0, p1;       // positions in `order`
     int npages;       // adapter pages
     int n;            // MMA N: npages * 8 rounded up to 16
-    float scale;
     const int32_t *pages;
+    const int32_t *scales;  // fp32 bits, one per page (up to n / 8 entries readable)
 };
 
 __device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs)
@@ -54,8 +54,8 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const 
     const int32_t *row = pool.slots + (size_t)tabs.seg_slot[s] * pool.slot_stride;
     r.npages = row[SLOT_NPAGES];
     r.n = ((r.npages * kRankPage + 15) / 16) * 16;
-    r.scale = __int_as_float(row[SLOT_SCALE]);
     r.pages = row + SLOT_PAGES;
+    r.scales = row + slot_page_scale(pool.max_pages, 0);
     return r;
 }
 
@@ -231,11 +231,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint32_t v[16];
                 tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(buf * nmax + col), v);
                 if (valid) {
+                    // each page's columns take that page's scale (a chain's members differ)
+                    const float s_lo = __int_as_float(ui.scales[col / kRankPage]);
+                    const float s_hi = __int_as_float(ui.scales[col / kRankPage + 1]);
                     uint32_t hi[8], lo[8];
 #pragma unroll
                     for (int j = 0; j < 16; j += 2) {
-                        const float a0 = ui.scale * __uint_as_float(v[j]);
-                        const float a1 = ui.scale * __uint_as_float(v[j + 1]);
+                        const float sc = j < kRankPage ? s_lo : s_hi;
+                        const float a0 = sc * __uint_as_float(v[j]);
+                        const float a1 = sc * __uint_as_float(v[j + 1]);
                         const uint32_t h = pack_bf16x2(a0, a1);
                         hi[j / 2] = h;
                         lo[j / 2] = pack_bf16x2(a0 - bf16_lo(h), a1 - bf16_hi(h));

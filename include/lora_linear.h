@@ -65,7 +65,8 @@ typedef enum {
     LORA_ERR_OOM = 9,             /* device allocation failed                  */
     LORA_ERR_TIMEOUT = 10,        /* a kernel's bounded wait ran out (reported
                                      by lora_pool_check_errors)                */
-    LORA_ERR_UNSUPPORTED = 11     /* no compute-capability-10.3 device         */
+    LORA_ERR_UNSUPPORTED = 11,    /* no compute-capability-10.3 device         */
+    LORA_ERR_IN_USE = 12          /* unload of an adapter a chain still lists  */
 } lora_status;
 
 /* Limits. */
@@ -136,8 +137,33 @@ lora_status lora_load_adapter(lora_pool_t pool, int slot, const void *A, const v
 
 /* Unload ("unload_adapter", same sections): waits for enqueued calls, returns
  * the slot's pages to the free list and marks it empty. Host-blocking.
- * Errors: SLOT_RANGE, SLOT_EMPTY. */
+ * Unloading a chain slot releases its members and frees no pages.
+ * Errors: SLOT_RANGE, SLOT_EMPTY, IN_USE (a chain still lists the adapter:
+ * unload the chain first). */
 lora_status lora_unload_adapter(lora_pool_t pool, int slot);
+
+/*
+ * Adapter chain: make chain_slot stand for the n adapters in member_slots
+ * applied together, so that a token with id chain_slot gets
+ *
+ *     Y[t] = X[t] W_base^T + sum over members m of s_m (X[t] A_m) B_m.
+ *
+ * The LoRA-Land blog combines adapters like a pipeline applied to the kernel
+ * in order (section 技术方案 item 3; section 核心实现解析 / 3. 热插拔 API 与组合,
+ * set_adaptive_chain); at one linear layer the members' weight updates add,
+ * W + dW_1 + ... + dW_n, whatever their order. The chain copies no weights:
+ * its slot lists the members' pages, each with its member's scale, so both
+ * kernel families run it as one adapter of rank sum(r_m).
+ *   member_slots: HOST array of n >= 1 distinct slots that hold adapters (not
+ *   chains); their pages together must fit one slot (sum of ceil(r_m / 8)
+ *   pages <= ceil(max_rank / 8)). chain_slot must be empty.
+ * Host-blocking; like a load, it waits for the calls already enqueued. While
+ * a chain lists an adapter, unloading that adapter fails with IN_USE.
+ * Errors: ARG (null list, n < 1, a repeated member, a member that is itself a
+ * chain or the chain slot), SLOT_RANGE, SLOT_OCCUPIED (chain_slot), SLOT_EMPTY
+ * (a member), RANK (the pages do not fit), CUDA.
+ */
+lora_status lora_define_chain(lora_pool_t pool, int chain_slot, const int *member_slots, int n);
 
 /*
  * The hot path. For every token t: Y[t] = X[t] W_base^T + s_i (X[t] A_i) B_i
