@@ -37,7 +37,10 @@ EXPORTS = (
     "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
+    "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
+    "lora_cache_stats",
 )
+CACHE_STATS_FIELDS = ("registered", "resident", "hits", "misses", "evictions")
 LORA_MAX_GROUP = 8
 LORA_KERNEL_SLOTS = 4
 KERNEL_SLOT_NAMES = ("segment_build", "shrink", "base_gemm", "finish_expand")
@@ -86,6 +89,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_base_linear_noalloc": [vp, vp, i32, i32, i32, vp, vp],
         "lora_linear_grouped": [i32, vp, vp, vp, vp, i32, vp, vp],
         "lora_define_chain": [vp, i32, vp, i32],
+        "lora_host_register": [vp, ctypes.c_int64, vp, vp, i32, f32],
+        "lora_host_unregister": [vp, ctypes.c_int64],
+        "lora_acquire": [vp, ctypes.c_int64, vp, ctypes.POINTER(i32)],
+        "lora_prefetch": [vp, ctypes.c_int64],
+        "lora_release": [vp, i32],
+        "lora_cache_stats": [vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -261,6 +270,32 @@ class LoraPool:
 
     def unload_adapter(self, slot: int):
         _check(lora_unload_adapter(self.handle, slot), "lora_unload_adapter")
+
+    # ---- host tier
+    def host_register(self, key: int, A, B, rank: int, alpha: float):
+        _check(load_library().lora_host_register(self.handle, key, _ptr(A), _ptr(B), rank,
+                                                 float(alpha)), "lora_host_register")
+
+    def host_unregister(self, key: int):
+        _check(load_library().lora_host_unregister(self.handle, key), "lora_host_unregister")
+
+    def acquire(self, key: int, stream=None) -> int:
+        slot = ctypes.c_int(-1)
+        _check(load_library().lora_acquire(self.handle, key, _stream(stream), ctypes.byref(slot)),
+               "lora_acquire")
+        return slot.value
+
+    def prefetch(self, key: int):
+        _check(load_library().lora_prefetch(self.handle, key), "lora_prefetch")
+
+    def release(self, slot: int):
+        _check(load_library().lora_release(self.handle, slot), "lora_release")
+
+    def cache_stats(self) -> Dict[str, int]:
+        import numpy as np
+        out = np.zeros(len(CACHE_STATS_FIELDS), np.int64)
+        _check(load_library().lora_cache_stats(self.handle, out.ctypes.data), "lora_cache_stats")
+        return dict(zip(CACHE_STATS_FIELDS, (int(v) for v in out)))
 
     def define_chain(self, chain_slot: int, member_slots):
         _check(lora_define_chain(self.handle, chain_slot, list(member_slots)), "lora_define_chain")

@@ -19,68 +19,11 @@
 
 #include "../../include/lora_linear.h"
 #include "device_common.cuh"
+#include "pool_state.h"
 
 using namespace lora;
 
-struct TmapEntry {
-    const void *base = nullptr;
-    uint64_t inner = 0, rows = 0;
-    uint32_t box_inner = 0, box_rows = 0;
-    CUtensorMap map;
-};
-
-struct lora_pool {
-    int device = 0, num_sms = 0;
-    int max_adapters = 0, max_rank = 0, d_in = 0, d_out = 0;
-    int max_pages = 0;   // pages per adapter at max_rank
-    int num_pages = 0;   // arena pages, page 0 = zero page
-    int slot_stride = 0;
-    int ldv = 0;         // fp32 row stride of the decode path's low-rank intermediate
-    int ldh = 0;         // bf16 row stride of the prefill path's hi/lo intermediate
-    uint16_t *A_pages = nullptr, *B_pages = nullptr;
-    int32_t *d_slots = nullptr;
-    std::vector<int32_t> h_slots;
-    std::vector<int32_t> free_pages;  // stack; back() is taken first
-    std::vector<int32_t> chain_refs;  // per slot: chains that list it as a member
-    std::map<int, std::vector<int>> chain_members;  // chain slot -> member slots
-    int *d_err = nullptr;
-    uint16_t *stage_A = nullptr, *stage_B = nullptr;
-    int32_t *d_page_list = nullptr;
-    cudaStream_t copy_stream = nullptr;
-    CUtensorMap tmA;  // A arena [num_pages*8 rows x d_in], box 8 x 64
-
-    // per-call scratch, sized for cap_T tokens
-    int cap_T = 0;
-    int32_t *order = nullptr, *hdr = nullptr, *seg_start = nullptr, *seg_slot = nullptr,
-            *seg_ublk = nullptr, *tile_info = nullptr;
-    float *V = nullptr;
-    uint16_t *Vhl = nullptr;
-    float *partials = nullptr;
-    size_t partials_floats = 0;
-    // device staging of lora_linear_host
-    int cap_host_T = 0;
-    uint16_t *hx = nullptr, *hy = nullptr;
-    int32_t *hids = nullptr;
-
-    TmapEntry tmaps[6];
-    int tmap_next = 0;
-
-    int path = LORA_PATH_AUTO;
-    bool timing = false;
-    cudaEvent_t ev[LORA_KERNEL_SLOTS + 1] = {};
-    bool ev_used[LORA_KERNEL_SLOTS] = {};
-    int ev_last = 0;  // index of the last event the last timed call recorded
-    int64_t n_loads = 0, n_unloads = 0, n_calls = 0;
-    size_t bytes_held = 0;
-};
-
-namespace {
-
-#define CUDA_TRY(expr)                                  \
-    do {                                                \
-        cudaError_t e_ = (expr);                        \
-        if (e_ != cudaSuccess) return LORA_ERR_CUDA;    \
-    } while (0)
+namespace lora {
 
 lora_status alloc_dev(lora_pool *p, void **ptr, size_t bytes)
 {
@@ -115,6 +58,10 @@ PoolDev pool_view(const lora_pool *p)
     v.d_out = p->d_out;
     return v;
 }
+
+}  // namespace lora
+
+namespace {
 
 size_t seg_entries(const lora_pool *p, int T) { return (size_t)std::min(T, p->max_adapters) + 1; }
 
@@ -356,7 +303,7 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (!mark(2)) return LORA_ERR_CUDA;
     }
     p->n_calls += 1;
-    return LORA_OK;
+    return note_call(p, stream);
 }
 
 }  // namespace
@@ -454,6 +401,7 @@ lora_status lora_pool_destroy(lora_pool_t p)
 {
     if (!p) return LORA_ERR_ARG;
     cudaDeviceSynchronize();
+    destroy_host_tier(p);
     free_scratch(p);
     free_dev(p, p->hx, (size_t)p->cap_host_T * p->d_in * 2);
     free_dev(p, p->hy, (size_t)p->cap_host_T * p->d_out * 2);
@@ -533,6 +481,7 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
     int32_t *row = &p->h_slots[(size_t)slot * p->slot_stride];
     if (row[SLOT_RANK] == 0) return LORA_ERR_SLOT_EMPTY;
     if (p->chain_refs[slot] > 0) return LORA_ERR_IN_USE;  // a chain still lists it
+    if (slot_is_held(p, slot)) return LORA_ERR_IN_USE;    // acquired from the host tier
     CUDA_TRY(cudaDeviceSynchronize());
     std::vector<int32_t> zero(p->slot_stride, 0);
     if (cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, zero.data(),
@@ -549,6 +498,7 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
         for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
     }
     std::fill(row, row + p->slot_stride, 0);
+    forget_cached_slot(p, slot);
     p->n_unloads += 1;
     return LORA_OK;
 }
@@ -642,7 +592,11 @@ lora_status lora_linear_grouped(int n, const lora_pool_t *pools, const void *con
     if (!marks.begin()) return LORA_ERR_CUDA;
     lora_status st = run_decode(pools, n, X, W_base, token_adapter_ids, T, Y, s, true, marks);
     if (st != LORA_OK) return st;
-    for (int m = 0; m < n; ++m) pools[m]->n_calls += 1;
+    for (int m = 0; m < n; ++m) {
+        pools[m]->n_calls += 1;
+        st = note_call(pools[m], s);
+        if (st != LORA_OK) return st;
+    }
     return LORA_OK;
 }
 

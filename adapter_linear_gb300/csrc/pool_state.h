@@ -1,0 +1,115 @@
+// pool_state.h -- the host-side state of a lora_pool (private to the library):
+// the paged arenas, the slot table and its host mirror, per-call scratch, the
+// measurement hook and the host-tier adapter cache. pool.cu implements the pool
+// and the layer calls, cache.cu the host tier.
+#pragma once
+
+#include <climits>
+#include <map>
+#include <unordered_map>
+#include <vector>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/lora_linear.h"
+#include "internal.h"
+
+#define CUDA_TRY(expr)                                  \
+    do {                                                \
+        cudaError_t e_ = (expr);                        \
+        if (e_ != cudaSuccess) return LORA_ERR_CUDA;    \
+    } while (0)
+
+struct TmapEntry {
+    const void *base = nullptr;
+    uint64_t inner = 0, rows = 0;
+    uint32_t box_inner = 0, box_rows = 0;
+    CUtensorMap map;
+};
+
+// One adapter of the host tier: pool-owned pinned copies of A and B.
+struct HostAdapter {
+    void *A = nullptr, *B = nullptr;  // pinned, the lora_load_adapter layouts
+    int rank = 0;
+    float alpha = 0.f;
+    int slot = -1;                    // the GPU slot it occupies, or -1
+};
+
+constexpr int64_t kNoKey = INT64_MIN;
+
+struct lora_pool {
+    int device = 0, num_sms = 0;
+    int max_adapters = 0, max_rank = 0, d_in = 0, d_out = 0;
+    int max_pages = 0;   // pages per adapter at max_rank
+    int num_pages = 0;   // arena pages, page 0 = zero page
+    int slot_stride = 0;
+    int ldv = 0;         // fp32 row stride of the decode path's low-rank intermediate
+    int ldh = 0;         // bf16 row stride of the prefill path's hi/lo intermediate
+    uint16_t *A_pages = nullptr, *B_pages = nullptr;
+    int32_t *d_slots = nullptr;
+    std::vector<int32_t> h_slots;
+    std::vector<int32_t> free_pages;  // stack; back() is taken first
+    std::vector<int32_t> chain_refs;  // per slot: chains that list it as a member
+    std::map<int, std::vector<int>> chain_members;  // chain slot -> member slots
+    int *d_err = nullptr;
+    uint16_t *stage_A = nullptr, *stage_B = nullptr;
+    int32_t *d_page_list = nullptr;
+    cudaStream_t copy_stream = nullptr;
+    CUtensorMap tmA;  // A arena [num_pages*8 rows x d_in], box 8 x 64
+
+    // per-call scratch, sized for cap_T tokens
+    int cap_T = 0;
+    int32_t *order = nullptr, *hdr = nullptr, *seg_start = nullptr, *seg_slot = nullptr,
+            *seg_ublk = nullptr, *tile_info = nullptr;
+    float *V = nullptr;
+    uint16_t *Vhl = nullptr;
+    float *partials = nullptr;
+    size_t partials_floats = 0;
+    // device staging of lora_linear_host
+    int cap_host_T = 0;
+    uint16_t *hx = nullptr, *hy = nullptr;
+    int32_t *hids = nullptr;
+
+    TmapEntry tmaps[6];
+    int tmap_next = 0;
+
+    int path = LORA_PATH_AUTO;
+    bool timing = false;
+    cudaEvent_t ev[LORA_KERNEL_SLOTS + 1] = {};
+    bool ev_used[LORA_KERNEL_SLOTS] = {};
+    int ev_last = 0;  // index of the last event the last timed call recorded
+    int64_t n_loads = 0, n_unloads = 0, n_calls = 0;
+    size_t bytes_held = 0;
+
+    // marks each layer call enqueued directly on a stream (not inside a graph
+    // capture) for the copy stream to wait on: asynchronous swap-ins start after it
+    cudaEvent_t ev_call = nullptr;
+
+    // host tier (cache.cu): key -> host copy; per slot the cached key it holds
+    // (kNoKey: a manual or empty slot), acquisitions outstanding, last use, and
+    // the swap-in that last wrote it (its pinned staging row is reused only after
+    // that copy has run)
+    std::unordered_map<int64_t, HostAdapter> host_tier;
+    std::vector<int64_t> slot_key;
+    std::vector<int32_t> slot_pins;
+    std::vector<uint64_t> slot_tick;
+    std::vector<cudaEvent_t> slot_copy_ev;
+    int32_t *stage_rows = nullptr;  // pinned [max_adapters][slot_stride + max_pages]
+    cudaEvent_t ev_copy = nullptr;  // the last swap-in enqueued on copy_stream
+    uint64_t tick = 0;
+    int64_t cache_hits = 0, cache_misses = 0, cache_evictions = 0;
+};
+
+namespace lora {
+lora_status alloc_dev(lora_pool *p, void **ptr, size_t bytes);
+void free_dev(lora_pool *p, void *ptr, size_t bytes);
+PoolDev pool_view(const lora_pool *p);
+// After a layer call on `stream`: remember it for the swap-ins of the host tier.
+lora_status note_call(lora_pool *p, cudaStream_t stream);
+// Free the host tier's pinned memory and events (pool destruction).
+void destroy_host_tier(lora_pool *p);
+// A slot the host tier holds for an outstanding acquisition?
+bool slot_is_held(const lora_pool *p, int slot);
+// A cached slot emptied through lora_unload_adapter: drop it from the tier.
+void forget_cached_slot(lora_pool *p, int slot);
+}  // namespace lora

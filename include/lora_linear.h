@@ -137,9 +137,10 @@ lora_status lora_load_adapter(lora_pool_t pool, int slot, const void *A, const v
 
 /* Unload ("unload_adapter", same sections): waits for enqueued calls, returns
  * the slot's pages to the free list and marks it empty. Host-blocking.
- * Unloading a chain slot releases its members and frees no pages.
- * Errors: SLOT_RANGE, SLOT_EMPTY, IN_USE (a chain still lists the adapter:
- * unload the chain first). */
+ * Unloading a chain slot releases its members and frees no pages; unloading a
+ * slot the host tier filled drops it from the cache (the key stays registered).
+ * Errors: SLOT_RANGE, SLOT_EMPTY, IN_USE (a chain still lists the adapter, or
+ * it is acquired from the host tier). */
 lora_status lora_unload_adapter(lora_pool_t pool, int slot);
 
 /*
@@ -190,6 +191,55 @@ lora_status lora_define_chain(lora_pool_t pool, int chain_slot, const int *membe
 lora_status lora_linear(lora_pool_t pool, const void *X, const void *W_base,
                         const int32_t *token_adapter_ids, int T, void *Y,
                         lora_stream_t stream);
+
+/*
+ * Host tier. More adapters than the pool's slots can be registered under
+ * 64-bit keys; the pool keeps pinned host copies and caches the active ones on
+ * the GPU, swapping the least recently used one out when a missing adapter is
+ * needed (icman.com.cn Multi-LoRA article, sections 2.1-2.2: adapters kept in
+ * host memory, the active ones cached on the GPU, LRU swap-out; the vLLM
+ * tutorial's "max-loras vs max-cpu-loras": a GPU set backed by a CPU set).
+ * A swap-in is asynchronous: it is enqueued on the pool's copy stream after
+ * every layer call already enqueued on the pool (on any stream) and never
+ * blocks the host, and the acquiring stream waits for it (the same article's section 4.2: cold loads
+ * must not stall the requests already running). The tier takes empty slots
+ * (from the highest index down) and evicts only slots it filled itself with
+ * no acquisition outstanding and no chain listing them; manually loaded slots
+ * are never evicted. Calls captured into a CUDA graph are not ordered against
+ * swap-ins: acquire before capturing, and keep the slots acquired while the
+ * graph replays.
+ */
+
+/* Register an adapter in the host tier: A, B (host or device pointers, the
+ * lora_load_adapter layouts) are copied into pool-owned pinned memory.
+ * Host-blocking. Errors: ARG (null pointers, key INT64_MIN), RANK,
+ * SLOT_OCCUPIED (the key is taken), OOM, CUDA. */
+lora_status lora_host_register(lora_pool_t pool, int64_t key, const void *A, const void *B,
+                               int rank, float alpha);
+
+/* Remove a key from the host tier (evicting it from the GPU if resident).
+ * Errors: ARG (unknown key), IN_USE (acquired, or listed by a chain), CUDA. */
+lora_status lora_host_unregister(lora_pool_t pool, int64_t key);
+
+/* Make `key` resident and hold it: *slot_out receives its slot id for
+ * token_adapter_ids. On a miss the least recently used unheld cached adapter
+ * may be evicted and the swap-in is enqueued; `stream` is made to wait for the
+ * copy, so layer calls enqueued on it afterwards see the adapter. Each acquire
+ * needs a lora_release. Errors: ARG (unknown key, null slot_out), OOM (every
+ * slot or page is held), CUDA. */
+lora_status lora_acquire(lora_pool_t pool, int64_t key, lora_stream_t stream, int *slot_out);
+
+/* Start the swap-in of `key` without holding it (a hot adapter named ahead of
+ * its requests); a later lora_acquire then hits. Errors: as lora_acquire. */
+lora_status lora_prefetch(lora_pool_t pool, int64_t key);
+
+/* Drop one hold on a slot returned by lora_acquire. The adapter stays cached
+ * until it is evicted. Errors: SLOT_RANGE, ARG (not a held cached slot). */
+lora_status lora_release(lora_pool_t pool, int slot);
+
+/* out[5]: registered keys, resident cached adapters, hits, misses, evictions. */
+#define LORA_CACHE_STATS_COUNT 5
+lora_status lora_cache_stats(lora_pool_t pool, int64_t *out);
 
 /*
  * Several LoRA linear layers that share one batch of token ids, in one launch
