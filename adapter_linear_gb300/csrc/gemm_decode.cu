@@ -10,7 +10,8 @@
 //      (T rounded up to 16; rows past T read as zero from TMA);
 //    * stream-K: the problems' (tile, 128-wide k-block) units, concatenated in
 //      problem order, are cut into G equal contiguous ranges, one per CTA
-//      (G = number of SMs, or fewer for small problems), so every SM streams
+//      (G = number of SMs, or fewer for small problems; small layers launch
+//      extra CTAs that only take shrink pairs), so every SM streams
 //      the same share of all the weights of the group. Every tile a range
 //      touches (a "segment" of the range) gets a TMEM accumulator from a small
 //      ring and is written out as an fp32 partial sum [cta][segment][T][128];
@@ -164,7 +165,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
-    const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
+    // CTAs past the G stream-K ranges (launched when the shrink has more pairs than
+    // there are ranges) only run shrink pairs
+    const bool ranged = c < p.G;
+    const int u0 = ranged ? cta_start(c, p.U, p.G) : 0, u1 = ranged ? cta_start(c + 1, p.U, p.G) : 0;
     const int g0 = unit_tile(p, u0);  // the tile of segment 0
     const int nseg = u1 > u0 ? unit_tile(p, u1 - 1) - g0 + 1 : 0;
 
@@ -295,7 +299,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
         if (ids != nullptr) {
             int m = 0;
-            for (int u = c; u < p.pairs; u += p.G) {
+            for (int u = c; u < p.pairs; u += (int)gridDim.x) {
                 while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
                 const DecodeProblem &pr = p.prob[pick<NP>(m)];
                 const int lp = u - pr.pair_begin;
@@ -529,6 +533,9 @@ bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max
     if (U * G >= (1ll << 31) || pairs >= (1ll << 31) || cols >= (1ll << 31)) return false;
     p.U = (int)U;
     p.G = (int)G;
+    // more CTAs than ranges when the shrink pairs outnumber them (small layers)
+    p.grid = p.G;
+    if (pairs > p.grid) p.grid = (int)(pairs < max_G ? pairs : max_G);
     p.pairs = (int)pairs;
     p.col_blocks = (int)cols;
     int max_seg = 1;
@@ -566,6 +573,7 @@ DecodePlanT<NP> narrow_plan(const DecodePlan &p)
     q.ntok = p.ntok;
     q.U = p.U;
     q.G = p.G;
+    q.grid = p.grid;
     q.max_seg = p.max_seg;
     q.n_acc = p.n_acc;
     q.stages = p.stages;
@@ -588,7 +596,7 @@ cudaError_t launch_gemm_decode_n(const DecodeMaps &maps, const DecodePlan &plan,
         m.W[i] = maps.W[i];
         m.X[i] = maps.X[i];
     }
-    return launch_pdl(gemm_decode_kernel<NP>, dim3(plan.G), dim3(kThreads), plan.smem_bytes, stream, m,
+    return launch_pdl(gemm_decode_kernel<NP>, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, m,
                       narrow_plan<NP>(plan), ids, partials, err);
 }
 

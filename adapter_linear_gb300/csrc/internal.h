@@ -109,6 +109,7 @@ struct DecodePlanT {
     static constexpr int kNP = NP;
     int n, T, ntok;
     int U, G;               // units, CTAs (stream-K ranges)
+    int grid;               // CTAs launched (>= G: the rest only run shrink pairs)
     int max_seg;            // most tiles one range touches (partials per CTA)
     int n_acc;              // TMEM accumulators in the ring
     int stages;

@@ -224,10 +224,11 @@ def source_digest(path=GEMM_SRC) -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the base GEMM from the committed ncu summary, if it was
-    taken on the current kernel source (else None)."""
-    if not os.path.exists(PROFILE):
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch of the decode GEMM from the committed ncu summary, if it was
+    taken on this workload (the default q_proj decode) with the current kernel source
+    (else None)."""
+    if workload_name != "q_proj_decode" or not os.path.exists(PROFILE):
         return None
     text = open(PROFILE).read()
     m_src = re.search(r"source_digest:\s*([0-9a-f]+)", text)
@@ -707,7 +708,7 @@ def main():
         achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9
         roof = {"kernel": "gemm_decode_kernel", "bound": "hbm", "achieved": achieved,
                 "peak": hbm_peak, "unit": "GB/s", "frac": achieved / hbm_peak,
-                "traffic": profiled_traffic(), "algorithmic_bytes": gemm_bytes,
+                "traffic": profiled_traffic(args.workload), "algorithmic_bytes": gemm_bytes,
                 "peak_source": peak_src}
     else:
         gemm_flops = 2.0 * p.T * p.d_in * p.d_out
