@@ -138,8 +138,13 @@ struct UnitCursor {
     }
 };
 
+// At most 96 registers a thread: the register file is split among an SM's four
+// sub-partitions (16384 each) and a CTA's warps are dealt to them in turn, so the
+// six GEMM warps put two warps (2 x 96 x 32 registers) on two sub-partitions; two
+// finishing CTAs (one warp per sub-partition each, <= 152 registers a thread) then
+// still fit beside them (see finish_decode_kernel).
 template <int NP>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(96)
     gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
                        const __grid_constant__ DecodePlanT<NP> p, const int32_t *__restrict__ ids,
                        float *__restrict__ partials, int *err)
@@ -357,11 +362,13 @@ __device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *
 }
 
 // LORA = false: the base-only variant (no adapter state, few registers).
-// At most 168 registers a thread (the bound for 3 CTAs): two finishing CTAs then
-// fit on an SM beside the GEMM CTA (192 threads x 112 registers) and have their
-// B words in registers when the GEMM ends.
+// At most 152 registers a thread: two finishing CTAs then fit on an SM beside the
+// GEMM CTA (per sub-partition 2 x 96 x 32 + 2 x 152 x 32 <= 16384 registers), so
+// all of them are resident with their B words in registers when the GEMM ends
+// (measured: with one CTA per SM, 104 of q_proj's 256 finishing CTAs and then a
+// quarter of the next call's GEMM CTAs started only as GEMM CTAs left).
 template <int NP, bool LORA>
-__global__ void __launch_bounds__(kFinishThreads, 3)
+__global__ void __maxnreg__(152)
     finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
                          const int32_t *__restrict__ ids)
 {
