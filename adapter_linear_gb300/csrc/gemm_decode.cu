@@ -138,16 +138,10 @@ struct UnitCursor {
     }
 };
 
-// At most 96 registers a thread: the register file is split among an SM's four
-// sub-partitions (16384 each) and a CTA's warps are dealt to them in turn, so the
-// six GEMM warps put two warps (2 x 96 x 32 registers) on two sub-partitions; two
-// finishing CTAs (one warp per sub-partition each, <= 152 registers a thread) then
-// still fit beside them (see finish_decode_kernel).
 template <int NP>
-__global__ void __maxnreg__(96)
-    gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
-                       const __grid_constant__ DecodePlanT<NP> p, const int32_t *__restrict__ ids,
-                       float *__restrict__ partials, int *err)
+__device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, const DecodePlanT<NP> &p,
+                                                 const int32_t *__restrict__ ids,
+                                                 float *__restrict__ partials, int *err)
 {
     extern __shared__ uint8_t dec_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -361,16 +355,11 @@ __device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *
     for (int c = 0; c < kFinishCols; ++c) acc[c] = dot8_f32_bf16(v, b[c], acc[c]);
 }
 
-// LORA = false: the base-only variant (no adapter state, few registers).
-// At most 152 registers a thread: two finishing CTAs then fit on an SM beside the
-// GEMM CTA (per sub-partition 2 x 96 x 32 + 2 x 152 x 32 <= 16384 registers), so
-// all of them are resident with their B words in registers when the GEMM ends
-// (measured: with one CTA per SM, 104 of q_proj's 256 finishing CTAs and then a
-// quarter of the next call's GEMM CTAs started only as GEMM CTAs left).
+// LORA = false: the base-only pass (no adapter state, few registers).
 template <int NP, bool LORA>
-__global__ void __maxnreg__(152)
-    finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
-                         const int32_t *__restrict__ ids)
+__device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
+                                                   const float *__restrict__ partials,
+                                                   const int32_t *__restrict__ ids)
 {
     // The next call's GEMM may launch now: its CTAs take an SM as soon as this call's
     // GEMM CTA leaves it and stream their first W tiles; everything they write comes
@@ -483,6 +472,54 @@ __global__ void __maxnreg__(152)
     *reinterpret_cast<uint4 *>(pr.Y + (size_t)t * pool.d_out + n0) = o;
 }
 
+// Register budgets. The register file is split among an SM's four sub-partitions
+// (16384 registers each) and a CTA's warps are dealt to them in turn, so the six
+// GEMM warps put two warps on two sub-partitions. When the adapter finishing pass
+// has more CTAs than there are SMs, two of its CTAs (one warp per sub-partition
+// each) must fit beside a GEMM CTA to be resident, with their B words loaded,
+// when the GEMM ends: 2 x 96 x 32 + 2 x 152 x 32 <= 16384. Measured on q_proj
+// (T = 64, 256 finishing CTAs): without the bounds only 152 were resident, the
+// other 104 and then a quarter of the next call's GEMM CTAs started only as GEMM
+// CTAs left (15.7 vs 17.2 us a step). The bounds cost registers the shrink and the
+// partial loads use, so they are taken only where they pay: the finishing grid
+// exceeds the SMs and a CTA's shrink pairs read at most half as many bytes as its
+// share of W (the "tight" plans; measured faster for q_proj T = 64, gate_proj
+// T = 32 and the grouped 7-module layer; slower for T = 32 layers whose finishing
+// grid fits the SMs and for T = 256 with ~4 shrink pairs per CTA).
+template <int NP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
+                       const __grid_constant__ DecodePlanT<NP> p, const int32_t *__restrict__ ids,
+                       float *__restrict__ partials, int *err)
+{
+    gemm_decode_body<NP>(maps, p, ids, partials, err);
+}
+
+template <int NP>
+__global__ void __maxnreg__(96)
+    gemm_decode_kernel_tight(const __grid_constant__ DecodeMapsT<NP> maps,
+                             const __grid_constant__ DecodePlanT<NP> p,
+                             const int32_t *__restrict__ ids, float *__restrict__ partials, int *err)
+{
+    gemm_decode_body<NP>(maps, p, ids, partials, err);
+}
+
+template <int NP, bool LORA>
+__global__ void __launch_bounds__(kFinishThreads)
+    finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
+                         const int32_t *__restrict__ ids)
+{
+    finish_decode_body<NP, LORA>(p, partials, ids);
+}
+
+template <int NP>
+__global__ void __maxnreg__(152)
+    finish_decode_kernel_tight(const __grid_constant__ DecodePlanT<NP> p,
+                               const float *__restrict__ partials, const int32_t *__restrict__ ids)
+{
+    finish_decode_body<NP, true>(p, partials, ids);
+}
+
 uint32_t pow2_cols(uint32_t n)
 {
     uint32_t c = 32;
@@ -545,6 +582,13 @@ bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max
     if (pairs > p.grid) p.grid = (int)(pairs < max_G ? pairs : max_G);
     p.pairs = (int)pairs;
     p.col_blocks = (int)cols;
+    // bounded registers where the finishing grid exceeds the SMs and each CTA's
+    // shrink work (A bytes of its pairs) stays well under its share of the W stream
+    int max_d_in = 0;
+    for (int m = 0; m < n; ++m) max_d_in = d_in[m] > max_d_in ? d_in[m] : max_d_in;
+    const double shrink_bytes = (double)((pairs + p.grid - 1) / p.grid) * 2.0 * kRankPage * max_d_in;
+    const double stream_bytes = (double)U / (double)G * kBoxes * kWTileBytes;
+    p.tight = pairs > 0 && cols * T > max_G && 2.0 * shrink_bytes <= stream_bytes;
     int max_seg = 1;
     for (int c = 0; c < p.G; ++c) {
         const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
@@ -586,6 +630,7 @@ DecodePlanT<NP> narrow_plan(const DecodePlan &p)
     q.stages = p.stages;
     q.pairs = p.pairs;
     q.col_blocks = p.col_blocks;
+    q.tight = p.tight;
     q.tmem_cols = p.tmem_cols;
     q.smem_bytes = p.smem_bytes;
     for (int m = 0; m < NP; ++m) q.prob[m] = p.prob[m];
@@ -596,25 +641,29 @@ template <int NP>
 cudaError_t launch_gemm_decode_n(const DecodeMaps &maps, const DecodePlan &plan, const int32_t *ids,
                                  float *partials, int *err, cudaStream_t stream)
 {
-    cudaError_t e = ensure_smem_attr((const void *)gemm_decode_kernel<NP>, plan.smem_bytes);
+    auto kernel = plan.tight ? gemm_decode_kernel_tight<NP> : gemm_decode_kernel<NP>;
+    cudaError_t e = ensure_smem_attr((const void *)kernel, plan.smem_bytes);
     if (e != cudaSuccess) return e;
     DecodeMapsT<NP> m;
     for (int i = 0; i < NP; ++i) {
         m.W[i] = maps.W[i];
         m.X[i] = maps.X[i];
     }
-    return launch_pdl(gemm_decode_kernel<NP>, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, m,
+    return launch_pdl(kernel, dim3(plan.grid), dim3(kThreads), plan.smem_bytes, stream, m,
                       narrow_plan<NP>(plan), ids, partials, err);
 }
 
-template <int NP, bool LORA>
+template <int NP>
 cudaError_t launch_finish_decode_n(const DecodePlan &plan, const float *partials, const int32_t *ids,
                                    cudaStream_t stream)
 {
-    cudaError_t e = ensure_smem_attr((const void *)finish_decode_kernel<NP, LORA>, 0);
+    auto kernel = ids == nullptr ? finish_decode_kernel<NP, false>
+                                 : (plan.tight ? finish_decode_kernel_tight<NP>
+                                               : finish_decode_kernel<NP, true>);
+    cudaError_t e = ensure_smem_attr((const void *)kernel, 0);
     if (e != cudaSuccess) return e;
-    return launch_pdl(finish_decode_kernel<NP, LORA>, dim3(plan.col_blocks, plan.T),
-                      dim3(kFinishThreads), 0, stream, narrow_plan<NP>(plan), partials, ids);
+    return launch_pdl(kernel, dim3(plan.col_blocks, plan.T), dim3(kFinishThreads), 0, stream,
+                      narrow_plan<NP>(plan), partials, ids);
 }
 
 }  // namespace
@@ -629,12 +678,8 @@ cudaError_t launch_gemm_decode(const DecodeMaps &maps, const DecodePlan &plan, c
 cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, const int32_t *ids,
                                  cudaStream_t stream)
 {
-    if (ids == nullptr) {
-        if (plan.n == 1) return launch_finish_decode_n<1, false>(plan, partials, ids, stream);
-        return launch_finish_decode_n<kMaxGroup, false>(plan, partials, ids, stream);
-    }
-    if (plan.n == 1) return launch_finish_decode_n<1, true>(plan, partials, ids, stream);
-    return launch_finish_decode_n<kMaxGroup, true>(plan, partials, ids, stream);
+    if (plan.n == 1) return launch_finish_decode_n<1>(plan, partials, ids, stream);
+    return launch_finish_decode_n<kMaxGroup>(plan, partials, ids, stream);
 }
 
 }  // namespace lora

@@ -115,6 +115,7 @@ struct DecodePlanT {
     int stages;
     int pairs;              // shrink pairs of all problems
     int col_blocks;         // finishing grid.x
+    bool tight;             // register-bounded kernel variants (see gemm_decode.cu)
     uint32_t tmem_cols;
     size_t smem_bytes;
     DecodeProblem prob[NP];
