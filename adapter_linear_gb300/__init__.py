@@ -38,7 +38,7 @@ EXPORTS = (
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
-    "lora_cache_stats",
+    "lora_cache_stats", "lora_pool_selftest_wait",
 )
 CACHE_STATS_FIELDS = ("registered", "resident", "hits", "misses", "evictions")
 LORA_MAX_GROUP = 8
@@ -95,6 +95,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_prefetch": [vp, ctypes.c_int64],
         "lora_release": [vp, i32],
         "lora_cache_stats": [vp, vp],
+        "lora_pool_selftest_wait": [vp, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -335,6 +336,10 @@ class LoraPool:
             Y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=X.device)
         _check(lora_base_linear(self.handle, X, W, T, Y, stream), "lora_base_linear")
         return Y
+
+    def selftest_wait(self, limit_us: int, stream=None):
+        _check(load_library().lora_pool_selftest_wait(self.handle, limit_us, _stream(stream)),
+               "lora_pool_selftest_wait")
 
     def check_errors(self) -> int:
         return lora_pool_check_errors(self.handle)

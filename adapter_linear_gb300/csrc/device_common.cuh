@@ -123,11 +123,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
-// Wait for the phase with `parity` to complete, for at most kWaitTimeoutNs.
+// Wait for the phase with `parity` to complete, for at most limit_ns.
 // Returns false (after raising the CTA's abort flag and the pool's timeout
 // bit) if it runs out, or if another role of the CTA has already aborted.
 static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                       int *err)
+                                       int *err, uint64_t limit_ns = kWaitTimeoutNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t start = global_timer_ns();
@@ -135,7 +135,7 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, vo
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0) {
             if (*abort_flag) return false;
-            if (global_timer_ns() - start > kWaitTimeoutNs) {
+            if (global_timer_ns() - start > limit_ns) {
                 *abort_flag = 1;
                 atomicOr(err, kErrTimeoutBit);
                 return false;

@@ -180,6 +180,22 @@ __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16
 
 bool dims_ok(int d) { return d > 0 && d <= LORA_MAX_DIM && d % 8 == 0; }
 
+// One bounded wait on an mbarrier that nothing arrives on: the kernels' wait
+// runs out after limit_ns, raises the timeout bit and returns (no trap, no hang).
+__global__ void wait_selftest_kernel(int *err, uint64_t limit_ns)
+{
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, &abort_flag, err, limit_ns);
+    __syncthreads();
+}
+
 // Split-K partials of a grouped decode call (held by its first pool): grown on
 // first use of a larger group, like the rest of the scratch.
 lora_status ensure_partials(lora_pool *p, size_t floats)
@@ -627,6 +643,14 @@ lora_status lora_linear_host(lora_pool_t p, const void *X_host, const void *W_ba
     if (st != LORA_OK) return st;
     CUDA_TRY(cudaMemcpyAsync(Y_host, p->hy, (size_t)T * p->d_out * 2, cudaMemcpyDeviceToHost, s));
     CUDA_TRY(cudaStreamSynchronize(s));
+    return LORA_OK;
+}
+
+lora_status lora_pool_selftest_wait(lora_pool_t p, int limit_us, lora_stream_t stream)
+{
+    if (!p || limit_us < 1 || limit_us > 2000000) return LORA_ERR_ARG;
+    wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(p->d_err, (uint64_t)limit_us * 1000ull);
+    CUDA_TRY(cudaGetLastError());
     return LORA_OK;
 }
 

@@ -329,6 +329,17 @@ lora_status lora_base_linear_noalloc(const void *X, const void *W_base, int T, i
 lora_status lora_pool_check_errors(lora_pool_t pool);
 
 /*
+ * Test hook for the kernels' bounded waits (no counterpart in the pages): runs
+ * one wait, with the same code the kernels use, on an mbarrier that nothing
+ * completes. It gives up after limit_us microseconds (1..2,000,000), sets the
+ * pool's timeout bit and returns; the next lora_pool_check_errors reports
+ * LORA_ERR_TIMEOUT and the context stays usable. Every mbarrier wait in the
+ * kernels is bounded this way (2 s): a lost arrival ends as an error status,
+ * never as a hang. Asynchronous on `stream`. Errors: ARG, CUDA.
+ */
+lora_status lora_pool_selftest_wait(lora_pool_t pool, int limit_us, lora_stream_t stream);
+
+/*
  * Test hook: run only the segment builder on device ids[T] and copy its
  * tables out (device pointers): order[T] (token indices stably sorted by id,
  * base-only tokens first), *n_base, *num_seg, seg_start[num_seg + 1] (offsets
