@@ -76,7 +76,10 @@ cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, Seg
 
 // Prefill shrink (tcgen05), 128-token units per segment: writes s_i X[t,:] A_i as
 // bf16 hi/lo pairs grouped per 32 rank columns (see shrink.cu) into Vhl [T][ldh].
-cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
+// tmA: the A arena with a box of one page (8 rows x 64); tmAw: a box of
+// round16(8 * max_pages) rows x 64 (consecutive pages in one copy).
+cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
+                             const CUtensorMap &tmAw, const uint16_t *X,
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
                              int num_sms, int *err, cudaStream_t stream);
 

@@ -309,7 +309,7 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (with_lora) {
             // rows of tokens without an adapter must read as zero in the expand
             CUDA_TRY(cudaMemsetAsync(p->Vhl, 0, sizeof(uint16_t) * (size_t)T * p->ldh, stream));
-            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
+            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
                                       p->d_err, stream));
         }
         if (!mark(1)) return LORA_ERR_CUDA;
@@ -405,6 +405,9 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
         cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
         !make_tmap_bf16_2d(&p->tmA, p->A_pages, d_in, (uint64_t)p->num_pages * kRankPage,
                            (uint64_t)d_in * 2, 64, kRankPage) ||
+        !make_tmap_bf16_2d(&p->tmAw, p->A_pages, d_in, (uint64_t)p->num_pages * kRankPage,
+                           (uint64_t)d_in * 2, 64,
+                           (uint32_t)(((p->max_pages * kRankPage + 15) / 16) * 16)) ||
         cudaDeviceSynchronize() != cudaSuccess) {
         lora_pool_destroy(p);
         return LORA_ERR_CUDA;

@@ -55,7 +55,8 @@ struct lora_pool {
     uint16_t *stage_A = nullptr, *stage_B = nullptr;
     int32_t *d_page_list = nullptr;
     cudaStream_t copy_stream = nullptr;
-    CUtensorMap tmA;  // A arena [num_pages*8 rows x d_in], box 8 x 64
+    CUtensorMap tmA;   // A arena [num_pages*8 rows x d_in], box 8 x 64
+    CUtensorMap tmAw;  // the same, box round16(8 * max_pages) x 64
 
     // per-call scratch, sized for cap_T tokens
     int cap_T = 0;

@@ -61,6 +61,7 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const 
 
 __global__ void __launch_bounds__(kTcThreads, 1)
     shrink_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmA,
+                     const __grid_constant__ CUtensorMap tmAw,
                      const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
                      uint16_t *__restrict__ Vhl, int ldh, int nmax, int stages, uint32_t tmem_cols,
                      int *err)
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (warp == 4 && lane == 0) {
         tma_prefetch_map(&tmX);
         tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmAw);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -121,7 +123,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 contiguous &= (tabs.order[ui.p0 + r] == row0 + r);
             contiguous = __all_sync(0xffffffffu, contiguous);
             const int npad = ui.n / kRankPage;
-            const uint32_t bytes = kSBoxes * ((uint32_t)npad * 1024u + (contiguous ? kXTileBytes : 0u));
+            // an even number of consecutive pages: one box of nmax rows per 64 columns
+            // (rows past the adapter are read but not used by the MMA; past the arena
+            // they read as zero) instead of one 1 KB box per page
+            bool wide = npad == ui.npages;
+            for (int q = 1; q < ui.npages && wide; ++q) wide = ui.pages[q] == ui.pages[0] + q;
+            const uint32_t a_bytes = wide ? p_bytes : (uint32_t)npad * 1024u;
+            const uint32_t bytes = kSBoxes * (a_bytes + (contiguous ? kXTileBytes : 0u));
             bool ok = true;
             for (int kb = 0; kb < KB && ok; ++kb, ++it) {
                 const int s = it % stages;
@@ -155,9 +163,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     for (int b = 0; b < kSBoxes; ++b) {
                         const int k0 = (kb * kSBoxes + b) * 64;
                         if (contiguous) tma_load_2d(xs + b * kXTileBytes, &tmX, &full[s], k0, row0);
-                        for (int q = 0; q < npad; ++q) {
-                            const int page = q < ui.npages ? ui.pages[q] : 0;
-                            tma_load_2d(ps + b * p_bytes + q * 1024, &tmA, &full[s], k0, page * kRankPage);
+                        if (wide) {
+                            tma_load_2d(ps + b * p_bytes, &tmAw, &full[s], k0, ui.pages[0] * kRankPage);
+                        } else {
+                            for (int q = 0; q < npad; ++q) {
+                                const int page = q < ui.npages ? ui.pages[q] : 0;
+                                tma_load_2d(ps + b * p_bytes + q * 1024, &tmA, &full[s], k0,
+                                            page * kRankPage);
+                            }
                         }
                     }
                 }
@@ -282,7 +295,8 @@ uint32_t pow2_cols(uint32_t n)
 
 }  // namespace
 
-cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, const uint16_t *X,
+cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
+                             const CUtensorMap &tmAw, const uint16_t *X,
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
                              int num_sms, int *err, cudaStream_t stream)
 {
@@ -299,7 +313,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA, con
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
-    shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, X, pool, tabs, Vhl, ldh, nmax,
+    shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, tmAw, X, pool, tabs, Vhl, ldh, nmax,
                                                           stages, tmem_cols, err);
     return cudaGetLastError();
 }
