@@ -23,7 +23,8 @@
 //      low-rank shrink V[t, 8q..8q+7] = s_i X[t,:] A_i[:, 8q..8q+7] for the
 //      (problem, token, page) triples dealt to this CTA round-robin (a
 //      BGMV-style per-token gather: each reads one 8 x d_in A page with 128-bit
-//      loads), so the adapter reads overlap the W stream; then they read the
+//      loads; one pair at a time on all four warps, or, when a CTA has several,
+//      one pair per warp), so the adapter reads overlap the W stream; then they read the
 //      accumulators back with tcgen05.ld (TMEM lane = output row n) and store
 //      the partials.
 // 2. finish_decode_kernel (launched with programmatic stream serialization, so
@@ -115,6 +116,37 @@ __device__ __forceinline__ void shrink_pair(int t, int page, float scale, const 
         pr.V[(size_t)t * pr.ldv + q * kRankPage + tid] = scale * s;
     }
     named_bar_sync(kBarShrink, 128);
+}
+
+// The same pair computed by one warp alone (lanes stride over d_in): when a CTA has
+// several pairs, its four epilogue warps each take one and run them in parallel.
+__device__ __forceinline__ void shrink_pair_warp(int t, int page, float scale, const DecodeProblem &pr,
+                                                 int q)
+{
+    const int lane = threadIdx.x & 31;
+    const int d_in = pr.pool.d_in;
+    const uint16_t *Ap = pr.pool.A_pages + (size_t)page * kRankPage * d_in;
+    const uint16_t *xr = pr.X + (size_t)t * d_in;
+    float acc[kRankPage];
+#pragma unroll
+    for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = 0.f;
+#pragma unroll 2
+    for (int c = lane; c < d_in / 8; c += 32) {
+        const uint4 x = ldg_nc_v4(xr + c * 8);
+        uint4 a[kRankPage];
+#pragma unroll
+        for (int jj = 0; jj < kRankPage; ++jj) a[jj] = ldg_nc_v4(Ap + (size_t)jj * d_in + c * 8);
+#pragma unroll
+        for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = dot8_bf16(x, a[jj], acc[jj]);
+    }
+    float mine = 0.f;
+#pragma unroll
+    for (int jj = 0; jj < kRankPage; ++jj) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) acc[jj] += __shfl_xor_sync(0xffffffffu, acc[jj], o);
+        if (lane == jj) mine = acc[jj];
+    }
+    if (lane < kRankPage) pr.V[(size_t)t * pr.ldv + q * kRankPage + lane] = scale * mine;
 }
 
 // The current problem's unit bookkeeping, kept in registers while a loop walks
@@ -297,8 +329,13 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         const uint32_t tmem = *tmem_slot;
         pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
         if (ids != nullptr) {
+            // this CTA's pairs: c, c + grid, c + 2 grid, ...; with more than one of them
+            // on average the four warps take every fourth pair each, else all 128
+            // threads work on one pair at a time
+            const int stride = (int)gridDim.x;
+            const bool by_warp = p.pairs > stride;
             int m = 0;
-            for (int u = c; u < p.pairs; u += (int)gridDim.x) {
+            for (int u = by_warp ? c + warp * stride : c; u < p.pairs; u += by_warp ? 4 * stride : stride) {
                 while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
                 const DecodeProblem &pr = p.prob[pick<NP>(m)];
                 const int lp = u - pr.pair_begin;
@@ -307,8 +344,11 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
                 if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
                 const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
                 if (q >= row[SLOT_NPAGES]) continue;
-                shrink_pair(t, row[SLOT_PAGES + q],
-                            __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]), pr, q, red);
+                const float scale = __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]);
+                if (by_warp)
+                    shrink_pair_warp(t, row[SLOT_PAGES + q], scale, pr, q);
+                else
+                    shrink_pair(t, row[SLOT_PAGES + q], scale, pr, q, red);
             }
         }
         for (int seg = 0; seg < nseg; ++seg) {
