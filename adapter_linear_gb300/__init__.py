@@ -38,8 +38,10 @@ EXPORTS = (
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
-    "lora_cache_stats", "lora_pool_selftest_wait",
+    "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info",
 )
+PLAN_INFO_FIELDS = ("units", "G", "grid", "max_seg", "n_acc", "stages", "tmem_cols", "smem_bytes",
+                    "pairs", "col_blocks", "tight", "ntok", "partials_floats")
 CACHE_STATS_FIELDS = ("registered", "resident", "hits", "misses", "evictions")
 LORA_MAX_GROUP = 8
 LORA_KERNEL_SLOTS = 4
@@ -96,6 +98,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_release": [vp, i32],
         "lora_cache_stats": [vp, vp],
         "lora_pool_selftest_wait": [vp, i32, vp],
+        "lora_decode_plan_info": [i32, i32, vp, vp, vp, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -162,6 +165,19 @@ def lora_linear(pool: int, X, W_base, ids, T: int, Y, stream=None) -> int:
 def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream=None) -> int:
     return load_library().lora_linear_host(pool, _ptr(X_host), _ptr(W_base), _ptr(ids_host), T,
                                            _ptr(Y_host), _stream(stream))
+
+
+def decode_plan_info(T: int, d_in, d_out, max_pages, num_sms: int = 152) -> Dict[str, int]:
+    """The decode plan for len(d_in) layers of T tokens (host only, no GPU)."""
+    import numpy as np
+    n = len(d_in)
+    a = np.ascontiguousarray(d_in, np.int32)
+    b = np.ascontiguousarray(d_out, np.int32)
+    c = np.ascontiguousarray(max_pages, np.int32)
+    out = np.zeros(len(PLAN_INFO_FIELDS), np.int64)
+    _check(load_library().lora_decode_plan_info(n, T, a.ctypes.data, b.ctypes.data, c.ctypes.data,
+                                                num_sms, out.ctypes.data), "lora_decode_plan_info")
+    return dict(zip(PLAN_INFO_FIELDS, (int(v) for v in out)))
 
 
 def lora_define_chain(pool: int, chain_slot: int, member_slots) -> int:

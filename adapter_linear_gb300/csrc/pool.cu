@@ -649,6 +649,22 @@ lora_status lora_linear_host(lora_pool_t p, const void *X_host, const void *W_ba
     return LORA_OK;
 }
 
+lora_status lora_decode_plan_info(int n, int T, const int *d_in, const int *d_out,
+                                  const int *max_pages, int num_sms, int64_t *out)
+{
+    if (!d_in || !d_out || !max_pages || !out) return LORA_ERR_ARG;
+    for (int m = 0; m < n && m < kMaxGroup; ++m)
+        if (!dims_ok(d_in[m]) || !dims_ok(d_out[m]) || max_pages[m] < 0) return LORA_ERR_SHAPE;
+    DecodePlan p;
+    if (!plan_decode(n, T, d_in, d_out, max_pages, num_sms, &p)) return LORA_ERR_ARG;
+    const int64_t v[LORA_PLAN_INFO_COUNT] = {p.U, p.G, p.grid, p.max_seg, p.n_acc, p.stages,
+                                             (int64_t)p.tmem_cols, (int64_t)p.smem_bytes, p.pairs,
+                                             p.col_blocks, p.tight ? 1 : 0, p.ntok,
+                                             (int64_t)decode_partials_floats(p)};
+    for (int i = 0; i < LORA_PLAN_INFO_COUNT; ++i) out[i] = v[i];
+    return LORA_OK;
+}
+
 lora_status lora_pool_selftest_wait(lora_pool_t p, int limit_us, lora_stream_t stream)
 {
     if (!p || limit_us < 1 || limit_us > 2000000) return LORA_ERR_ARG;

@@ -329,6 +329,22 @@ lora_status lora_base_linear_noalloc(const void *X, const void *W_base, int T, i
 lora_status lora_pool_check_errors(lora_pool_t pool);
 
 /*
+ * Test hook (host only, needs no GPU; no counterpart in the pages): the decode
+ * path's plan for n layers of T tokens -- the stream-K split and the kernels'
+ * resources -- as lora_linear / lora_linear_grouped would compute it with
+ * num_sms SMs. d_in, d_out, max_pages: HOST arrays of n entries (max_pages 0:
+ * no adapters). out[LORA_PLAN_INFO_COUNT] = {units, ranges G, CTAs launched,
+ * most tiles per range, TMEM accumulators, pipeline stages, TMEM columns,
+ * GEMM dynamic shared memory bytes, shrink pairs, finishing blocks, register-
+ * bounded variant (0/1), T rounded up to 16, split-K partial floats}.
+ * Errors: ARG (null pointers, n outside 1..LORA_MAX_GROUP, T outside 1..256,
+ * num_sms < 1), SHAPE.
+ */
+#define LORA_PLAN_INFO_COUNT 13
+lora_status lora_decode_plan_info(int n, int T, const int *d_in, const int *d_out,
+                                  const int *max_pages, int num_sms, int64_t *out);
+
+/*
  * Test hook for the kernels' bounded waits (no counterpart in the pages): runs
  * one wait, with the same code the kernels use, on an mbarrier that nothing
  * completes. It gives up after limit_us microseconds (1..2,000,000), sets the
