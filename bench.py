@@ -480,6 +480,92 @@ def run_grouped_layer(args):
         torch.distributed.destroy_process_group()
 
 
+# ------------------------------------------------- hot-swap stream (config 5 as specified)
+
+def run_hotswap_stream(args):
+    """1000 calls of 256 tokens over 2000 r16 adapters with Zipf ids (a new id vector
+    every call), with one unload + reload of a slot in every block of 20 calls (50
+    cycles), all through the public API; the same 1000 calls without the swaps give
+    the swap cost."""
+    import torch
+    import adapter_linear_gb300 as al
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    p, sched = L.hotswap()
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+
+    pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
+    for slot, ad in p.adapters.items():
+        pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
+    pool.reserve(p.T)
+    pool.set_path(al.LORA_PATH_DECODE)
+    X, W = t(p.X), t(p.W)
+    ids = t(sched.ids)                                 # [calls, T]
+    Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=dev)
+    swaps = {c: (slot, gen) for c, slot, gen in sched.swaps}
+    fresh = {}
+    for c, (slot, gen) in swaps.items():
+        ad = L.make_adapter(p.seed, slot, p.d_in, p.d_out, 16, 32.0, generation=gen)
+        fresh[c] = (t(ad.A), t(ad.B))
+    old = {c: (t(p.adapters[slot].A), t(p.adapters[slot].B)) for c, (slot, _) in swaps.items()}
+
+    def run(with_swaps, restore):
+        for c in range(sched.calls):
+            pool.linear(X, W, ids[c], Y)
+            if with_swaps and c in swaps:
+                slot, _ = swaps[c]
+                pool.unload_adapter(slot)
+                A, B = (old if restore else fresh)[c]
+                pool.load_adapter(slot, A, B, 16, 32.0)
+
+    for _ in range(args.warmup):
+        pool.linear(X, W, ids[0], Y)
+    torch.cuda.synchronize(dev)
+
+    def timed(fn):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        fn()
+        torch.cuda.synchronize(dev)
+        return time.perf_counter() - t0
+
+    nvml = NvmlClockSampler(dev)
+    with ClockSampler(dev.index or 0) as clocks, nvml:
+        swap_s = timed(lambda: run(True, False))
+    nosw_s = timed(lambda: run(False, False))
+    timed(lambda: run(True, True))                     # put the first generation back
+    assert pool.check_errors() == al.LORA_OK
+    n_tok = p.T * sched.calls
+    clk = nvml.summary() or dict(clocks.summary(), source="nvidia-smi")
+    out = {
+        "metric": METRIC, "value": n_tok / swap_s, "unit": UNIT, "n_gpus": 1,
+        "steps": sched.calls, "warmup": args.warmup,
+        "ms_per_step": 1e3 * swap_s / sched.calls, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "hot-swap stream: 1000 calls x 256 tokens, 2000 x r16 adapters, "
+                               "Zipf ids, 50 unload+reload cycles", "T": p.T, "d_in": p.d_in,
+                   "d_out": p.d_out, "adapters": p.max_adapters, "rank": 16,
+                   "launch": "direct calls (a swap synchronises the device)",
+                   "l2": "one W (33.5 MB) stays in L2 across calls; the 2000 adapters' pages "
+                         "(524 MB) do not",
+                   "parallelism": "single GPU"},
+        "no_swap_ms_per_step": 1e3 * nosw_s / sched.calls,
+        "swap_cycle_ms": 1e3 * (swap_s - nosw_s) / max(1, len(swaps)),
+        "clocks": clk,
+        "e2e": {"value": n_tok / swap_s, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 2 * sched.calls + len(swaps),
+        "cpu_baseline": None,
+    }
+    print(json.dumps(out), flush=True)
+
+
 # --------------------------------------------------------------------- main
 
 def dist_env():
@@ -538,6 +624,8 @@ def main():
         return run_reference(args)
     if args.workload == "llama3_layer":
         return run_grouped_layer(args)
+    if args.workload == "hotswap_stream":
+        return run_hotswap_stream(args)
 
     import torch
     import adapter_linear_gb300 as al
