@@ -375,10 +375,7 @@ def run_grouped_layer(args):
         torch.cuda.synchronize(dev)
         total_ms = time_program(g_prog)
         torch.cuda.synchronize(dev)
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, ws, dev)
     sep_ms = time_program(s_prog)
     base_ms = time_program(b_prog)
     gbase_ms = time_program(gb_prog)
@@ -449,7 +446,7 @@ def run_grouped_layer(args):
                "sample": f"{n} of {T} tokens through all 7 modules per pass, {done} tokens in {el:.1f} s"}
     clk = nvml.summary() or dict(clocks.summary(), source="nvidia-smi")
     out = {
-        "metric": METRIC, "value": T * args.steps * ws / (total_ms / 1e3), "unit": UNIT,
+        "metric": METRIC, "value": job_tokens_per_s(T * args.steps, ws, total_ms), "unit": UNIT,
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
@@ -573,6 +570,23 @@ def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     return ws, rank, local
+
+
+def max_over_ranks(ms: float, ws: int, device=None) -> float:
+    """The timed region's length as the slowest rank saw it (replicas: every rank runs
+    the same steps on its own GPU; the job takes as long as its slowest rank)."""
+    if ws <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tt = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_tokens_per_s(tokens_per_rank: int, ws: int, ms: float) -> float:
+    """Whole-job throughput: the tokens all ranks processed over the slowest rank's time."""
+    return tokens_per_rank * ws / (ms / 1e3)
 
 
 def run_reference(args):
@@ -725,12 +739,8 @@ def main():
         barrier()
         total_ms = time_program(lora_prog)
         barrier()
-    if ws > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    tokens = p.T * args.steps * ws
-    value = tokens / (total_ms / 1e3)
+    total_ms = max_over_ranks(total_ms, ws, dev)
+    value = job_tokens_per_s(p.T * args.steps, ws, total_ms)
 
     # ---- base-only reference, same structure
     base_prog()
