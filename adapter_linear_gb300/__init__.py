@@ -41,7 +41,7 @@ EXPORTS = (
     "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info",
 )
 PLAN_INFO_FIELDS = ("units", "G", "grid", "max_seg", "n_acc", "stages", "tmem_cols", "smem_bytes",
-                    "pairs", "col_blocks", "tight", "ntok", "partials_floats")
+                    "pairs", "col_blocks", "tight", "ntok", "partials_floats", "prefetch_a")
 CACHE_STATS_FIELDS = ("registered", "resident", "hits", "misses", "evictions")
 LORA_MAX_GROUP = 8
 LORA_KERNEL_SLOTS = 4

@@ -327,6 +327,30 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         named_bar_sync(kBarSetup, kThreads);
         tc_fence_after_sync();
         const uint32_t tmem = *tmem_slot;
+        // Before the wait on the previous kernel: the A pages of this CTA's shrink pairs
+        // into L2 (line prefetches, so the TMA engine keeps serving the W ring), where
+        // the plan says it pays. The ids read here may still be written by an earlier
+        // kernel in the stream, so they only steer these requests; the pairs below
+        // read the ids again after the wait.
+        if (ids != nullptr && p.prefetch_a) {
+            int m = 0;
+            for (int u = c; u < p.pairs; u += (int)gridDim.x) {
+                while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
+                const DecodeProblem &pr = p.prob[pick<NP>(m)];
+                const int lp = u - pr.pair_begin;
+                const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
+                const int id = ids[t];
+                if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
+                const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
+                if (q >= row[SLOT_NPAGES]) continue;
+                const int page = row[SLOT_PAGES + q];
+                if (page < 0 || page >= pr.pool.num_pages) continue;
+                const uint8_t *Ap = reinterpret_cast<const uint8_t *>(pr.pool.A_pages) +
+                                    (size_t)page * kRankPage * pr.pool.d_in * 2;
+                for (int i = threadIdx.x; i < kRankPage * pr.pool.d_in * 2 / 128; i += 128)
+                    prefetch_l2(Ap + (size_t)i * 128);
+            }
+        }
         pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
         if (ids != nullptr) {
             // this CTA's pairs: c, c + grid, c + 2 grid, ...; with more than one of them
@@ -395,6 +419,34 @@ __device__ __forceinline__ void expand8(float (&acc)[kFinishCols], const float *
     for (int c = 0; c < kFinishCols; ++c) acc[c] = dot8_f32_bf16(v, b[c], acc[c]);
 }
 
+// The pages of adapter slot `id` (0 pages when the slot is not loaded or id is -1).
+__device__ __forceinline__ int finish_adapter(const PoolDev &pool, int id, const int32_t *&pages)
+{
+    if (!slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+        pages = nullptr;
+        return 0;
+    }
+    const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+    pages = row + SLOT_PAGES;
+    return row[SLOT_NPAGES];
+}
+
+// The B words of columns n0..n0+7 of the first kPrefetchPages pages into registers,
+// the later pages' line into L2.
+__device__ __forceinline__ void finish_b_words(const PoolDev &pool, const int32_t *pages, int np,
+                                               int n0, uint4 (&b)[kPrefetchPages][8])
+{
+#pragma unroll
+    for (int q = 0; q < kPrefetchPages; ++q)
+        if (q < np) {
+            const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
+        }
+    for (int q = kPrefetchPages; q < np; ++q)
+        prefetch_l2(pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage);
+}
+
 // LORA = false: the base-only pass (no adapter state, few registers).
 template <int NP, bool LORA>
 __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
@@ -414,32 +466,18 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     const int t = blockIdx.y;
     const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
 
-    // ---- independent of the GEMM kernel: this token's adapter and its B words (the
+    // ---- ahead of the GEMM kernel's end: this token's adapter and its B words (the
     // 8 columns' 16-byte words of a page are one 128-byte line): the first pages into
-    // registers, the rest into L2
-    int np = 0;
+    // registers, the rest into L2. The id read here may still be written by a kernel
+    // ahead of the GEMM in the stream, so it is read again after the wait and the
+    // words are reloaded if it changed.
+    int id = -1, np = 0;
     const int32_t *pages = nullptr;
-    if (LORA && pool.slots != nullptr) {
-        const int id = ids[t];
-        if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
-            const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
-            np = row[SLOT_NPAGES];
-            pages = row + SLOT_PAGES;
-        } else if (id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin) {
-            atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
-        }
-    }
     uint4 b[kPrefetchPages][8];
-    if (LORA && col_ok) {
-#pragma unroll
-        for (int q = 0; q < kPrefetchPages; ++q)
-            if (q < np) {
-                const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
-#pragma unroll
-                for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
-            }
-        for (int q = kPrefetchPages; q < np; ++q)
-            prefetch_l2(pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage);
+    if (LORA && pool.slots != nullptr) {
+        id = ids[t];
+        np = finish_adapter(pool, id, pages);
+        if (col_ok) finish_b_words(pool, pages, np, n0, b);
     }
     // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
     // can have started before the tile; its partial for the tile is its segment
@@ -456,6 +494,17 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
 
     // ---- partials and V are written by the GEMM kernel
     pdl_wait_prior();
+    bool early = true;  // the words in b belong to this token's adapter
+    if (LORA && pool.slots != nullptr) {
+        const int id_now = ids[t];
+        if (id_now != id) {
+            id = id_now;
+            np = finish_adapter(pool, id, pages);
+            early = false;
+        }
+        if (np == 0 && id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin)
+            atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
+    }
     if (!col_ok) return;
 
     float acc[kFinishCols];
@@ -493,7 +542,7 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
         const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
         v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
         v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
-        if (q < kPrefetchPages) {
+        if (q < kPrefetchPages && early) {
             if (q == 0) expand8(acc, v, b[0]);
             else expand8(acc, v, b[1]);
         } else {
@@ -545,7 +594,7 @@ __global__ void __maxnreg__(96)
 }
 
 template <int NP, bool LORA>
-__global__ void __launch_bounds__(kFinishThreads)
+__global__ void __launch_bounds__(kFinishThreads, 3)
     finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
                          const int32_t *__restrict__ ids)
 {
@@ -629,6 +678,11 @@ bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max
     const double shrink_bytes = (double)((pairs + p.grid - 1) / p.grid) * 2.0 * kRankPage * max_d_in;
     const double stream_bytes = (double)U / (double)G * kBoxes * kWTileBytes;
     p.tight = pairs > 0 && cols * T > max_G && 2.0 * shrink_bytes <= stream_bytes;
+    // the A pages requested into L2 before the wait on the previous kernel: measured
+    // faster where a CTA has one pair (k_proj T = 32: 10.5 -> 10.0 us) or its pairs'
+    // A bytes are small beside its W bytes (the 7-module layer: 95 -> 92 us), slower
+    // where they are as large as its W share (T = 256, ~3.4 pairs per CTA: 34 -> 37)
+    p.prefetch_a = pairs > 0 && (pairs <= p.grid || 4.0 * shrink_bytes <= stream_bytes);
     int max_seg = 1;
     for (int c = 0; c < p.G; ++c) {
         const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
@@ -671,6 +725,7 @@ DecodePlanT<NP> narrow_plan(const DecodePlan &p)
     q.pairs = p.pairs;
     q.col_blocks = p.col_blocks;
     q.tight = p.tight;
+    q.prefetch_a = p.prefetch_a;
     q.tmem_cols = p.tmem_cols;
     q.smem_bytes = p.smem_bytes;
     for (int m = 0; m < NP; ++m) q.prob[m] = p.prob[m];

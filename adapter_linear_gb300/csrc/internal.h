@@ -65,6 +65,7 @@ struct PoolDev {
     int slot_stride;
     int max_adapters;
     int max_pages;            // pages per adapter at max_rank
+    int num_pages;            // pages in each arena
     int d_in, d_out;
 };
 
@@ -119,6 +120,7 @@ struct DecodePlanT {
     int pairs;              // shrink pairs of all problems
     int col_blocks;         // finishing grid.x
     bool tight;             // register-bounded kernel variants (see gemm_decode.cu)
+    bool prefetch_a;        // A pages of the shrink pairs into L2 before the wait
     uint32_t tmem_cols;
     size_t smem_bytes;
     DecodeProblem prob[NP];

@@ -54,6 +54,7 @@ PoolDev pool_view(const lora_pool *p)
     v.slot_stride = p->slot_stride;
     v.max_adapters = p->max_adapters;
     v.max_pages = p->max_pages;
+    v.num_pages = p->num_pages;
     v.d_in = p->d_in;
     v.d_out = p->d_out;
     return v;
@@ -660,7 +661,8 @@ lora_status lora_decode_plan_info(int n, int T, const int *d_in, const int *d_ou
     const int64_t v[LORA_PLAN_INFO_COUNT] = {p.U, p.G, p.grid, p.max_seg, p.n_acc, p.stages,
                                              (int64_t)p.tmem_cols, (int64_t)p.smem_bytes, p.pairs,
                                              p.col_blocks, p.tight ? 1 : 0, p.ntok,
-                                             (int64_t)decode_partials_floats(p)};
+                                             (int64_t)decode_partials_floats(p),
+                                             p.prefetch_a ? 1 : 0};
     for (int i = 0; i < LORA_PLAN_INFO_COUNT; ++i) out[i] = v[i];
     return LORA_OK;
 }

@@ -336,11 +336,12 @@ lora_status lora_pool_check_errors(lora_pool_t pool);
  * no adapters). out[LORA_PLAN_INFO_COUNT] = {units, ranges G, CTAs launched,
  * most tiles per range, TMEM accumulators, pipeline stages, TMEM columns,
  * GEMM dynamic shared memory bytes, shrink pairs, finishing blocks, register-
- * bounded variant (0/1), T rounded up to 16, split-K partial floats}.
+ * bounded variant (0/1), T rounded up to 16, split-K partial floats, A pages
+ * requested into L2 before the wait on the previous kernel (0/1)}.
  * Errors: ARG (null pointers, n outside 1..LORA_MAX_GROUP, T outside 1..256,
  * num_sms < 1), SHAPE.
  */
-#define LORA_PLAN_INFO_COUNT 13
+#define LORA_PLAN_INFO_COUNT 14
 lora_status lora_decode_plan_info(int n, int T, const int *d_in, const int *d_out,
                                   const int *max_pages, int num_sms, int64_t *out);
 

@@ -65,6 +65,10 @@ def check(T, d_in, d_out, pages, sms=152):
     if pairs > info["G"]:
         assert info["grid"] == min(pairs, sms)
     assert info["partials_floats"] == info["G"] * max_seg * T * 128
+    # A-page prefetch: one pair per CTA, or the pairs' A bytes a quarter of the W share
+    shrink = -(-pairs // info["grid"]) * 16 * max(d_in) if pairs else 0
+    stream = U / info["G"] * 2 * 128 * 128
+    assert info["prefetch_a"] == int(pairs > 0 and (pairs <= info["grid"] or 4 * shrink <= stream))
     assert U * info["G"] < 2 ** 31
     return info
 
@@ -77,6 +81,7 @@ def test_plan_of_the_benchmarked_shapes():
     assert layer["units"] == 13312 and layer["col_blocks"] == 42
     hs = check(256, [4096], [4096], [2])
     assert hs["tight"] == 0 and hs["n_acc"] == 2       # 256 columns per accumulator
+    assert (q["prefetch_a"], layer["prefetch_a"], hs["prefetch_a"]) == (1, 1, 0)
     tiny = check(64, [256], [256], [1])
     assert tiny["G"] == 4 and tiny["grid"] == 64       # extra CTAs run shrink pairs only
     base = check(64, [4096], [4096], [0])
