@@ -27,6 +27,7 @@ STATUS_NAMES = {
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 LORA_PATH_AUTO, LORA_PATH_DECODE, LORA_PATH_PREFILL = 0, 1, 2
+LORA_PREFILL_AUTO, LORA_PREFILL_SINGLE, LORA_PREFILL_PAIR = 0, 1, 2
 LORA_STATS_COUNT = 7
 STATS_FIELDS = ("loaded", "free_pages", "total_pages", "loads", "unloads", "calls", "bytes_held")
 
@@ -34,7 +35,7 @@ STATS_FIELDS = ("loaded", "free_pages", "total_pages", "loads", "unloads", "call
 EXPORTS = (
     "lora_pool_create", "lora_pool_destroy", "lora_pool_reserve", "lora_load_adapter",
     "lora_unload_adapter", "lora_linear", "lora_linear_host", "lora_base_linear",
-    "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path",
+    "lora_pool_check_errors", "lora_build_segments", "lora_pool_stats", "lora_pool_set_path", "lora_pool_set_prefill_kernel",
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
@@ -84,6 +85,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_build_segments": [vp, vp, i32, vp, vp, vp, vp, vp, vp],
         "lora_pool_stats": [vp, vp],
         "lora_pool_set_path": [vp, i32],
+        "lora_pool_set_prefill_kernel": [vp, i32],
         "lora_status_string": [i32],
         "lora_abi_version": [],
         "lora_pool_enable_timing": [vp, i32],
@@ -231,6 +233,10 @@ def lora_pool_set_path(pool: int, path: int) -> int:
     return load_library().lora_pool_set_path(pool, path)
 
 
+def lora_pool_set_prefill_kernel(pool: int, kernel: int) -> int:
+    return load_library().lora_pool_set_prefill_kernel(pool, kernel)
+
+
 def lora_pool_enable_timing(pool: int, enable: bool) -> int:
     return load_library().lora_pool_enable_timing(pool, int(bool(enable)))
 
@@ -319,6 +325,9 @@ class LoraPool:
 
     def set_path(self, path: int):
         _check(lora_pool_set_path(self.handle, path), "lora_pool_set_path")
+
+    def set_prefill_kernel(self, kernel: int):
+        _check(lora_pool_set_prefill_kernel(self.handle, kernel), "lora_pool_set_prefill_kernel")
 
     def linear(self, X, W, ids, Y=None, stream=None):
         import torch

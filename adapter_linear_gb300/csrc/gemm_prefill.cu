@@ -25,6 +25,8 @@
 //    bf16 and stores Y. For a tile whose tokens use more than one adapter the
 //    expand is added here instead, on CUDA cores (B pages read 16 bytes = 8
 //    rank rows per column), before the rounding.
+#include <mutex>
+
 #include "device_common.cuh"
 
 namespace lora {
@@ -90,6 +92,71 @@ __device__ __forceinline__ TileLora tile_lora(int m, const PrefillArgs &a, const
     r.blocks = (r.npages + kPagesPerBlock - 1) / kPagesPerBlock;
     r.pages = row + SLOT_PAGES;
     return r;
+}
+
+// One epilogue warp's share of a finished accumulator: TMEM lanes 32*quarter.. (token
+// rows t = row0 + lane), columns 128*half.. of the tile at column n0, in chunks of 32;
+// with `own_expand`, each row's adapter expand added on CUDA cores; rounded to bf16
+// and stored.
+__device__ __forceinline__ void epilogue_rows(uint32_t tmem_buf, int quarter, int half, int row0, int n0,
+                                              bool own_expand, const PrefillArgs &a, const PoolDev &pool)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = row0 + lane;
+    const bool row_ok = t < a.T;
+    int np = 0;
+    const int32_t *pages = nullptr;
+    const uint16_t *hrow = nullptr;
+    if (own_expand && row_ok) {  // several adapters: this row's own expand
+        const int id = a.ids[t];
+        if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+            const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+            np = row[SLOT_NPAGES];
+            pages = row + SLOT_PAGES;
+            hrow = a.Vhl + (size_t)t * a.ldh;
+        }
+    }
+    uint16_t *yrow = a.Y + (size_t)t * a.d_out;
+#pragma unroll 1
+    for (int ch = 0; ch < 4; ++ch) {
+        const int col0 = half * 128 + ch * 32;
+        const int ncol = n0 + col0;
+        uint32_t r[32];
+        tmem_ld32_wait(tmem_buf + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0, r);
+        float acc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+        for (int q = 0; q < np; ++q) {
+            const uint16_t *g = hrow + (q / 4) * 64 + (q % 4) * 8;
+            const uint4 h = *reinterpret_cast<const uint4 *>(g);
+            const uint4 l = *reinterpret_cast<const uint4 *>(g + 32);
+            const float vv[8] = {bf16_lo(h.x) + bf16_lo(l.x), bf16_hi(h.x) + bf16_hi(l.x),
+                                 bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
+                                 bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
+                                 bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
+            const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if (ncol + j < a.d_out) {
+                    const uint4 b = ldg_nc_v4(bp + j * kRankPage);
+                    acc[j] = dot8_f32_bf16(vv, b, acc[j]);
+                }
+            }
+        }
+        if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 8) {
+                if (ncol + j < a.d_out) {
+                    uint4 o;
+                    o.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
+                    o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
+                    o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
+                    o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
+                    *reinterpret_cast<uint4 *>(yrow + ncol + j) = o;
+                }
+            }
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -240,61 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
 
-            const int t = m * kBM + quarter * 32 + lane;
-            const bool row_ok = t < a.T;
-            int np = 0;
-            const int32_t *pages = nullptr;
-            const uint16_t *hrow = nullptr;
-            if (tl.mode == 2 && row_ok) {  // several adapters: this row's own expand
-                const int id = a.ids[t];
-                if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
-                    const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
-                    np = row[SLOT_NPAGES];
-                    pages = row + SLOT_PAGES;
-                    hrow = a.Vhl + (size_t)t * a.ldh;
-                }
-            }
-            uint16_t *yrow = a.Y + (size_t)t * a.d_out;
-#pragma unroll 1
-            for (int ch = 0; ch < 4; ++ch) {
-                const int col0 = half * 128 + ch * 32;
-                const int ncol = n * kBN + col0;
-                uint32_t r[32];
-                tmem_ld32_wait(tmem + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * kBN + col0), r);
-                float acc[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
-                for (int q = 0; q < np; ++q) {
-                    const uint16_t *g = hrow + (q / 4) * 64 + (q % 4) * 8;
-                    const uint4 h = *reinterpret_cast<const uint4 *>(g);
-                    const uint4 l = *reinterpret_cast<const uint4 *>(g + 32);
-                    const float vv[8] = {bf16_lo(h.x) + bf16_lo(l.x), bf16_hi(h.x) + bf16_hi(l.x),
-                                         bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
-                                         bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
-                                         bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
-                    const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        if (ncol + j < a.d_out) {
-                            const uint4 b = ldg_nc_v4(bp + j * kRankPage);
-                            acc[j] = dot8_f32_bf16(vv, b, acc[j]);
-                        }
-                    }
-                }
-                if (row_ok) {
-#pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        if (ncol + j < a.d_out) {
-                            uint4 o;
-                            o.x = pack_bf16x2(acc[j + 0], acc[j + 1]);
-                            o.y = pack_bf16x2(acc[j + 2], acc[j + 3]);
-                            o.z = pack_bf16x2(acc[j + 4], acc[j + 5]);
-                            o.w = pack_bf16x2(acc[j + 6], acc[j + 7]);
-                            *reinterpret_cast<uint4 *>(yrow + ncol + j) = o;
-                        }
-                    }
-                }
-            }
+            epilogue_rows(tmem + (uint32_t)(buf * kBN), quarter, half, m * kBM + quarter * 32, n * kBN,
+                          tl.mode == 2, a, pool);
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
@@ -309,10 +323,391 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// ------------------------------------------------------------ CTA-pair variant
+//
+// A cluster of two CTAs computes a 256-token x 256-column tile with tcgen05 MMAs of
+// cta_group::2 (M = 256, N = 256, K = 16): CTA r holds tokens r*128.. of the tile
+// (its A half, and those rows of D in its TMEM) and W rows n0 + r*128.. (its half of
+// B). Per k-block each CTA stages 16 KB of X and 16 KB of W (32 KB instead of 48 KB
+// for 128 x 256 on one SM), so the tensor core's operand reads plus the TMA writes
+// into each SM's shared memory drop by a third and six stages fit. CTA 0 issues the
+// MMAs; both CTAs' TMA loads complete on CTA 0's stage barrier; its commits are
+// multicast to both CTAs' stage and accumulator barriers; both CTAs' epilogue warps
+// release the accumulator on CTA 0's barrier. The fused expand works as in the
+// single-CTA kernel when every adapter token of the 256 uses one adapter: V rows of
+// each half and each half's 128 columns of the adapter's B pages (one 2 KB TMA box
+// per page: the B arena read as [pages x d_out] rows of 8 rank values).
+
+// The pair kernel's epilogue for one warp: as epilogue_rows, but each 64-column chunk
+// goes, as bf16, into a 128-byte-swizzled 32-row x 64-column staging tile in shared
+// memory and leaves with one TMA store (rows past T and columns past d_out are not
+// written), so Y reaches L2 in whole 128-byte row segments instead of 16-byte pieces
+// of 32 rows at a time.
+__device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quarter, int half, int row0, int n0,
+                                                     bool own_expand, const PrefillArgs &a, const PoolDev &pool,
+                                                     uint8_t *ybuf, const CUtensorMap *tmY)
+{
+    const int lane = threadIdx.x & 31;
+    const int t = row0 + lane;
+    int np = 0;
+    const int32_t *pages = nullptr;
+    const uint16_t *hrow = nullptr;
+    if (own_expand && t < a.T) {  // several adapters: this row's own expand
+        const int id = a.ids[t];
+        if (slot_loaded(pool.slots, pool.slot_stride, pool.max_adapters, id)) {
+            const int32_t *row = pool.slots + (size_t)id * pool.slot_stride;
+            np = row[SLOT_NPAGES];
+            pages = row + SLOT_PAGES;
+            hrow = a.Vhl + (size_t)t * a.ldh;
+        }
+    }
+#pragma unroll 1
+    for (int ch = 0; ch < 2; ++ch) {
+        if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read ybuf
+        __syncwarp();
+#pragma unroll 1
+        for (int sub = 0; sub < 2; ++sub) {
+            const int col0 = half * 128 + ch * 64 + sub * 32;
+            const int ncol = n0 + col0;
+            uint32_t r[32];
+            tmem_ld32_wait(tmem_buf + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0, r);
+            float acc[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) acc[j] = __uint_as_float(r[j]);
+            for (int q = 0; q < np; ++q) {
+                const uint16_t *g = hrow + (q / 4) * 64 + (q % 4) * 8;
+                const uint4 h = *reinterpret_cast<const uint4 *>(g);
+                const uint4 l = *reinterpret_cast<const uint4 *>(g + 32);
+                const float vv[8] = {bf16_lo(h.x) + bf16_lo(l.x), bf16_hi(h.x) + bf16_hi(l.x),
+                                     bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
+                                     bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
+                                     bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
+                const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if (ncol + j < a.d_out) {
+                        const uint4 b = ldg_nc_v4(bp + j * kRankPage);
+                        acc[j] = dot8_f32_bf16(vv, b, acc[j]);
+                    }
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[8 * k + 0], acc[8 * k + 1]);
+                o.y = pack_bf16x2(acc[8 * k + 2], acc[8 * k + 3]);
+                o.z = pack_bf16x2(acc[8 * k + 4], acc[8 * k + 5]);
+                o.w = pack_bf16x2(acc[8 * k + 6], acc[8 * k + 7]);
+                const int c = sub * 4 + k;  // 16-byte chunk of the 128-byte row
+                *reinterpret_cast<uint4 *>(ybuf + lane * 128 + ((c ^ (lane & 7)) << 4)) = o;
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        const int x = n0 + half * 128 + ch * 64;
+        if (lane == 0 && x < a.d_out && row0 < a.T) tma_store_2d(tmY, ybuf, x, row0);
+    }
+}
+
+constexpr int kPBM = 256;                     // tokens per pair tile (128 per CTA)
+constexpr int kPHalfBytes = 128 * kBK * 2;    // 16 KB: one CTA's X or W half of a k-block
+constexpr int kPStageBytes = 2 * kPHalfBytes;
+constexpr int kPStages = 6;
+constexpr int kPGroupM = 8;                   // 8 x 256 tokens share one column sweep
+constexpr int kPSliceBytes = 128 * 16;        // 128 columns x 8 rank values of one page
+constexpr int kPYStageBytes = 32 * 128;       // one epilogue warp's 32 x 64 bf16 staging tile
+constexpr size_t kPairSmem =
+    1024 + (size_t)kPStages * kPStageBytes + kEpiWarps * kPYStageBytes + (2 * kPStages + 5) * 8 + 16;
+
+__device__ __forceinline__ void pair_tile_coords(int tile, const PrefillArgs &a, int &m, int &n)
+{
+    const int tiles_m = (a.T + kPBM - 1) / kPBM;
+    const int per_group = kPGroupM * a.tiles_n;
+    const int g = tile / per_group;
+    const int first_m = g * kPGroupM;
+    const int gm = min(kPGroupM, tiles_m - first_m);
+    const int local = tile - g * per_group;
+    m = first_m + local % gm;
+    n = local / gm;
+}
+
+// Adapter use of a pair tile: the tensor-core expand (mode 1) when every token of the
+// 256 that has an adapter uses the same one; otherwise each CTA adds its own rows'
+// expand in the epilogue (own_expand) where its 128-token half has adapters.
+__device__ __forceinline__ TileLora pair_tile_lora(int m, uint32_t rank, const PrefillArgs &a,
+                                                   const PoolDev &pool, bool &own_expand)
+{
+    own_expand = false;
+    TileLora r{0, -1, 0, 0, nullptr};
+    if (a.tile_info == nullptr) return r;
+    const int i0 = a.tile_info[2 * m];
+    const int i1 = 2 * m + 1 < a.tiles_m ? a.tile_info[2 * m + 1] : kTileNoAdapter;
+    int slot = -1;
+    bool single = true;
+    for (int k = 0; k < 2; ++k) {
+        const int ti = k ? i1 : i0;
+        if (ti == kTileMixed) single = false;
+        else if (ti >= 0) {
+            if (slot < 0) slot = ti;
+            else if (slot != ti) single = false;
+        }
+    }
+    if (!single) {
+        own_expand = (rank ? i1 : i0) != kTileNoAdapter;
+        return r;
+    }
+    if (slot < 0) return r;
+    const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
+    r.mode = 1;
+    r.slot = slot;
+    r.npages = row[SLOT_NPAGES];
+    r.blocks = (r.npages + kPagesPerBlock - 1) / kPagesPerBlock;
+    r.pages = row + SLOT_PAGES;
+    return r;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
+                             const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
+                             const __grid_constant__ CUtensorMap tmY, PrefillArgs a, PoolDev pool)
+{
+    extern __shared__ uint8_t pre_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(pre_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *ystage = smem + (size_t)kPStages * kPStageBytes;  // [kEpiWarps][32 x 128 B]
+    uint64_t *full = reinterpret_cast<uint64_t *>(ystage + kEpiWarps * kPYStageBytes);
+    uint64_t *empty = full + kPStages;
+    uint64_t *acc_full = empty + kPStages;  // [2]
+    uint64_t *acc_empty = acc_full + 2;     // [2], used in CTA 0
+    uint64_t *drain = acc_empty + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    __shared__ int abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_cta_rank();
+    const int cluster = (int)blockIdx.x >> 1, clusters = (int)gridDim.x >> 1;
+    const int tiles = ((a.T + kPBM - 1) / kPBM) * a.tiles_n;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&acc_full[i], 1);
+            mbar_init(&acc_empty[i], 2 * kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_map(&tmX);
+        tma_prefetch_map(&tmW);
+        tma_prefetch_map(&tmV);
+        tma_prefetch_map(&tmB);
+        tma_prefetch_map(&tmY);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before either signals the other's
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 8) {
+        // ------------------------------------------- producer (both CTAs, own halves)
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < tiles && ok; tile += clusters) {
+                int m, n;
+                pair_tile_coords(tile, a, m, n);
+                bool own;
+                const TileLora tl = pair_tile_lora(m, rank, a, pool, own);
+                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
+                const int n0 = n * kBN + (int)rank * 128;   // this CTA's W rows / B columns
+                const int r0 = m * kPBM + (int)rank * 128;  // this CTA's token rows
+                for (int kb = 0; kb < steps; ++kb, ++it) {
+                    const int s = it % kPStages;
+                    ok = mbar_wait_cluster(&empty[s], ((uint32_t)(it / kPStages) & 1u) ^ 1u, &abort_flag,
+                                           a.err);
+                    if (!ok) break;
+                    const uint32_t fb = cluster_map(&full[s], 0);
+                    uint8_t *xs = smem + (size_t)s * kPStageBytes;
+                    if (kb < a.KB) {
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kPStageBytes);
+                        tma_load_2d_pair(xs, &tmX, fb, kb * kBK, r0);
+                        tma_load_2d_pair(xs + kPHalfBytes, &tmW, fb, kb * kBK, n0);
+                    } else {
+                        const int e = kb - a.KB;
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(&full[s], 2 * (kPHalfBytes + kPagesPerBlock * kPSliceBytes));
+                        tma_load_2d_pair(xs, &tmV, fb, e * 64, r0);
+                        for (int i = 0; i < kPagesPerBlock; ++i) {
+                            const int q = e * kPagesPerBlock + i;
+                            const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
+                            tma_load_2d_pair(xs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
+                                             page * a.d_out + n0);
+                        }
+                    }
+                }
+            }
+            // CTA 0's stage barriers count both CTAs' copies: do not leave while any is
+            // in flight
+            for (int i = 0; rank == 0 && i < kPStages && i < it; ++i) {
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait_cluster(&full[j % kPStages], (uint32_t)(j / kPStages) & 1u, &dummy, a.err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 9) {
+        // ------------------------------------------------------- MMA (CTA 0 only)
+        if (lane == 0 && rank == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kPBM, kBN);
+            int it = 0, tc = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < tiles && ok; tile += clusters, ++tc) {
+                int m, n;
+                pair_tile_coords(tile, a, m, n);
+                bool own;
+                const TileLora tl = pair_tile_lora(m, rank, a, pool, own);
+                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
+                const int buf = tc & 1;
+                ok = mbar_wait_cluster(&acc_empty[buf], ((uint32_t)(tc >> 1) & 1u) ^ 1u, &abort_flag, a.err);
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t d = tmem + (uint32_t)(buf * kBN);
+                for (int kb = 0; kb < steps; ++kb, ++it) {
+                    const int s = it % kPStages;
+                    ok = mbar_wait_cluster(&full[s], (uint32_t)(it / kPStages) & 1u, &abort_flag, a.err);
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    const uint32_t xa = smem_u32(smem + (size_t)s * kPStageBytes);
+                    const uint32_t wa = xa + kPHalfBytes;
+                    if (kb < a.KB) {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32), idesc,
+                                             (kb | kk) != 0);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32),
+                                             sdesc_k_none(wa + (kk & 1) * 2 * kPSliceBytes, kPSliceBytes, 128),
+                                             idesc, 1u);
+                    }
+                    mma_commit_pair(&empty[s], 0x3);
+                }
+                if (ok) mma_commit_pair(&acc_full[buf], 0x3);
+            }
+            mma_commit_pair(drain, 0x1);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, a.err);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------- epilogue (both CTAs, own rows)
+        const int quarter = warp & 3, half = warp >> 2;
+        const uint32_t release = 0;  // CTA 0 holds the accumulator barriers' empty side
+        int tc = 0;
+        for (int tile = cluster; tile < tiles; tile += clusters, ++tc) {
+            int m, n;
+            pair_tile_coords(tile, a, m, n);
+            bool own;
+            pair_tile_lora(m, rank, a, pool, own);
+            const int buf = tc & 1;
+            bool ok = true;
+            if (lane == 0)
+                ok = mbar_wait_cluster(&acc_full[buf], (uint32_t)(tc >> 1) & 1u, &abort_flag, a.err);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            tc_fence_after_sync();
+            epilogue_rows_staged(tmem + (uint32_t)(buf * kBN), quarter, half,
+                                 m * kPBM + (int)rank * 128 + quarter * 32, n * kBN, own, a, pool,
+                                 ystage + warp * kPYStageBytes, &tmY);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(cluster_map(&acc_empty[buf], release));
+        }
+        if (lane == 0) bulk_wait_all();  // this warp's stores of Y have completed
+        __syncwarp();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the other may still use its memory
+    if (warp == 9) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem, kTmemCols);
+    }
+}
+
+// Clusters of the pair kernel that can be resident at once on the current device
+// (clusters sit within one GPC, so this can be below half the SMs).
+int pair_clusters(size_t smem, int num_sms)
+{
+    static int cached[64];
+    static std::once_flag once[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return num_sms / 2;
+    std::call_once(once[dev], [&] {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (num_sms / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, (const void *)gemm_prefill_pair_kernel, &cfg) != cudaSuccess ||
+            n < 1) {
+            cudaGetLastError();
+            n = num_sms / 2;
+        }
+        cached[dev] = n < num_sms / 2 ? n : num_sms / 2;
+    });
+    return cached[dev] > 0 ? cached[dev] : 1;
+}
+
+cudaError_t launch_pair(const CUtensorMap &tmX, const CUtensorMap &tmW, const CUtensorMap &tmV,
+                        const CUtensorMap &tmB, const CUtensorMap &tmY, const PrefillArgs &a, const PoolDev &pool,
+                        int num_sms, cudaStream_t stream)
+{
+    const size_t smem = kPairSmem;
+    cudaError_t e = ensure_smem_attr((const void *)gemm_prefill_pair_kernel, smem);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((a.T + kPBM - 1) / kPBM) * a.tiles_n;
+    int clusters = pair_clusters(smem, num_sms);
+    if (clusters > tiles) clusters = tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_prefill_pair_kernel, tmX, tmW, tmV, tmB, tmY, a, pool);
+}
+
 }  // namespace
 
 cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
-                                const CUtensorMap &tmV, int T, const int32_t *ids,
+                                const CUtensorMap &tmV, const CUtensorMap *tmB, const CUtensorMap *tmY, int T,
+                                const int32_t *ids,
                                 const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
                                 int num_sms, int *err, cudaStream_t stream)
 {
@@ -331,6 +726,10 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
     a.Y = Y;
     a.err = err;
     if (a.num_tiles == 0) return cudaSuccess;
+    if (tmB != nullptr) {
+        if (tmY == nullptr) return cudaErrorInvalidValue;
+        return launch_pair(tmX, tmW, tmV, *tmB, *tmY, a, pool, num_sms, stream);
+    }
     const size_t smem = 1024 + (size_t)kStages * kStageBytes + (2 * kStages + 5) * 8 + 16;
     cudaError_t e = ensure_smem_attr((const void *)gemm_prefill_kernel, smem);
     if (e != cudaSuccess) return e;

@@ -150,8 +150,12 @@ cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, 
 
 // Prefill GEMM with the expand: tmV is a TMA map of Vhl [T x ldh] (box 128 x 64);
 // tile_info from the segment builder; ids == nullptr: base product only.
+// tmB == nullptr: one CTA per 128 x 256 tile (tmW box 256 x 64); else CTA pairs per
+// 256 x 256 tile (tmW box 128 x 64, tmB the B arena's 128 x 8 boxes, tmY a map of Y
+// with box 32 x 64).
 cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
-                                const CUtensorMap &tmV, int T, const int32_t *ids,
+                                const CUtensorMap &tmV, const CUtensorMap *tmB, const CUtensorMap *tmY, int T,
+                                const int32_t *ids,
                                 const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
                                 int num_sms, int *err, cudaStream_t stream);
 
@@ -165,9 +169,11 @@ cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, 
 // per kernel and device, so repeated launches do not repeat the driver calls).
 cudaError_t ensure_smem_attr(const void *kernel, size_t bytes);
 
-// Host: build a 2-D bf16 TMA descriptor with 128-byte swizzle over a row-major
-// [rows x inner] tensor, box [box_rows x box_inner].
+// Host: build a 2-D bf16 TMA descriptor over a row-major [rows x inner] tensor, box
+// [box_rows x box_inner], with 128-byte swizzle (or none: rows land box_inner * 2
+// bytes apart).
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows,
+                       bool swizzle128 = true);
 
 }  // namespace lora

@@ -303,10 +303,13 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
     } else {
         if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
         if (!mark(0)) return LORA_ERR_CUDA;
+        const bool pair = p->pair_ok && (p->prefill_kernel == LORA_PREFILL_PAIR ||
+                                         (p->prefill_kernel == LORA_PREFILL_AUTO && T > 128));
         const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, 128);
-        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, 256);
+        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, pair ? 128 : 256);
         const CUtensorMap *tmV = tmap_for(p, p->Vhl, p->ldh, T, 64, 128);
-        if (!tmW || !tmX || !tmV) return LORA_ERR_ARG;
+        const CUtensorMap *tmY = pair ? tmap_for(p, Y, p->d_out, T, 64, 32) : nullptr;
+        if (!tmW || !tmX || !tmV || (pair && !tmY)) return LORA_ERR_ARG;
         if (with_lora) {
             // rows of tokens without an adapter must read as zero in the expand
             CUDA_TRY(cudaMemsetAsync(p->Vhl, 0, sizeof(uint16_t) * (size_t)T * p->ldh, stream));
@@ -314,7 +317,7 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
                                       p->d_err, stream));
         }
         if (!mark(1)) return LORA_ERR_CUDA;
-        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, *tmV, T, with_lora ? ids : nullptr,
+        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, *tmV, pair ? &p->tmB : nullptr, tmY, T, with_lora ? ids : nullptr,
                                      with_lora ? p->tile_info : nullptr, pd, p->Vhl, p->ldh, Yb,
                                      p->num_sms, p->d_err, stream));
         if (!mark(2)) return LORA_ERR_CUDA;
@@ -413,6 +416,11 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
         lora_pool_destroy(p);
         return LORA_ERR_CUDA;
     }
+    // the CTA-pair prefill kernel reads B page slices with one TMA box each; its row
+    // coordinate (page * d_out + column) is a 32-bit int
+    const uint64_t b_rows = (uint64_t)p->num_pages * d_out;
+    p->pair_ok = b_rows + 256 < (1ull << 31) &&
+                 make_tmap_bf16_2d(&p->tmB, p->B_pages, kRankPage, b_rows, kRankPage * 2, kRankPage, 128, false);
     *out = p;
     return LORA_OK;
 }
@@ -765,6 +773,14 @@ lora_status lora_pool_set_path(lora_pool_t p, int path)
     return LORA_OK;
 }
 
+lora_status lora_pool_set_prefill_kernel(lora_pool_t p, int kernel)
+{
+    if (!p || kernel < LORA_PREFILL_AUTO || kernel > LORA_PREFILL_PAIR) return LORA_ERR_ARG;
+    if (kernel == LORA_PREFILL_PAIR && !p->pair_ok) return LORA_ERR_UNSUPPORTED;
+    p->prefill_kernel = kernel;
+    return LORA_OK;
+}
+
 }  // extern "C"
 
 // ============================================================== helpers
@@ -816,7 +832,7 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t bytes)
 }
 
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows)
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
 {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
@@ -835,7 +851,8 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint6
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }

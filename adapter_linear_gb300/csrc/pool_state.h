@@ -57,6 +57,8 @@ struct lora_pool {
     cudaStream_t copy_stream = nullptr;
     CUtensorMap tmA;   // A arena [num_pages*8 rows x d_in], box 8 x 64
     CUtensorMap tmAw;  // the same, box round16(8 * max_pages) x 64
+    CUtensorMap tmB;   // B arena as [num_pages*d_out rows x 8], box 128 x 8, no swizzle
+    bool pair_ok = false;  // tmB exists (rows < 2^31): the CTA-pair prefill kernel can run
 
     // per-call scratch, sized for cap_T tokens
     int cap_T = 0;
@@ -71,10 +73,11 @@ struct lora_pool {
     uint16_t *hx = nullptr, *hy = nullptr;
     int32_t *hids = nullptr;
 
-    TmapEntry tmaps[6];
+    TmapEntry tmaps[8];
     int tmap_next = 0;
 
     int path = LORA_PATH_AUTO;
+    int prefill_kernel = LORA_PREFILL_AUTO;
     bool timing = false;
     cudaEvent_t ev[LORA_KERNEL_SLOTS + 1] = {};
     bool ev_used[LORA_KERNEL_SLOTS] = {};

@@ -80,6 +80,11 @@ typedef enum {
  * PREFILL above; DECODE accepts T <= 256 only. Both compute the same result. */
 typedef enum { LORA_PATH_AUTO = 0, LORA_PATH_DECODE = 1, LORA_PATH_PREFILL = 2 } lora_path;
 
+/* Which prefill GEMM kernel the PREFILL path uses. AUTO picks PAIR for T > 128:
+ * a cluster of two CTAs per 256-token x 256-column tile (tcgen05 MMAs spanning
+ * both SMs); SINGLE is one CTA per 128 x 256 tile. Both compute the same result. */
+typedef enum { LORA_PREFILL_AUTO = 0, LORA_PREFILL_SINGLE = 1, LORA_PREFILL_PAIR = 2 } lora_prefill_kernel;
+
 /*
  * Create a pool on the current CUDA device for one linear layer of shape
  * d_in -> d_out, with room for max_adapters adapters of rank <= max_rank.
@@ -390,6 +395,11 @@ lora_status lora_pool_kernel_times(lora_pool_t pool, float *ms);
 
 /* Force a kernel family (lora_path); LORA_PATH_AUTO restores the default. */
 lora_status lora_pool_set_path(lora_pool_t pool, int path);
+
+/* Force the prefill GEMM kernel (lora_prefill_kernel); LORA_PREFILL_AUTO restores
+ * the default. Errors: ARG (unknown value), UNSUPPORTED (PAIR on a pool whose B arena
+ * has 2^31 or more rows of 8 rank values). */
+lora_status lora_pool_set_prefill_kernel(lora_pool_t pool, int kernel);
 
 /* Static description of a status code. */
 const char *lora_status_string(lora_status status);

@@ -1,0 +1,123 @@
+"""The prefill path's two GEMM kernels on the same inputs, against the oracle: one CTA per
+128-token x 256-column tile, and a CTA pair (cluster of two, tcgen05 MMAs spanning both
+SMs) per 256 x 256 tile. The pair kernel decides per 256-token tile whether the expand
+runs on the tensor cores (every adapter token of the 256 uses one adapter) or in each
+CTA's epilogue (the halves use different adapters, or a half is mixed); the cases below
+put each combination of halves in its own tile, with a d_out tail that leaves the second
+CTA's column half empty and a ragged last tile whose second half has no tokens.
+"""
+import numpy as np
+import pytest
+
+import lora_inputs as L
+import oracle
+from _helpers import assert_parity, assert_routing, load_pool, to_dev, to_host_f64
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+al = pytest.importorskip("adapter_linear_gb300")
+
+KERNELS = {"single": 1, "pair": 2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    al.load_library()
+    torch.cuda.set_device(0)
+
+
+def run(pool, prob, kernel):
+    pool.set_path(al.LORA_PATH_PREFILL)
+    pool.set_prefill_kernel(KERNELS[kernel])
+    Y = pool.linear(to_dev(prob.X), to_dev(prob.W), to_dev(prob.ids))
+    torch.cuda.synchronize()
+    assert pool.check_errors() == al.LORA_OK
+    return Y
+
+
+def tile_mode_problem():
+    d_in, d_out, seed = 136, 520, 61
+    T = 5 * 256 + 77
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d_in), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.1)
+    ranks = [5, 40, 13, 64]        # rank 64: two expand k-blocks
+    ads = {i: L.make_adapter(seed, i, d_in, d_out, r, 2.0 * r, std=0.2) for i, r in enumerate(ranks)}
+    g = L.rng_for(seed, L.ROLE_IDS)
+    ids = np.full(T, -1, np.int32)
+    ids[0:256] = 3                 # one adapter over both halves (tensor-core expand) ...
+    ids[40:44] = -1                # ... with base rows inside
+    ids[256:384] = 1               # halves with different adapters: epilogue expand
+    ids[384:512] = 2
+    ids[300] = -1
+    ids[512:640] = 0               # one adapter and a base-only half: tensor-core expand
+    ids[768:896] = -1              # a base-only half beside a mixed half
+    ids[896:1024] = g.integers(-1, 4, size=128)
+    ids[1024:1280] = -1            # all base
+    ids[1280:] = g.integers(-1, 4, size=T - 1280)   # mixed, ragged (second half empty)
+    return L.Problem("pair_tile_modes", d_in, d_out, X, W, ids, ads, 4, 64, seed)
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_tile_modes(kernel):
+    prob = tile_mode_problem()
+    pool = load_pool(al, prob)
+    got = to_host_f64(run(pool, prob, kernel))
+    ads = oracle.problem_adapters(prob)
+    ref = oracle.lora_linear(prob.X, prob.W, prob.ids, ads, prob.max_adapters)
+    base = oracle.lora_linear(prob.X, prob.W, np.full_like(prob.ids, -1), {}, prob.max_adapters)
+    assert_parity(got, ref, f"prefill tile modes ({kernel})")
+    assert_routing(got, ref, base, prob.ids, f"prefill tile modes ({kernel})")
+    pool.close()
+
+
+@pytest.mark.parametrize("T", [129, 255, 256, 257, 511, 640])
+def test_pair_ragged_token_counts(T):
+    """Token counts around the pair tile: a second half with a few rows, exactly one tile,
+    one row past it, and several tiles of random ids."""
+    d_in, d_out, seed = 72, 264, 67
+    X = L.normal_bf16(seed, L.ROLE_X, T, (T, d_in), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.1)
+    ranks = [8, 24, 3]
+    ads = {i: L.make_adapter(seed, i, d_in, d_out, r, 1.5 * r, std=0.2) for i, r in enumerate(ranks)}
+    ids = L.rng_for(seed, L.ROLE_IDS, T).integers(-1, len(ranks), size=T).astype(np.int32)
+    ids[: T // 2] = 1              # a single-adapter stretch as well
+    prob = L.Problem("pair_ragged", d_in, d_out, X, W, ids, ads, len(ranks), 24, seed)
+    pool = load_pool(al, prob)
+    got = to_host_f64(run(pool, prob, "pair"))
+    ref = oracle.lora_linear(prob.X, prob.W, prob.ids, oracle.problem_adapters(prob), prob.max_adapters)
+    assert_parity(got, ref, f"pair kernel T={T}")
+    pool.close()
+
+
+def test_kernels_agree_on_mixed_ranks():
+    """The benchmarked prefill workload (8 sequences x 2048 tokens, gate_proj, ranks
+    8..64): both kernels against the oracle on sampled rows, and against each other on
+    the whole output."""
+    prob = L.prefill_mixed()
+    pool = load_pool(al, prob)
+    Ys = run(pool, prob, "single").float()
+    Yp = run(pool, prob, "pair").float()
+    assert bool(torch.all((Yp - Ys).abs() <= 1e-2 + 1e-2 * Ys.abs()))
+    rows = np.array(sorted({s + o for s in range(0, prob.T, 2048) for o in (0, 1, 127, 128, 255, 256, 1024, 2047)}))
+    ads = oracle.problem_adapters(prob)
+    ref = oracle.lora_linear(prob.X[rows], prob.W, prob.ids[rows], ads, prob.max_adapters)
+    assert_parity(to_host_f64(Yp[torch.from_numpy(rows).cuda()]), ref, "pair kernel, sampled rows")
+    pool.close()
+
+
+def test_prefill_kernel_setter():
+    prob = L.tiny()
+    pool = load_pool(al, prob)
+    for bad in (-1, 3):
+        assert al.lora_pool_set_prefill_kernel(pool.handle, bad) == al.LORA_ERR_ARG
+    # T <= 128 under AUTO takes the single-CTA kernel; PAIR forced runs the pair kernel
+    # on a tile whose second half is empty
+    for kernel in ("single", "pair"):
+        got = to_host_f64(run(pool, prob, kernel))
+        ref = oracle.lora_linear(prob.X, prob.W, prob.ids, oracle.problem_adapters(prob), prob.max_adapters)
+        assert_parity(got, ref, f"tiny, {kernel} kernel")
+    pool.set_prefill_kernel(al.LORA_PREFILL_AUTO)
+    pool.close()
