@@ -200,6 +200,14 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
         : "memory");
 }
 
+// Request the box at (x, y) into L2 only (no shared memory, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x),
+                 "r"(y)
+                 : "memory");
+}
+
 // 2-D tiled store of the box at (x = inner coordinate, y = row) from shared memory
 // (parts of the box outside the tensor are not written), as one bulk async-group.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *smem_src, int x, int y)

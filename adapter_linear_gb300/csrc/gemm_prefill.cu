@@ -466,6 +466,24 @@ __device__ __forceinline__ TileLora pair_tile_lora(int m, uint32_t rank, const P
     return r;
 }
 
+// A pair tile's coordinates and adapter use; each role loads the next tile's while the
+// current one runs, so the dependent table loads stay off the tile boundary.
+struct PairTile {
+    int m, n;
+    TileLora tl;
+    bool own;
+};
+
+__device__ __forceinline__ PairTile pair_tile(int tile, int tiles, uint32_t rank, const PrefillArgs &a,
+                                              const PoolDev &pool)
+{
+    PairTile r{0, 0, TileLora{0, -1, 0, 0, nullptr}, false};
+    if (tile >= tiles) return r;
+    pair_tile_coords(tile, a, r.m, r.n);
+    r.tl = pair_tile_lora(r.m, rank, a, pool, r.own);
+    return r;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_pair_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
@@ -523,14 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             int it = 0;
             bool ok = true;
+            PairTile cur = pair_tile(cluster, tiles, rank, a, pool);
             for (int tile = cluster; tile < tiles && ok; tile += clusters) {
-                int m, n;
-                pair_tile_coords(tile, a, m, n);
-                bool own;
-                const TileLora tl = pair_tile_lora(m, rank, a, pool, own);
+                const PairTile nxt = pair_tile(tile + clusters, tiles, rank, a, pool);
+                const TileLora &tl = cur.tl;
                 const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
-                const int n0 = n * kBN + (int)rank * 128;   // this CTA's W rows / B columns
-                const int r0 = m * kPBM + (int)rank * 128;  // this CTA's token rows
+                const int n0 = cur.n * kBN + (int)rank * 128;   // this CTA's W rows / B columns
+                const int r0 = cur.m * kPBM + (int)rank * 128;  // this CTA's token rows
                 for (int kb = 0; kb < steps; ++kb, ++it) {
                     const int s = it % kPStages;
                     ok = mbar_wait_cluster(&empty[s], ((uint32_t)(it / kPStages) & 1u) ^ 1u, &abort_flag,
@@ -555,6 +572,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
+                cur = nxt;
             }
             // CTA 0's stage barriers count both CTAs' copies: do not leave while any is
             // in flight
@@ -571,12 +589,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_bf16_f32(kPBM, kBN);
             int it = 0, tc = 0;
             bool ok = true;
+            PairTile cur = pair_tile(cluster, tiles, rank, a, pool);
             for (int tile = cluster; tile < tiles && ok; tile += clusters, ++tc) {
-                int m, n;
-                pair_tile_coords(tile, a, m, n);
-                bool own;
-                const TileLora tl = pair_tile_lora(m, rank, a, pool, own);
-                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
+                const PairTile nxt = pair_tile(tile + clusters, tiles, rank, a, pool);
+                const int steps = a.KB + (cur.tl.mode == 1 ? cur.tl.blocks : 0);
                 const int buf = tc & 1;
                 ok = mbar_wait_cluster(&acc_empty[buf], ((uint32_t)(tc >> 1) & 1u) ^ 1u, &abort_flag, a.err);
                 if (!ok) break;
@@ -604,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_commit_pair(&empty[s], 0x3);
                 }
                 if (ok) mma_commit_pair(&acc_full[buf], 0x3);
+                cur = nxt;
             }
             mma_commit_pair(drain, 0x1);
             int dummy = 0;
@@ -615,11 +632,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3, half = warp >> 2;
         const uint32_t release = 0;  // CTA 0 holds the accumulator barriers' empty side
         int tc = 0;
+        PairTile cur = pair_tile(cluster, tiles, rank, a, pool);
         for (int tile = cluster; tile < tiles; tile += clusters, ++tc) {
-            int m, n;
-            pair_tile_coords(tile, a, m, n);
-            bool own;
-            pair_tile_lora(m, rank, a, pool, own);
+            const PairTile t = cur;
+            cur = pair_tile(tile + clusters, tiles, rank, a, pool);
+            const int m = t.m, n = t.n;
+            const bool own = t.own;
             const int buf = tc & 1;
             bool ok = true;
             if (lane == 0)

@@ -71,7 +71,7 @@ struct PoolDev {
 
 // ------------------------------------------------------------------ launchers
 
-size_t seg_build_smem_bytes(int max_adapters);
+size_t seg_build_smem_bytes(int max_adapters, int warps);
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
                              int *err, cudaStream_t stream);
 

@@ -4,7 +4,8 @@
 //
 // One CTA performs a stable counting sort of the token indices by adapter id.
 // Key = id + 1 (key 0 collects the base-only tokens and any invalid id, so
-// they come first). The tokens are cut into 8 contiguous chunks, one per warp:
+// they come first). The tokens are cut into W contiguous chunks, one per warp
+// (W = 32 when the per-(key, warp) counters fit in shared memory, else 8):
 //   A. each warp counts its chunk per key (warp match, leader adds);
 //   B. per-key warp prefixes + one block-wide exclusive scan over keys give
 //      every (key, warp) its first output position, and every present key
@@ -18,8 +19,6 @@ namespace lora {
 
 namespace {
 
-constexpr int kSegThreads = 256;
-constexpr int kSegWarps = kSegThreads / 32;
 constexpr size_t kSegSmemLimit = 200 * 1024;
 
 __device__ __forceinline__ uint32_t lanemask_lt()
@@ -38,10 +37,12 @@ __device__ __forceinline__ int token_key(int id, const PoolDev &pool, bool &bad)
     return 0;
 }
 
-__global__ void __launch_bounds__(kSegThreads, 1)
+template <int kSegWarps>
+__global__ void __launch_bounds__(kSegWarps * 32, 1)
     seg_build_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
                      int *__restrict__ err, int cache_keys)
 {
+    constexpr int kSegThreads = kSegWarps * 32;
     extern __shared__ uint32_t seg_smem[];
     const int K = pool.max_adapters + 1;
     uint32_t *cnt = seg_smem;                          // [K][kSegWarps]
@@ -199,22 +200,37 @@ __global__ void __launch_bounds__(kSegThreads, 1)
 
 }  // namespace
 
-size_t seg_build_smem_bytes(int max_adapters)
+size_t seg_build_smem_bytes(int max_adapters, int warps)
 {
     const size_t K = (size_t)max_adapters + 1;
-    return K * kSegWarps * sizeof(uint32_t) + K * sizeof(uint32_t);
+    return K * warps * sizeof(uint32_t) + K * sizeof(uint32_t);
 }
 
+namespace {
+
+template <int W>
+cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs, int *err,
+                               cudaStream_t stream)
+{
+    size_t smem = seg_build_smem_bytes(pool.max_adapters, W);
+    const int cache_keys = smem + (size_t)T * sizeof(int) <= kSegSmemLimit;
+    if (cache_keys) smem += (size_t)T * sizeof(int);
+    cudaError_t e = ensure_smem_attr((const void *)seg_build_kernel<W>, smem);
+    if (e != cudaSuccess) return e;
+    seg_build_kernel<W><<<1, W * 32, smem, stream>>>(ids, T, pool, tabs, err, cache_keys);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+// 32 warps (each walks a 32nd of the tokens) when their counters and the cached keys
+// fit in shared memory; 8 warps otherwise (large pools).
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
                              int *err, cudaStream_t stream)
 {
-    size_t smem = seg_build_smem_bytes(pool.max_adapters);
-    const int cache_keys = smem + (size_t)T * sizeof(int) <= kSegSmemLimit;
-    if (cache_keys) smem += (size_t)T * sizeof(int);
-    cudaError_t e = ensure_smem_attr((const void *)seg_build_kernel, smem);
-    if (e != cudaSuccess) return e;
-    seg_build_kernel<<<1, kSegThreads, smem, stream>>>(ids, T, pool, tabs, err, cache_keys);
-    return cudaGetLastError();
+    if (seg_build_smem_bytes(pool.max_adapters, 32) + (size_t)T * sizeof(int) <= kSegSmemLimit)
+        return launch_seg_build_w<32>(ids, T, pool, tabs, err, stream);
+    return launch_seg_build_w<8>(ids, T, pool, tabs, err, stream);
 }
 
 }  // namespace lora
