@@ -411,8 +411,10 @@ __device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quar
 
 constexpr int kPBM = 256;                     // tokens per pair tile (128 per CTA)
 constexpr int kPHalfBytes = 128 * kBK * 2;    // 16 KB: one CTA's X or W half of a k-block
-constexpr int kPStageBytes = 2 * kPHalfBytes;
-constexpr int kPStages = 6;
+constexpr int kPBlockBytes = 2 * kPHalfBytes;  // one k-block of one CTA: X half + W half
+constexpr int kPKps = 2;                       // k-blocks per pipeline stage
+constexpr int kPStageBytes = kPKps * kPBlockBytes;
+constexpr int kPStages = 3;
 constexpr int kPGroupM = 8;                   // 8 x 256 tokens share one column sweep
 constexpr int kPSliceBytes = 128 * 16;        // 128 columns x 8 rank values of one page
 constexpr int kPYStageBytes = 32 * 128;       // one epilogue warp's 32 x 64 bf16 staging tile
@@ -545,30 +547,38 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int tile = cluster; tile < tiles && ok; tile += clusters) {
                 const PairTile nxt = pair_tile(tile + clusters, tiles, rank, a, pool);
                 const TileLora &tl = cur.tl;
-                const int steps = a.KB + (tl.mode == 1 ? tl.blocks : 0);
+                const int ne = tl.mode == 1 ? tl.blocks : 0;
+                const int sb = (a.KB + kPKps - 1) / kPKps, steps = sb + (ne + kPKps - 1) / kPKps;
                 const int n0 = cur.n * kBN + (int)rank * 128;   // this CTA's W rows / B columns
                 const int r0 = cur.m * kPBM + (int)rank * 128;  // this CTA's token rows
-                for (int kb = 0; kb < steps; ++kb, ++it) {
+                for (int st = 0; st < steps; ++st, ++it) {
                     const int s = it % kPStages;
                     ok = mbar_wait_cluster(&empty[s], ((uint32_t)(it / kPStages) & 1u) ^ 1u, &abort_flag,
                                            a.err);
                     if (!ok) break;
                     const uint32_t fb = cluster_map(&full[s], 0);
                     uint8_t *xs = smem + (size_t)s * kPStageBytes;
-                    if (kb < a.KB) {
-                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * kPStageBytes);
-                        tma_load_2d_pair(xs, &tmX, fb, kb * kBK, r0);
-                        tma_load_2d_pair(xs + kPHalfBytes, &tmW, fb, kb * kBK, n0);
+                    if (st < sb) {
+                        const int k0 = st * kPKps, nk = min(kPKps, a.KB - k0);
+                        if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * nk * kPBlockBytes);
+                        for (int j = 0; j < nk; ++j) {
+                            tma_load_2d_pair(xs + j * kPBlockBytes, &tmX, fb, (k0 + j) * kBK, r0);
+                            tma_load_2d_pair(xs + j * kPBlockBytes + kPHalfBytes, &tmW, fb, (k0 + j) * kBK, n0);
+                        }
                     } else {
-                        const int e = kb - a.KB;
+                        const int e0 = (st - sb) * kPKps, nj = min(kPKps, ne - e0);
                         if (rank == 0)
-                            mbar_arrive_expect_tx(&full[s], 2 * (kPHalfBytes + kPagesPerBlock * kPSliceBytes));
-                        tma_load_2d_pair(xs, &tmV, fb, e * 64, r0);
-                        for (int i = 0; i < kPagesPerBlock; ++i) {
-                            const int q = e * kPagesPerBlock + i;
-                            const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
-                            tma_load_2d_pair(xs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
-                                             page * a.d_out + n0);
+                            mbar_arrive_expect_tx(&full[s], 2 * nj * (kPHalfBytes + kPagesPerBlock * kPSliceBytes));
+                        for (int j = 0; j < nj; ++j) {
+                            const int e = e0 + j;
+                            uint8_t *bs = xs + j * kPBlockBytes;
+                            tma_load_2d_pair(bs, &tmV, fb, e * 64, r0);
+                            for (int i = 0; i < kPagesPerBlock; ++i) {
+                                const int q = e * kPagesPerBlock + i;
+                                const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
+                                tma_load_2d_pair(bs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
+                                                 page * a.d_out + n0);
+                            }
                         }
                     }
                 }
@@ -592,30 +602,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             PairTile cur = pair_tile(cluster, tiles, rank, a, pool);
             for (int tile = cluster; tile < tiles && ok; tile += clusters, ++tc) {
                 const PairTile nxt = pair_tile(tile + clusters, tiles, rank, a, pool);
-                const int steps = a.KB + (cur.tl.mode == 1 ? cur.tl.blocks : 0);
+                const int ne = cur.tl.mode == 1 ? cur.tl.blocks : 0;
+                const int sb = (a.KB + kPKps - 1) / kPKps, steps = sb + (ne + kPKps - 1) / kPKps;
                 const int buf = tc & 1;
                 ok = mbar_wait_cluster(&acc_empty[buf], ((uint32_t)(tc >> 1) & 1u) ^ 1u, &abort_flag, a.err);
                 if (!ok) break;
                 tc_fence_after_sync();
                 const uint32_t d = tmem + (uint32_t)(buf * kBN);
-                for (int kb = 0; kb < steps; ++kb, ++it) {
+                for (int st = 0; st < steps; ++st, ++it) {
                     const int s = it % kPStages;
                     ok = mbar_wait_cluster(&full[s], (uint32_t)(it / kPStages) & 1u, &abort_flag, a.err);
                     if (!ok) break;
                     tc_fence_after_sync();
-                    const uint32_t xa = smem_u32(smem + (size_t)s * kPStageBytes);
-                    const uint32_t wa = xa + kPHalfBytes;
-                    if (kb < a.KB) {
+                    const uint32_t sa = smem_u32(smem + (size_t)s * kPStageBytes);
+                    if (st < sb) {
+                        const int nk = min(kPKps, a.KB - st * kPKps);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32), idesc,
-                                             (kb | kk) != 0);
+                        for (int j = 0; j < kPKps; ++j) {
+                            if (j >= nk) break;
+                            const uint32_t xa = sa + j * kPBlockBytes, wa = xa + kPHalfBytes;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32), sdesc_k_sw128(wa + kk * 32),
+                                                 idesc, (st | j | kk) != 0);
+                        }
                     } else {
+                        const int nj = min(kPKps, ne - (st - sb) * kPKps);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32),
-                                             sdesc_k_none(wa + (kk & 1) * 2 * kPSliceBytes, kPSliceBytes, 128),
-                                             idesc, 1u);
+                        for (int j = 0; j < kPKps; ++j) {
+                            if (j >= nj) break;
+                            const uint32_t xa = sa + j * kPBlockBytes, wa = xa + kPHalfBytes;
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32),
+                                                 sdesc_k_none(wa + (kk & 1) * 2 * kPSliceBytes, kPSliceBytes, 128),
+                                                 idesc, 1u);
+                        }
                     }
                     mma_commit_pair(&empty[s], 0x3);
                 }
