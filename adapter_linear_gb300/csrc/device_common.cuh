@@ -181,13 +181,6 @@ __device__ __forceinline__ uint64_t policy_evict_first()
     return p;
 }
 
-__device__ __forceinline__ uint64_t policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of 16),
 // completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint32_t bytes,
@@ -198,14 +191,6 @@ __device__ __forceinline__ void bulk_load(void *smem_dst, const void *gsrc, uint
             smem_u32(smem_dst)),
         "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
-}
-
-// Request the box at (x, y) into L2 only (no shared memory, nothing to wait for).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y)
-{
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(map), "r"(x),
-                 "r"(y)
-                 : "memory");
 }
 
 // 2-D tiled store of the box at (x = inner coordinate, y = row) from shared memory
