@@ -574,7 +574,9 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
 // exceeds the SMs and a CTA's shrink pairs read at most half as many bytes as its
 // share of W (the "tight" plans; measured faster for q_proj T = 64, gate_proj
 // T = 32 and the grouped 7-module layer; slower for T = 32 layers whose finishing
-// grid fits the SMs and for T = 256 with ~4 shrink pairs per CTA).
+// grid fits the SMs and for T = 256 with ~4 shrink pairs per CTA). The unbounded
+// finishing pass is still held to three CTAs per SM (168 registers): at 180 its
+// residency fell to two and T = 256 took 38 instead of 34.6 us a step.
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
