@@ -39,7 +39,7 @@ EXPORTS = (
     "lora_status_string", "lora_abi_version", "lora_pool_enable_timing", "lora_pool_kernel_times",
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
-    "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info",
+    "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info", "lora_test_delayed_copy",
 )
 PLAN_INFO_FIELDS = ("units", "G", "grid", "max_seg", "n_acc", "stages", "tmem_cols", "smem_bytes",
                     "pairs", "col_blocks", "tight", "ntok", "partials_floats", "prefetch_a")
@@ -101,6 +101,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_cache_stats": [vp, vp],
         "lora_pool_selftest_wait": [vp, i32, vp],
         "lora_decode_plan_info": [i32, i32, vp, vp, vp, i32, vp],
+        "lora_test_delayed_copy": [vp, vp, i32, i32, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -167,6 +168,13 @@ def lora_linear(pool: int, X, W_base, ids, T: int, Y, stream=None) -> int:
 def lora_linear_host(pool: int, X_host, W_base, ids_host, T: int, Y_host, stream=None) -> int:
     return load_library().lora_linear_host(pool, _ptr(X_host), _ptr(W_base), _ptr(ids_host), T,
                                            _ptr(Y_host), _stream(stream))
+
+
+def delayed_copy(src, dst, n: int, delay_us: int, stream=None):
+    """Stream-order test hook: copy n int32 src -> dst (device tensors) after delay_us,
+    letting the next kernel in the stream launch at once."""
+    _check(load_library().lora_test_delayed_copy(_ptr(src), _ptr(dst), n, delay_us, _stream(stream)),
+           "lora_test_delayed_copy")
 
 
 def decode_plan_info(T: int, d_in, d_out, max_pages, num_sms: int = 152) -> Dict[str, int]:

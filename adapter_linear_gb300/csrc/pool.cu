@@ -197,6 +197,21 @@ __global__ void wait_selftest_kernel(int *err, uint64_t limit_ns)
     __syncthreads();
 }
 
+// A producer of the kind that programmatic dependent launch allows: it lets the next
+// kernel in the stream start at once, then, after `delay_ns`, writes dst. Anything
+// that reads dst before its own wait on this kernel sees the old values.
+__global__ void delayed_copy_kernel(const int32_t *src, int32_t *dst, int n, uint64_t delay_ns)
+{
+    pdl_launch_dependents();
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        while (global_timer_ns() - t0 < delay_ns) {
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) dst[i] = src[i];
+}
+
 // Split-K partials of a grouped decode call (held by its first pool): grown on
 // first use of a larger group, like the rest of the scratch.
 lora_status ensure_partials(lora_pool *p, size_t floats)
@@ -679,6 +694,14 @@ lora_status lora_pool_selftest_wait(lora_pool_t p, int limit_us, lora_stream_t s
 {
     if (!p || limit_us < 1 || limit_us > 2000000) return LORA_ERR_ARG;
     wait_selftest_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(p->d_err, (uint64_t)limit_us * 1000ull);
+    CUDA_TRY(cudaGetLastError());
+    return LORA_OK;
+}
+
+lora_status lora_test_delayed_copy(const int32_t *src, int32_t *dst, int n, int delay_us, lora_stream_t stream)
+{
+    if (!src || !dst || n < 0 || delay_us < 1 || delay_us > 100000) return LORA_ERR_ARG;
+    delayed_copy_kernel<<<1, 256, 0, (cudaStream_t)stream>>>(src, dst, n, (uint64_t)delay_us * 1000ull);
     CUDA_TRY(cudaGetLastError());
     return LORA_OK;
 }

@@ -362,6 +362,18 @@ lora_status lora_decode_plan_info(int n, int T, const int *d_in, const int *d_ou
 lora_status lora_pool_selftest_wait(lora_pool_t pool, int limit_us, lora_stream_t stream);
 
 /*
+ * Test hook for stream order (no counterpart in the pages): one kernel that lets
+ * the next kernel in the stream launch at once (programmatic dependent launch) and
+ * only after delay_us microseconds (1..100,000) copies n int32 from src to dst (both
+ * DEVICE pointers). A lora_linear enqueued right after it with dst as its ids must
+ * still use the copied ids: its kernels may start early, but read stream-ordered
+ * data only after their wait on the kernel before them. Asynchronous on `stream`.
+ * Errors: ARG, CUDA.
+ */
+lora_status lora_test_delayed_copy(const int32_t *src, int32_t *dst, int n, int delay_us,
+                                   lora_stream_t stream);
+
+/*
  * Test hook: run only the segment builder on device ids[T] and copy its
  * tables out (device pointers): order[T] (token indices stably sorted by id,
  * base-only tokens first), *n_base, *num_seg, seg_start[num_seg + 1] (offsets
