@@ -185,6 +185,13 @@ lora_status lora_define_chain(lora_pool_t pool, int chain_slot, const int *membe
  *   once; must not alias X or W_base).  T >= 0 (T == 0 does nothing).
  * Asynchronous: enqueued on `stream`, returns without waiting. X, W_base and
  * the ids must stay valid until the stream reaches the call.
+ * Stream order: the decode kernels are launched with programmatic dependent
+ * launch and may start while the kernel before them in the stream still runs.
+ * X, the ids, Y and the pool's state are used in stream order; W_base, being a
+ * weight, is already read before that wait. A kernel that writes W_base must
+ * therefore not be the one directly before the call when it lets dependent
+ * kernels launch early (griddepcontrol.launch_dependents) before writing it;
+ * a copy, an event wait or any ordinary kernel in between keeps the order.
  * Ids that are neither -1 nor a loaded slot do not fall back silently (the
  * icman.com.cn article's section 4.1, strict mode): the kernels set the
  * pool's device error word, and the next lora_pool_check_errors returns
