@@ -99,7 +99,7 @@ def algorithmic_flops(p):
 
 class NvmlClockSampler:
     """SM clock and clock-event reasons read through NVML (read-only queries) every
-    millisecond while the timed region runs."""
+    half millisecond while the timed region runs."""
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
@@ -135,7 +135,7 @@ class NvmlClockSampler:
             if self.nv.nvmlDeviceGetClockInfo(self.h, 1, c.byref(mhz)) == 0 and \
                     self.reason_fn(self.h, c.byref(reasons)) == 0:
                 self.samples.append((float(mhz.value), int(reasons.value)))
-            time.sleep(0.001)
+            time.sleep(0.0005)
 
     def __enter__(self):
         if self.ok:
@@ -629,7 +629,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    # 1000 q_proj decode steps are ~16 ms of timed work: enough for a clock record
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="q_proj_decode")
