@@ -121,3 +121,28 @@ def test_prefill_kernel_setter():
         assert_parity(got, ref, f"tiny, {kernel} kernel")
     pool.set_prefill_kernel(al.LORA_PREFILL_AUTO)
     pool.close()
+
+
+def test_pair_random_shapes():
+    """Seeded random shapes (d_in, d_out multiples of 8 that are not multiples of the
+    tiles; T past one pair tile), ranks and id mixes, each against the oracle."""
+    g = np.random.default_rng(97)
+    for case in range(12):
+        d_in = int(8 * g.integers(1, 160))
+        d_out = int(8 * g.integers(1, 200))
+        T = int(g.integers(129, 1400))
+        n_ad = int(g.integers(1, 6))
+        ranks = [int(r) for r in g.integers(1, 65, size=n_ad)]
+        seed = 200 + case
+        X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d_in), 1.0)
+        W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.1)
+        ads = {i: L.make_adapter(seed, i, d_in, d_out, r, 2.0 * r, std=0.1) for i, r in enumerate(ranks)}
+        ids = g.integers(-1, n_ad, size=T).astype(np.int32)
+        if case % 3 == 0:              # long single-adapter runs (tensor-core expand)
+            ids = np.repeat(g.integers(-1, n_ad, size=-(-T // 300)), 300)[:T].astype(np.int32)
+        prob = L.Problem("pair_random", d_in, d_out, X, W, ids, ads, n_ad, max(ranks), seed)
+        pool = load_pool(al, prob)
+        got = to_host_f64(run(pool, prob, "pair"))
+        ref = oracle.lora_linear(X, W, ids, oracle.problem_adapters(prob), prob.max_adapters)
+        assert_parity(got, ref, f"pair kernel, case {case}: T={T} {d_in}->{d_out} ranks {ranks}")
+        pool.close()
