@@ -507,6 +507,19 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     }
     if (!col_ok) return;
 
+    // One round of loads first: the V values of the pages whose B words are already in
+    // registers, the first contributor's partial and the next kFinishBatch ones; the
+    // sums and the expand follow in the same order as before (partials in CTA order,
+    // then the pages), so the loads of V no longer wait for the partial sums.
+    const float *vrow = pr.V + (size_t)t * pr.ldv;
+    const int q_early = (LORA && early) ? (np < kPrefetchPages ? np : kPrefetchPages) : 0;
+    float4 vq[kPrefetchPages][2];
+#pragma unroll
+    for (int q = 0; q < kPrefetchPages; ++q)
+        if (q < q_early) {
+            vq[q][0] = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
+            vq[q][1] = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
+        }
     float acc[kFinishCols];
     {
         const float *src = partials + (((size_t)c_lo * p.max_seg + seg_lo) * p.T + t) * 128 + nl;
@@ -535,17 +548,20 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
                 acc[4] += v[i][1].x; acc[5] += v[i][1].y; acc[6] += v[i][1].z; acc[7] += v[i][1].w;
             }
     }
-    const float *vrow = pr.V + (size_t)t * pr.ldv;
-    for (int q = 0; q < np; ++q) {
+#pragma unroll
+    for (int q = 0; q < kPrefetchPages; ++q)
+        if (q < q_early) {
+            const float v[8] = {vq[q][0].x, vq[q][0].y, vq[q][0].z, vq[q][0].w,
+                                vq[q][1].x, vq[q][1].y, vq[q][1].z, vq[q][1].w};
+            expand8(acc, v, b[q]);
+        }
+    for (int q = q_early; q < np; ++q) {
         float v[8];
         const float4 v0 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
         const float4 v1 = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
         v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
         v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
-        if (q < kPrefetchPages && early) {
-            if (q == 0) expand8(acc, v, b[0]);
-            else expand8(acc, v, b[1]);
-        } else {
+        {
             uint4 bq[8];
             const uint16_t *bsrc = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
 #pragma unroll
