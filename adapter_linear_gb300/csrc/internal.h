@@ -72,8 +72,9 @@ struct PoolDev {
 // ------------------------------------------------------------------ launchers
 
 size_t seg_build_smem_bytes(int max_adapters, int warps);
+// vhl != nullptr: also zero the rows [ldh] of vhl of tokens without an adapter.
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
-                             int *err, cudaStream_t stream);
+                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream);
 
 // Prefill shrink (tcgen05), 128-token units per segment: writes s_i X[t,:] A_i as
 // bf16 hi/lo pairs grouped per 32 rank columns (see shrink.cu) into Vhl [T][ldh].

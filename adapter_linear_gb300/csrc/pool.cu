@@ -316,7 +316,8 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         st = run_decode(pools, 1, &X, &W, ids, T, &Y, stream, with_lora, marks);
         if (st != LORA_OK) return st;
     } else {
-        if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, stream));
+        // the segment tables; rows of the shrink output of tokens without an adapter zeroed
+        if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, p->Vhl, p->ldh, stream));
         if (!mark(0)) return LORA_ERR_CUDA;
         const bool pair = p->pair_ok && (p->prefill_kernel == LORA_PREFILL_PAIR ||
                                          (p->prefill_kernel == LORA_PREFILL_AUTO && T > 128));
@@ -326,8 +327,6 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         const CUtensorMap *tmY = pair ? tmap_for(p, Y, p->d_out, T, 64, 32) : nullptr;
         if (!tmW || !tmX || !tmV || (pair && !tmY)) return LORA_ERR_ARG;
         if (with_lora) {
-            // rows of tokens without an adapter must read as zero in the expand
-            CUDA_TRY(cudaMemsetAsync(p->Vhl, 0, sizeof(uint16_t) * (size_t)T * p->ldh, stream));
             CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
                                       p->d_err, stream));
         }
@@ -735,7 +734,7 @@ lora_status lora_build_segments(lora_pool_t p, const int32_t *ids, int T, int32_
     lora_status st = ensure_scratch(p, T);
     if (st != LORA_OK) return st;
     const SegTables tabs = seg_tables(p);
-    CUDA_TRY(launch_seg_build(ids, T, pool_view(p), tabs, p->d_err, s));
+    CUDA_TRY(launch_seg_build(ids, T, pool_view(p), tabs, p->d_err, nullptr, 0, s));
     const size_t se = seg_entries(p, T);
     CUDA_TRY(cudaMemcpyAsync(order, p->order, sizeof(int32_t) * T, cudaMemcpyDeviceToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(n_base, p->hdr + HDR_NBASE, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));

@@ -40,7 +40,7 @@ __device__ __forceinline__ int token_key(int id, const PoolDev &pool, bool &bad)
 template <int kSegWarps>
 __global__ void __launch_bounds__(kSegWarps * 32, 1)
     seg_build_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
-                     int *__restrict__ err, int cache_keys)
+                     int *__restrict__ err, int cache_keys, uint16_t *__restrict__ vhl, int ldh)
 {
     constexpr int kSegThreads = kSegWarps * 32;
     extern __shared__ uint32_t seg_smem[];
@@ -63,12 +63,17 @@ __global__ void __launch_bounds__(kSegWarps * 32, 1)
     const int chunk = (T + kSegWarps - 1) / kSegWarps;
     const int t0 = min(T, warp * chunk), t1 = min(T, t0 + chunk);
 
-    // ---- A: per-warp counts
+    // ---- A: per-warp counts; the shrink output rows of tokens without an adapter are
+    // zeroed here (the prefill expand reads them inside single-adapter tiles)
     for (int base = t0; base < t1; base += 32) {
         const int t = base + lane;
         const bool valid = t < t1;
         int key = 0;
         if (valid) key = cache_keys ? keys[t] : token_key(ids[t], pool, bad);
+        if (valid && key == 0 && vhl != nullptr) {
+            uint4 *row = reinterpret_cast<uint4 *>(vhl + (size_t)t * ldh);
+            for (int i = 0; i < ldh / 8; ++i) row[i] = make_uint4(0, 0, 0, 0);
+        }
         const unsigned active = __ballot_sync(0xffffffffu, valid);
         if (valid) {
             const unsigned same = __match_any_sync(active, key);
@@ -210,14 +215,14 @@ namespace {
 
 template <int W>
 cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs, int *err,
-                               cudaStream_t stream)
+                               uint16_t *vhl, int ldh, cudaStream_t stream)
 {
     size_t smem = seg_build_smem_bytes(pool.max_adapters, W);
     const int cache_keys = smem + (size_t)T * sizeof(int) <= kSegSmemLimit;
     if (cache_keys) smem += (size_t)T * sizeof(int);
     cudaError_t e = ensure_smem_attr((const void *)seg_build_kernel<W>, smem);
     if (e != cudaSuccess) return e;
-    seg_build_kernel<W><<<1, W * 32, smem, stream>>>(ids, T, pool, tabs, err, cache_keys);
+    seg_build_kernel<W><<<1, W * 32, smem, stream>>>(ids, T, pool, tabs, err, cache_keys, vhl, ldh);
     return cudaGetLastError();
 }
 
@@ -226,11 +231,11 @@ cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, S
 // 32 warps (each walks a 32nd of the tokens) when their counters and the cached keys
 // fit in shared memory; 8 warps otherwise (large pools).
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
-                             int *err, cudaStream_t stream)
+                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream)
 {
     if (seg_build_smem_bytes(pool.max_adapters, 32) + (size_t)T * sizeof(int) <= kSegSmemLimit)
-        return launch_seg_build_w<32>(ids, T, pool, tabs, err, stream);
-    return launch_seg_build_w<8>(ids, T, pool, tabs, err, stream);
+        return launch_seg_build_w<32>(ids, T, pool, tabs, err, vhl, ldh, stream);
+    return launch_seg_build_w<8>(ids, T, pool, tabs, err, vhl, ldh, stream);
 }
 
 }  // namespace lora

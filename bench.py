@@ -62,6 +62,10 @@ def workload(name: str):
         p = L.prefill_mixed()
         return p, {"workload": "gate_proj prefill, 8x2048 tokens, ranks 8..64", "T": 16384,
                    "d_in": 4096, "d_out": 14336, "adapters": 8, "rank": "8,8,16,16,32,32,64,64"}
+    if name == "prefill_r16":  # the same prefill with every adapter at rank 16 (alpha 32)
+        p = L.prefill_mixed(ranks=[16])
+        return p, {"workload": "gate_proj prefill, 8x2048 tokens, rank 16", "T": 16384,
+                   "d_in": 4096, "d_out": 14336, "adapters": 8, "rank": 16, "alpha": 32}
     if name == "prefill_small":  # same kernels and ranks, 8 x 512 tokens (for profiling)
         p = L.prefill_mixed(seq_len=512)
         return p, {"workload": "gate_proj prefill, 8x512 tokens, ranks 8..64", "T": 4096,

@@ -178,18 +178,20 @@ PREFILL_RANKS = [8, 8, 16, 16, 32, 32, 64, 64]
 
 
 def prefill_mixed(seed: int = 3, seq_len: int = 2048, n_seq: int = 8, d_in: int = 4096,
-                  d_out: int = 14336, padded: bool = False) -> Problem:
+                  d_out: int = 14336, padded: bool = False, ranks=None) -> Problem:
+    """ranks: the adapters' ranks in turn (default PREFILL_RANKS); alpha = 2 * rank."""
+    ranks = PREFILL_RANKS if ranks is None else ranks
     T = seq_len * n_seq
     X = normal_bf16(seed, ROLE_X, 0, (T, d_in), 1.0)
     W = normal_bf16(seed, ROLE_W, 0, (d_out, d_in), 1.0 / 64)
     ids = np.repeat(np.arange(n_seq, dtype=np.int32), seq_len)
     ads = {}
     for i in range(n_seq):
-        r = PREFILL_RANKS[i % len(PREFILL_RANKS)]
+        r = ranks[i % len(ranks)]
         ad = make_adapter(seed, i, d_in, d_out, r, 2.0 * r)
         ads[i] = pad_adapter(ad, 64) if padded else ad
     return Problem("prefill_mixed" + ("_padded" if padded else ""), d_in, d_out, X, W, ids,
-                   ads, max_adapters=n_seq, max_rank=64, seed=seed)
+                   ads, max_adapters=n_seq, max_rank=max(64 if padded else 0, max(ranks)), seed=seed)
 
 
 @dataclasses.dataclass

@@ -146,3 +146,30 @@ def test_pair_random_shapes():
         ref = oracle.lora_linear(X, W, ids, oracle.problem_adapters(prob), prob.max_adapters)
         assert_parity(got, ref, f"pair kernel, case {case}: T={T} {d_in}->{d_out} ranks {ranks}")
         pool.close()
+
+
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_shrink_rows_left_by_an_earlier_call(kernel):
+    """The shrink output is not cleared between calls: a row of a token without an
+    adapter is zeroed by the segment builder, and the columns past an adapter's own
+    32-column groups are never read. Call 1 writes every row at rank 64; call 2 puts
+    base-only tokens (and a rank-8 adapter) where those rows were."""
+    d_in, d_out, seed, T = 136, 264, 83, 512
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d_in), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d_out, d_in), 0.1)
+    ads = {0: L.make_adapter(seed, 0, d_in, d_out, 64, 128.0, std=0.2),
+           1: L.make_adapter(seed, 1, d_in, d_out, 8, 16.0, std=0.2)}
+    ids1 = np.zeros(T, np.int32)                       # every row at rank 64
+    ids2 = np.full(T, 1, np.int32)
+    ids2[3:40] = -1                                    # base rows inside single-adapter tiles
+    ids2[300:310] = -1
+    ids2[384:] = -1                                    # a base-only tile
+    pool = None
+    for ids in (ids1, ids2):
+        prob = L.Problem("stale_rows", d_in, d_out, X, W, ids, ads, 2, 64, seed)
+        if pool is None:
+            pool = load_pool(al, prob)
+        got = to_host_f64(run(pool, prob, kernel))
+        ref = oracle.lora_linear(X, W, ids, oracle.problem_adapters(prob), prob.max_adapters)
+        assert_parity(got, ref, f"rows left by an earlier call ({kernel})")
+    pool.close()
