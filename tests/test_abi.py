@@ -58,6 +58,8 @@ def test_null_handles_are_rejected_on_the_host(lib):
     assert lib.lora_base_linear(None, None, None, 4, None, None) == al.LORA_ERR_ARG
     assert lib.lora_linear_host(None, None, None, None, 4, None, None) == al.LORA_ERR_ARG
     assert lib.lora_pool_check_errors(None) == al.LORA_ERR_ARG
+    assert lib.lora_pool_set_prefill_kernel(None, al.LORA_PREFILL_PAIR) == al.LORA_ERR_ARG
+    assert lib.lora_test_delayed_copy(None, None, 4, 10, None) == al.LORA_ERR_ARG
     assert lib.lora_pool_set_path(None, 0) == al.LORA_ERR_ARG
     assert lib.lora_pool_stats(None, None) == al.LORA_ERR_ARG
     out = ctypes.c_void_p()
