@@ -866,6 +866,9 @@ def main():
                                 f"{lora_il_step_ms:.5f} ms per step there)",
         "isolated_call_ms": iso_ms,
         "adapter_path_gbs": adapter_gbs,
+        # the whole step's algorithmic bytes (W, X, Y, ids, the distinct adapters) over
+        # the back-to-back step time: both kernels, with the next call's W overlapping
+        "step_hbm_gbs": (ab["w"] + ab["x"] + ab["y"] + ab["ids"] + ab["adapters"]) / (total_ms / args.steps * 1e-3) / 1e9,
         "kernel_ms": {"segment_build": seg_ms, "shrink": shrink_ms, "base_gemm": gemm_ms,
                       "finish_expand": finish_ms},
         "base_only_kernel_ms": {"base_gemm": mean_of(base_kts, "base_gemm"),
