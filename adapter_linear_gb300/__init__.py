@@ -40,6 +40,7 @@ EXPORTS = (
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
     "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info", "lora_test_delayed_copy",
+    "lora_pool_set_trace",
 )
 PLAN_INFO_FIELDS = ("units", "G", "grid", "max_seg", "n_acc", "stages", "tmem_cols", "smem_bytes",
                     "pairs", "col_blocks", "tight", "ntok", "partials_floats", "prefetch_a")
@@ -102,6 +103,7 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_pool_selftest_wait": [vp, i32, vp],
         "lora_decode_plan_info": [i32, i32, vp, vp, vp, i32, vp],
         "lora_test_delayed_copy": [vp, vp, i32, i32, vp],
+        "lora_pool_set_trace": [vp, vp, i32],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -257,6 +259,11 @@ def lora_pool_kernel_times(pool: int) -> Dict[str, float]:
     return dict(zip(KERNEL_SLOT_NAMES, list(out)))
 
 
+def lora_pool_set_trace(pool: int, buf, n_calls: int) -> int:
+    """Span trace of the pool's next calls into a device buffer (see the header)."""
+    return load_library().lora_pool_set_trace(pool, _ptr(buf), n_calls)
+
+
 def lora_status_string(status: int) -> str:
     return load_library().lora_status_string(status).decode()
 
@@ -398,3 +405,7 @@ class LoraPool:
 
     def kernel_times(self) -> Dict[str, float]:
         return lora_pool_kernel_times(self.handle)
+
+    def set_trace(self, buf, n_calls: int = 1):
+        """buf: device int64/uint64 tensor of n_calls * LORA_KERNEL_SLOTS * 4 entries, or None."""
+        _check(lora_pool_set_trace(self.handle, buf, n_calls), "lora_pool_set_trace")

@@ -31,31 +31,10 @@ namespace {
 lora_status ensure_tier(lora_pool *p)
 {
     if (!p->slot_key.empty()) return LORA_OK;
-    const size_t row_ints = (size_t)p->slot_stride + p->max_pages;
-    // one staging row per slot, plus an all-zero row for evictions
-    if (cudaHostAlloc((void **)&p->stage_rows, sizeof(int32_t) * row_ints * (p->max_adapters + 1),
-                      cudaHostAllocDefault) != cudaSuccess) {
-        cudaGetLastError();
-        p->stage_rows = nullptr;
-        return LORA_ERR_OOM;
-    }
-    std::memset(p->stage_rows, 0, sizeof(int32_t) * row_ints * (p->max_adapters + 1));
     p->slot_key.assign(p->max_adapters, kNoKey);
     p->slot_pins.assign(p->max_adapters, 0);
     p->slot_tick.assign(p->max_adapters, 0);
-    p->slot_copy_ev.assign(p->max_adapters, nullptr);
-    if (cudaEventCreateWithFlags(&p->ev_copy, cudaEventDisableTiming) != cudaSuccess) {
-        p->ev_copy = nullptr;
-        return LORA_ERR_CUDA;
-    }
-    // calls made before the tier existed were not recorded: let them finish
-    CUDA_TRY(cudaDeviceSynchronize());
     return LORA_OK;
-}
-
-int32_t *stage_row(lora_pool *p, int slot)
-{
-    return p->stage_rows + (size_t)slot * (p->slot_stride + p->max_pages);
 }
 
 // Take cached slot s out of the GPU: its pages return to the free list and its
@@ -63,11 +42,10 @@ int32_t *stage_row(lora_pool *p, int slot)
 lora_status evict(lora_pool *p, int s)
 {
     int32_t *row = &p->h_slots[(size_t)s * p->slot_stride];
-    const int32_t *zero = stage_row(p, p->max_adapters);
-    CUDA_TRY(cudaMemcpyAsync(p->d_slots + (size_t)s * p->slot_stride, zero,
-                             sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice,
-                             p->copy_stream));
-    CUDA_TRY(cudaEventRecord(p->ev_copy, p->copy_stream));
+    int32_t *zero = nullptr;
+    lora_status st = stage_row_ready(p, p->max_adapters, &zero);
+    if (st != LORA_OK) return st;
+    if ((st = enqueue_row(p, s, zero)) != LORA_OK) return st;
     const int npages = row[SLOT_NPAGES];
     for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
     std::fill(row, row + p->slot_stride, 0);
@@ -113,13 +91,10 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
         if (st != LORA_OK) return st;
         if (slot < 0) slot = empty_slot(p);
     }
-    // the slot's staging row may still be read by its previous swap-in
-    if (p->slot_copy_ev[slot]) {
-        CUDA_TRY(cudaEventSynchronize(p->slot_copy_ev[slot]));
-    } else {
-        CUDA_TRY(cudaEventCreateWithFlags(&p->slot_copy_ev[slot], cudaEventDisableTiming));
-    }
-    int32_t *row = stage_row(p, slot);
+    // the slot's staging row may still be read by its previous table copy
+    int32_t *row = nullptr;
+    lora_status st = stage_row_ready(p, slot, &row);
+    if (st != LORA_OK) return st;
     int32_t *pages = row + p->slot_stride;
     std::fill(row, row + p->slot_stride + p->max_pages, 0);
     for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
@@ -140,10 +115,7 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
                              cudaMemcpyHostToDevice, s));
     CUDA_TRY(launch_pack_adapter(p->stage_A, p->stage_B, h.rank, p->d_page_list, npages,
                                  pool_view(p), p->A_pages, p->B_pages, s));
-    CUDA_TRY(cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, row,
-                             sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice, s));
-    CUDA_TRY(cudaEventRecord(p->slot_copy_ev[slot], s));
-    CUDA_TRY(cudaEventRecord(p->ev_copy, s));
+    if ((st = enqueue_row(p, slot, row)) != LORA_OK) return st;
 
     p->free_pages.resize(p->free_pages.size() - npages);
     std::copy(row, row + p->slot_stride, &p->h_slots[(size_t)slot * p->slot_stride]);
@@ -156,20 +128,6 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
 }  // namespace
 
 namespace lora {
-
-lora_status note_call(lora_pool *p, cudaStream_t stream)
-{
-    if (p->slot_key.empty()) return LORA_OK;  // no host tier: nothing is swapped in
-    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
-    CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
-    if (cs != cudaStreamCaptureStatusNone) return LORA_OK;  // graph replays are the caller's order
-    if (!p->ev_call) CUDA_TRY(cudaEventCreateWithFlags(&p->ev_call, cudaEventDisableTiming));
-    // every later copy on the copy stream (a swap-in changing pages or table rows)
-    // starts after this call, whichever stream it ran on
-    CUDA_TRY(cudaEventRecord(p->ev_call, stream));
-    CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_call, 0));
-    return LORA_OK;
-}
 
 // Called when a cached slot is unloaded through lora_unload_adapter.
 void forget_cached_slot(lora_pool *p, int slot)
@@ -192,14 +150,6 @@ void destroy_host_tier(lora_pool *p)
         if (kv.second.B) cudaFreeHost(kv.second.B);
     }
     p->host_tier.clear();
-    for (cudaEvent_t e : p->slot_copy_ev)
-        if (e) cudaEventDestroy(e);
-    p->slot_copy_ev.clear();
-    if (p->ev_copy) cudaEventDestroy(p->ev_copy);
-    if (p->ev_call) cudaEventDestroy(p->ev_call);
-    p->ev_copy = p->ev_call = nullptr;
-    if (p->stage_rows) cudaFreeHost(p->stage_rows);
-    p->stage_rows = nullptr;
 }
 
 }  // namespace lora

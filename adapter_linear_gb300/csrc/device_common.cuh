@@ -25,6 +25,51 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Measurement hook of one launch (kTraceWords words, no-op for nullptr), global timer
+// in ns: [0] the earliest CTA entry (atomic min), [1] the latest CTA exit (atomic
+// max), [2] / [3] the earliest / latest moment a CTA got past its wait on the
+// previous kernel in the stream (programmatic dependent launch; a kernel launched
+// without it stamps its entry there). A CTA stamps its exit once all its threads are
+// past their work; the caller of trace_release is the CTA's one thread that waits.
+constexpr int kTraceWords = 4;
+
+__device__ __forceinline__ void trace_stamp_min(uint64_t *w)
+{
+    atomicMin(reinterpret_cast<unsigned long long *>(w), (unsigned long long)global_timer_ns());
+}
+
+__device__ __forceinline__ void trace_stamp_max(uint64_t *w)
+{
+    atomicMax(reinterpret_cast<unsigned long long *>(w), (unsigned long long)global_timer_ns());
+}
+
+__device__ __forceinline__ void trace_enter(uint64_t *trace)
+{
+    if (trace && threadIdx.x == 0) trace_stamp_min(trace);
+}
+
+__device__ __forceinline__ void trace_release(uint64_t *trace)
+{
+    if (trace) {
+        trace_stamp_min(trace + 2);
+        trace_stamp_max(trace + 3);
+    }
+}
+
+// Entry and release together: kernels that do not wait on the previous kernel.
+__device__ __forceinline__ void trace_enter_released(uint64_t *trace)
+{
+    if (trace && threadIdx.x == 0) {
+        trace_stamp_min(trace);
+        trace_release(trace);
+    }
+}
+
+__device__ __forceinline__ void trace_exit(uint64_t *trace)
+{
+    if (trace && threadIdx.x == 0) trace_stamp_max(trace + 1);
+}
+
 // Two packed bf16 -> fp32 (exact widening).
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -124,8 +169,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Wait for the phase with `parity` to complete, for at most limit_ns.
-// Returns false (after raising the CTA's abort flag and the pool's timeout
-// bit) if it runs out, or if another role of the CTA has already aborted.
+// Returns false (after raising the CTA's abort flag and, when err is not null,
+// the pool's timeout bit) if it runs out, or if another role of the CTA has
+// already aborted.
 static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
                                        int *err, uint64_t limit_ns = kWaitTimeoutNs)
 {
@@ -137,7 +183,7 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, vo
             if (*abort_flag) return false;
             if (global_timer_ns() - start > limit_ns) {
                 *abort_flag = 1;
-                atomicOr(err, kErrTimeoutBit);
+                if (err) atomicOr(err, kErrTimeoutBit);
                 return false;
             }
         }
@@ -403,7 +449,7 @@ static __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t pa
             if (*abort_flag) return false;
             if (global_timer_ns() - start > limit_ns) {
                 *abort_flag = 1;
-                atomicOr(err, kErrTimeoutBit);
+                if (err) atomicOr(err, kErrTimeoutBit);
                 return false;
             }
         }

@@ -193,6 +193,8 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
 
     // the finishing kernel may start its independent prologue now
     pdl_launch_dependents();
+    uint64_t *const trace = p.trace ? p.trace + 2 * kTraceWords : nullptr;  // kernel slot 2
+    trace_enter(trace);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c = blockIdx.x;
@@ -242,6 +244,7 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
                                      &full[i], (kb * kBoxes + b) * 64, tile * 128, pol_w);
             }
             pdl_wait_prior();
+            trace_release(trace);
             cur.load(p, unit_problem(p, u0));
             for (int i = 0; i < pre; ++i) {
                 const int u = u0 + i;
@@ -402,6 +405,7 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         tc_fence_after_sync();
         tmem_dealloc(*tmem_slot, p.tmem_cols);
     }
+    trace_exit(trace);
 }
 
 constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
@@ -449,65 +453,16 @@ __device__ __forceinline__ void finish_b_words(const PoolDev &pool, const int32_
         prefetch_l2(pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage);
 }
 
-// LORA = false: the base-only pass (no adapter state, few registers).
+// The sums of one thread's 8 columns of token t (see finish_decode_body).
 template <int NP, bool LORA>
-__device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
-                                                   const float *__restrict__ partials,
-                                                   const int32_t *__restrict__ ids)
+__device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const DecodeProblem &pr,
+                                               const float *__restrict__ partials, int t, int n0,
+                                               int c_lo, int c_hi, int seg_lo, int np,
+                                               const int32_t *pages, bool early,
+                                               const uint4 (&b)[kPrefetchPages][8])
 {
-    // The next call's GEMM may launch now: its CTAs take an SM as soon as this call's
-    // GEMM CTA leaves it and stream their first W tiles; everything they write comes
-    // after their own wait for this kernel.
-    pdl_launch_dependents();
-    int m = 0;
-    for (int k = 1; NP > 1 && k < p.n; ++k)
-        if (p.prob[pick<NP>(k)].col_blk_begin <= (int)blockIdx.x) m = k;
-    const DecodeProblem &pr = p.prob[pick<NP>(m)];
     const PoolDev &pool = pr.pool;
-    const int n0 = ((blockIdx.x - pr.col_blk_begin) * kFinishThreads + threadIdx.x) * kFinishCols;
-    const int t = blockIdx.y;
-    const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
-
-    // ---- ahead of the GEMM kernel's end: this token's adapter and its B words (the
-    // 8 columns' 16-byte words of a page are one 128-byte line): the first pages into
-    // registers, the rest into L2. The id read here may still be written by a kernel
-    // ahead of the GEMM in the stream, so it is read again after the wait and the
-    // words are reloaded if it changed.
-    int id = -1, np = 0;
-    const int32_t *pages = nullptr;
-    uint4 b[kPrefetchPages][8];
-    if (LORA && pool.slots != nullptr) {
-        id = ids[t];
-        np = finish_adapter(pool, id, pages);
-        if (col_ok) finish_b_words(pool, pages, np, n0, b);
-    }
-    // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
-    // can have started before the tile; its partial for the tile is its segment
-    // (tile - its first tile), the others' is their segment 0. (U * G < 2^31 is
-    // checked on the host, so the products fit in 32 bits.)
-    const int tile = n0 >> 7, nl = n0 & 127;
-    const int ub = pr.u_begin + tile * pr.KB, ue = ub + pr.KB;
-    int c_lo = (ub * p.G) / p.U;
-    while (c_lo > 0 && (c_lo * p.U) / p.G > ub) --c_lo;
-    while (((c_lo + 1) * p.U) / p.G <= ub) ++c_lo;
-    int c_hi = c_lo;
-    while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < ue) ++c_hi;
-    const int seg_lo = pr.g_begin + tile - unit_tile(p, (c_lo * p.U) / p.G);
-
-    // ---- partials and V are written by the GEMM kernel
-    pdl_wait_prior();
-    bool early = true;  // the words in b belong to this token's adapter
-    if (LORA && pool.slots != nullptr) {
-        const int id_now = ids[t];
-        if (id_now != id) {
-            id = id_now;
-            np = finish_adapter(pool, id, pages);
-            early = false;
-        }
-        if (np == 0 && id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin)
-            atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
-    }
-    if (!col_ok) return;
+    const int nl = n0 & 127;
 
     // One round of loads first: the V values of the pages whose B words are already in
     // registers, the first contributor's partial and the next kFinishBatch ones; the
@@ -577,6 +532,74 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     o.z = pack_bf16x2(acc[4], acc[5]);
     o.w = pack_bf16x2(acc[6], acc[7]);
     *reinterpret_cast<uint4 *>(pr.Y + (size_t)t * pool.d_out + n0) = o;
+}
+
+// LORA = false: the base-only pass (no adapter state, few registers).
+template <int NP, bool LORA>
+__device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
+                                                   const float *__restrict__ partials,
+                                                   const int32_t *__restrict__ ids)
+{
+    // The next call's GEMM may launch now: its CTAs take an SM as soon as this call's
+    // GEMM CTA leaves it and stream their first W tiles; everything they write comes
+    // after their own wait for this kernel.
+    pdl_launch_dependents();
+    uint64_t *const trace = p.trace ? p.trace + 3 * kTraceWords : nullptr;  // kernel slot 3
+    trace_enter(trace);
+    int m = 0;
+    for (int k = 1; NP > 1 && k < p.n; ++k)
+        if (p.prob[pick<NP>(k)].col_blk_begin <= (int)blockIdx.x) m = k;
+    const DecodeProblem &pr = p.prob[pick<NP>(m)];
+    const PoolDev &pool = pr.pool;
+    const int n0 = ((blockIdx.x - pr.col_blk_begin) * kFinishThreads + threadIdx.x) * kFinishCols;
+    const int t = blockIdx.y;
+    const bool col_ok = n0 < pool.d_out;  // d_out is a multiple of 8
+
+    // ---- ahead of the GEMM kernel's end: this token's adapter and its B words (the
+    // 8 columns' 16-byte words of a page are one 128-byte line): the first pages into
+    // registers, the rest into L2. The id read here may still be written by a kernel
+    // ahead of the GEMM in the stream, so it is read again after the wait and the
+    // words are reloaded if it changed.
+    int id = -1, np = 0;
+    const int32_t *pages = nullptr;
+    uint4 b[kPrefetchPages][8];
+    if (LORA && pool.slots != nullptr) {
+        id = ids[t];
+        np = finish_adapter(pool, id, pages);
+        if (col_ok) finish_b_words(pool, pages, np, n0, b);
+    }
+    // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
+    // can have started before the tile; its partial for the tile is its segment
+    // (tile - its first tile), the others' is their segment 0. (U * G < 2^31 is
+    // checked on the host, so the products fit in 32 bits.)
+    const int tile = n0 >> 7;
+    const int ub = pr.u_begin + tile * pr.KB, ue = ub + pr.KB;
+    int c_lo = (ub * p.G) / p.U;
+    while (c_lo > 0 && (c_lo * p.U) / p.G > ub) --c_lo;
+    while (((c_lo + 1) * p.U) / p.G <= ub) ++c_lo;
+    int c_hi = c_lo;
+    while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < ue) ++c_hi;
+    const int seg_lo = pr.g_begin + tile - unit_tile(p, (c_lo * p.U) / p.G);
+
+    // ---- partials and V are written by the GEMM kernel
+    pdl_wait_prior();
+    if (threadIdx.x == 0) trace_release(trace);
+    bool early = true;  // the words in b belong to this token's adapter
+    if (LORA && pool.slots != nullptr) {
+        const int id_now = ids[t];
+        if (id_now != id) {
+            id = id_now;
+            np = finish_adapter(pool, id, pages);
+            early = false;
+        }
+        if (np == 0 && id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin)
+            atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
+    }
+    if (col_ok) finish_columns<NP, LORA>(p, pr, partials, t, n0, c_lo, c_hi, seg_lo, np, pages, early, b);
+    if (trace) {
+        __syncthreads();
+        trace_exit(trace);
+    }
 }
 
 // Register budgets. The register file is split among an SM's four sub-partitions
@@ -732,7 +755,7 @@ namespace {
 template <int NP>
 DecodePlanT<NP> narrow_plan(const DecodePlan &p)
 {
-    DecodePlanT<NP> q;
+    DecodePlanT<NP> q{};
     q.n = p.n;
     q.T = p.T;
     q.ntok = p.ntok;
@@ -746,6 +769,7 @@ DecodePlanT<NP> narrow_plan(const DecodePlan &p)
     q.col_blocks = p.col_blocks;
     q.tight = p.tight;
     q.prefetch_a = p.prefetch_a;
+    q.trace = p.trace;
     q.tmem_cols = p.tmem_cols;
     q.smem_bytes = p.smem_bytes;
     for (int m = 0; m < NP; ++m) q.prob[m] = p.prob[m];

@@ -56,6 +56,7 @@ struct PrefillArgs {
     int ldh;
     uint16_t *Y;
     int *err;
+    uint64_t *trace;  // measurement hook (first entry, last exit), or nullptr
 };
 
 __device__ __forceinline__ void tile_coords(int tile, const PrefillArgs &a, int &m, int &n)
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_prefill_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW,
                         const __grid_constant__ CUtensorMap tmV, PrefillArgs a, PoolDev pool)
 {
+    trace_enter_released(a.trace);
     extern __shared__ uint8_t pre_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(pre_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -323,6 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }
+    trace_exit(a.trace);
 }
 
 // ------------------------------------------------------------ CTA-pair variant
@@ -496,6 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                              const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmB,
                              const __grid_constant__ CUtensorMap tmY, PrefillArgs a, PoolDev pool)
 {
+    trace_enter_released(a.trace);
     extern __shared__ uint8_t pre_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(pre_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -690,6 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc_pair(tmem, kTmemCols);
     }
+    trace_exit(a.trace);
 }
 
 // Clusters of the pair kernel that can be resident at once on the current device
@@ -754,9 +759,10 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
                                 const CUtensorMap &tmV, const CUtensorMap *tmB, const CUtensorMap *tmY, int T,
                                 const int32_t *ids,
                                 const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
-                                int num_sms, int *err, cudaStream_t stream)
+                                int num_sms, int *err, cudaStream_t stream, uint64_t *trace)
 {
     PrefillArgs a{};
+    a.trace = trace;
     a.T = T;
     a.d_in = pool.d_in;
     a.d_out = pool.d_out;

@@ -73,8 +73,11 @@ struct PoolDev {
 
 size_t seg_build_smem_bytes(int max_adapters, int warps);
 // vhl != nullptr: also zero the rows [ldh] of vhl of tokens without an adapter.
+// trace (here and below): the launch's four words of the measurement hook (see
+// trace_enter in device_common.cuh), or nullptr.
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
-                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream);
+                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream,
+                             uint64_t *trace = nullptr);
 
 // Prefill shrink (tcgen05), 128-token units per segment: writes s_i X[t,:] A_i as
 // bf16 hi/lo pairs grouped per 32 rank columns (see shrink.cu) into Vhl [T][ldh].
@@ -83,7 +86,7 @@ cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, Seg
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
                              const CUtensorMap &tmAw, const uint16_t *X,
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
-                             int num_sms, int *err, cudaStream_t stream);
+                             int num_sms, int *err, cudaStream_t stream, uint64_t *trace = nullptr);
 
 // ---------------------------------------------------------------- decode path
 // One decode call covers 1..kMaxGroup problems that share the token ids (one
@@ -122,6 +125,7 @@ struct DecodePlanT {
     int col_blocks;         // finishing grid.x
     bool tight;             // register-bounded kernel variants (see gemm_decode.cu)
     bool prefetch_a;        // A pages of the shrink pairs into L2 before the wait
+    uint64_t *trace;        // measurement hook: LORA_KERNEL_SLOTS x 4 words (see trace_enter), or nullptr
     uint32_t tmem_cols;
     size_t smem_bytes;
     DecodeProblem prob[NP];
@@ -158,7 +162,7 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
                                 const CUtensorMap &tmV, const CUtensorMap *tmB, const CUtensorMap *tmY, int T,
                                 const int32_t *ids,
                                 const int32_t *tile_info, const PoolDev &pool, const uint16_t *Vhl, int ldh, uint16_t *Y,
-                                int num_sms, int *err, cudaStream_t stream);
+                                int num_sms, int *err, cudaStream_t stream, uint64_t *trace = nullptr);
 
 // Pack a row-major A (d_in x rank) and B (rank x d_out) into pool pages.
 cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,

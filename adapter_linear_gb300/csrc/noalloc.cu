@@ -21,10 +21,9 @@
 namespace lora {
 namespace {
 
-// Split-K partial sums (G * max_seg * T * 128 floats per call): 16 MiB, after a
-// 256-byte reserved head whose first word takes the kernels' timeout bit.
-constexpr size_t kNoallocReserved = 64;
-constexpr size_t kNoallocScratchFloats = ((size_t)4 << 20) + kNoallocReserved;
+// Split-K partial sums (G * max_seg * T * 128 floats per call): 16 MiB. The kernels
+// get no error word here (a wait that times out is not reported by this entry point).
+constexpr size_t kNoallocScratchFloats = (size_t)4 << 20;
 
 static __device__ __align__(256) float g_noalloc_scratch[kNoallocScratchFloats];
 
@@ -81,7 +80,7 @@ extern "C" lora_status lora_base_linear_noalloc(const void *X, const void *W_bas
     if (st != LORA_OK) return st;
 
     // fewer stream-K ranges when the partial sums would not fit the fixed scratch
-    const size_t avail = kNoallocScratchFloats - kNoallocReserved;
+    const size_t avail = kNoallocScratchFloats;
     const int no_pages = 0;
     DecodePlan plan;
     int max_G = dev->num_sms;
@@ -101,8 +100,8 @@ extern "C" lora_status lora_base_linear_noalloc(const void *X, const void *W_bas
         return LORA_ERR_ARG;
     // the partials need no clearing: every slot the finishing pass reads is
     // written by this call's GEMM kernel first
-    int *err = reinterpret_cast<int *>(dev->scratch);
-    float *partials = dev->scratch + kNoallocReserved;
+    int *err = nullptr;
+    float *partials = dev->scratch;
     DecodeProblem &q = plan.prob[0];
     q.pool.d_in = d_in;
     q.pool.d_out = d_out;

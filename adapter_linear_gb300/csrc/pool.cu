@@ -60,6 +60,49 @@ PoolDev pool_view(const lora_pool *p)
     return v;
 }
 
+lora_status order_after_changes(lora_pool *p, cudaStream_t stream)
+{
+    if (p->copy_epoch == p->waited_epoch && stream == p->waited_stream) return LORA_OK;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+    if (cs != cudaStreamCaptureStatusNone) return LORA_OK;  // graph replays are the caller's order
+    CUDA_TRY(cudaStreamWaitEvent(stream, p->ev_copy, 0));
+    p->waited_epoch = p->copy_epoch;
+    p->waited_stream = stream;
+    return LORA_OK;
+}
+
+lora_status note_call(lora_pool *p, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+    if (cs != cudaStreamCaptureStatusNone) return LORA_OK;  // graph replays are the caller's order
+    // every later change on the copy stream (pages, table rows, the error-word read)
+    // starts after this call, whichever stream it ran on
+    CUDA_TRY(cudaEventRecord(p->ev_call, stream));
+    CUDA_TRY(cudaStreamWaitEvent(p->copy_stream, p->ev_call, 0));
+    return LORA_OK;
+}
+
+lora_status stage_row_ready(lora_pool *p, int slot, int32_t **row)
+{
+    *row = p->stage_rows + (size_t)slot * (p->slot_stride + p->max_pages);
+    if (slot < p->max_adapters) CUDA_TRY(cudaEventSynchronize(p->slot_copy_ev[slot]));
+    return LORA_OK;
+}
+
+lora_status enqueue_row(lora_pool *p, int slot, const int32_t *row)
+{
+    cudaStream_t s = p->copy_stream;
+    CUDA_TRY(cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, row,
+                             sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice, s));
+    if (row != p->stage_rows + (size_t)p->max_adapters * (p->slot_stride + p->max_pages))
+        CUDA_TRY(cudaEventRecord(p->slot_copy_ev[slot], s));
+    CUDA_TRY(cudaEventRecord(p->ev_copy, s));
+    p->copy_epoch += 1;
+    return LORA_OK;
+}
+
 }  // namespace lora
 
 namespace {
@@ -197,6 +240,9 @@ __global__ void wait_selftest_kernel(int *err, uint64_t limit_ns)
     __syncthreads();
 }
 
+// err[1] = the error word err[0], which is cleared in the same atomic step.
+__global__ void read_clear_kernel(int *err) { err[1] = atomicExch(err, 0); }
+
 // A producer of the kind that programmatic dependent launch allows: it lets the next
 // kernel in the stream start at once, then, after `delay_ns`, writes dst. Anything
 // that reads dst before its own wait on this kernel sees the old values.
@@ -253,6 +299,17 @@ struct CallMarks {
 // The decode path for n problems that share the ids (scratch already sized for T
 // on every pool). Per-token (BGMV-style) shrink fused into the GEMM kernel: no
 // segment tables.
+// The span-trace words of the next call on p (LORA_KERNEL_SLOTS x kTraceWords), or nullptr.
+uint64_t *next_trace(lora_pool *p)
+{
+    if (!p->trace) return nullptr;
+    uint64_t *t = p->trace + (size_t)(p->trace_k % p->trace_calls) * LORA_KERNEL_SLOTS * kTraceWords;
+    p->trace_k += 1;
+    return t;
+}
+
+uint64_t *trace_slot(uint64_t *t, int slot) { return t ? t + kTraceWords * slot : nullptr; }
+
 lora_status run_decode(lora_pool *const *pools, int n, const void *const *X, const void *const *W,
                        const int32_t *ids, int T, void *const *Y, cudaStream_t stream, bool with_lora,
                        CallMarks &marks)
@@ -285,6 +342,7 @@ lora_status run_decode(lora_pool *const *pools, int n, const void *const *X, con
         q.err = p->d_err;
     }
     const int32_t *tids = with_lora ? ids : nullptr;
+    plan.trace = next_trace(p0);
     CUDA_TRY(launch_gemm_decode(maps, plan, tids, p0->partials, p0->d_err, stream));
     if (!marks.mark(2)) return LORA_ERR_CUDA;
     CUDA_TRY(launch_finish_decode(plan, p0->partials, tids, stream));
@@ -303,6 +361,7 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
     lora_status st = ensure_scratch(p, T);
     if (st != LORA_OK) return st;
 
+    if ((st = order_after_changes(p, stream)) != LORA_OK) return st;
     const PoolDev pd = pool_view(p);
     const SegTables tabs = seg_tables(p);
     CallMarks marks{p, stream};
@@ -317,7 +376,9 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (st != LORA_OK) return st;
     } else {
         // the segment tables; rows of the shrink output of tokens without an adapter zeroed
-        if (with_lora) CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, p->Vhl, p->ldh, stream));
+        uint64_t *tr = next_trace(p);
+        if (with_lora)
+            CUDA_TRY(launch_seg_build(ids, T, pd, tabs, p->d_err, p->Vhl, p->ldh, stream, trace_slot(tr, 0)));
         if (!mark(0)) return LORA_ERR_CUDA;
         const bool pair = p->pair_ok && (p->prefill_kernel == LORA_PREFILL_PAIR ||
                                          (p->prefill_kernel == LORA_PREFILL_AUTO && T > 128));
@@ -328,12 +389,12 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (!tmW || !tmX || !tmV || (pair && !tmY)) return LORA_ERR_ARG;
         if (with_lora) {
             CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
-                                      p->d_err, stream));
+                                      p->d_err, stream, trace_slot(tr, 1)));
         }
         if (!mark(1)) return LORA_ERR_CUDA;
         CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, *tmV, pair ? &p->tmB : nullptr, tmY, T, with_lora ? ids : nullptr,
                                      with_lora ? p->tile_info : nullptr, pd, p->Vhl, p->ldh, Yb,
-                                     p->num_sms, p->d_err, stream));
+                                     p->num_sms, p->d_err, stream, trace_slot(tr, 2)));
         if (!mark(2)) return LORA_ERR_CUDA;
     }
     p->n_calls += 1;
@@ -399,6 +460,7 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
     p->ldv = ((p->max_pages * kRankPage + 15) / 16) * 16;
     p->ldh = 2 * (((p->max_pages * kRankPage + 31) / 32) * 32);
     p->h_slots.assign((size_t)max_adapters * p->slot_stride, 0);
+    p->slot_copy_ev.assign(max_adapters, nullptr);
     p->chain_refs.assign(max_adapters, 0);
     p->free_pages.reserve(p->num_pages - 1);
     for (int pg = p->num_pages - 1; pg >= 1; --pg) p->free_pages.push_back(pg);
@@ -409,18 +471,40 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
     if ((st = alloc_dev(p, (void **)&p->A_pages, a_bytes)) ||
         (st = alloc_dev(p, (void **)&p->B_pages, b_bytes)) ||
         (st = alloc_dev(p, (void **)&p->d_slots, sizeof(int32_t) * p->h_slots.size())) ||
-        (st = alloc_dev(p, (void **)&p->d_err, sizeof(int))) ||
+        (st = alloc_dev(p, (void **)&p->d_err, 2 * sizeof(int))) ||
         (st = alloc_dev(p, (void **)&p->stage_A, (size_t)d_in * max_rank * 2)) ||
         (st = alloc_dev(p, (void **)&p->stage_B, (size_t)d_out * max_rank * 2)) ||
+        (st = alloc_dev(p, (void **)&p->load_A, (size_t)d_in * max_rank * 2)) ||
+        (st = alloc_dev(p, (void **)&p->load_B, (size_t)d_out * max_rank * 2)) ||
         (st = alloc_dev(p, (void **)&p->d_page_list, sizeof(int32_t) * p->max_pages))) {
         lora_pool_destroy(p);
         return st;
     }
-    if (cudaMemset(p->A_pages, 0, (size_t)kRankPage * d_in * 2) != cudaSuccess ||
+    const size_t row_ints = (size_t)p->slot_stride + p->max_pages;
+    if (cudaHostAlloc((void **)&p->stage_rows, sizeof(int32_t) * row_ints * (max_adapters + 1),
+                      cudaHostAllocDefault) != cudaSuccess ||
+        cudaHostAlloc((void **)&p->h_err, sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        lora_pool_destroy(p);
+        return LORA_ERR_OOM;
+    }
+    std::memset(p->stage_rows, 0, sizeof(int32_t) * row_ints * (max_adapters + 1));
+    bool events_ok = cudaEventCreateWithFlags(&p->ev_call, cudaEventDisableTiming) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p->ev_copy, cudaEventDisableTiming) == cudaSuccess &&
+                     cudaEventCreateWithFlags(&p->ev_loaded, cudaEventDisableTiming) == cudaSuccess;
+    for (int i = 0; events_ok && i < max_adapters; ++i)
+        events_ok = cudaEventCreateWithFlags(&p->slot_copy_ev[i], cudaEventDisableTiming) == cudaSuccess;
+    if (!events_ok ||
+        cudaMemset(p->A_pages, 0, (size_t)kRankPage * d_in * 2) != cudaSuccess ||
         cudaMemset(p->B_pages, 0, (size_t)d_out * kRankPage * 2) != cudaSuccess ||
         cudaMemset(p->d_slots, 0, sizeof(int32_t) * p->h_slots.size()) != cudaSuccess ||
-        cudaMemset(p->d_err, 0, sizeof(int)) != cudaSuccess ||
+        cudaMemset(p->d_err, 0, 2 * sizeof(int)) != cudaSuccess ||
         cudaStreamCreateWithFlags(&p->copy_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&p->load_stream, cudaStreamNonBlocking) != cudaSuccess ||
+        // the kernels of loads, unloads and error reads are loaded now: a first launch
+        // of a kernel not yet loaded (lazy module loading) can wait for the whole device
+        ensure_smem_attr((const void *)pack_adapter_kernel, 0) != cudaSuccess ||
+        ensure_smem_attr((const void *)read_clear_kernel, 0) != cudaSuccess ||
         !make_tmap_bf16_2d(&p->tmA, p->A_pages, d_in, (uint64_t)p->num_pages * kRankPage,
                            (uint64_t)d_in * 2, 64, kRankPage) ||
         !make_tmap_bf16_2d(&p->tmAw, p->A_pages, d_in, (uint64_t)p->num_pages * kRankPage,
@@ -454,10 +538,19 @@ lora_status lora_pool_destroy(lora_pool_t p)
     free_dev(p, p->d_err, 0);
     free_dev(p, p->stage_A, 0);
     free_dev(p, p->stage_B, 0);
+    free_dev(p, p->load_A, 0);
+    free_dev(p, p->load_B, 0);
     free_dev(p, p->d_page_list, 0);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
+    if (p->load_stream) cudaStreamDestroy(p->load_stream);
     for (auto &e : p->ev)
         if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : p->slot_copy_ev)
+        if (e) cudaEventDestroy(e);
+    for (cudaEvent_t e : {p->ev_call, p->ev_copy, p->ev_loaded})
+        if (e) cudaEventDestroy(e);
+    if (p->stage_rows) cudaFreeHost(p->stage_rows);
+    if (p->h_err) cudaFreeHost(p->h_err);
     delete p;
     return LORA_OK;
 }
@@ -479,39 +572,46 @@ lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void
     const int npages = (rank + kRankPage - 1) / kRankPage;
     if ((int)p->free_pages.size() < npages) return LORA_ERR_OOM;
 
-    // calls already enqueued keep seeing the old pages and table
-    CUDA_TRY(cudaDeviceSynchronize());
-
-    std::vector<int32_t> pages(npages);
-    for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
-
-    cudaStream_t s = p->copy_stream;
+    // The caller's A and B into the pool's load buffers first, on a stream of their
+    // own (not behind the pool's calls), so that the caller may free them on return;
+    // the previous load's packing must have read those buffers.
     const size_t a_bytes = (size_t)p->d_in * rank * 2, b_bytes = (size_t)rank * p->d_out * 2;
-    bool ok = cudaMemcpyAsync(p->stage_A, A, a_bytes, cudaMemcpyDefault, s) == cudaSuccess &&
-              cudaMemcpyAsync(p->stage_B, B, b_bytes, cudaMemcpyDefault, s) == cudaSuccess &&
-              cudaMemcpyAsync(p->d_page_list, pages.data(), sizeof(int32_t) * npages,
-                              cudaMemcpyHostToDevice, s) == cudaSuccess &&
-              launch_pack_adapter(p->stage_A, p->stage_B, rank, p->d_page_list, npages,
-                                  pool_view(p), p->A_pages, p->B_pages, s) == cudaSuccess;
-    std::vector<int32_t> new_row(p->slot_stride, 0);
-    new_row[SLOT_RANK] = rank;
-    new_row[SLOT_NPAGES] = npages;
-    const float scale = alpha / (float)rank;
-    std::memcpy(&new_row[SLOT_SCALE], &scale, sizeof(float));
-    for (int q = 0; q < npages; ++q) {
-        new_row[SLOT_PAGES + q] = pages[q];
-        std::memcpy(&new_row[slot_page_scale(p->max_pages, q)], &scale, sizeof(float));
-    }
-    ok = ok &&
-         cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, new_row.data(),
-                         sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice, s) == cudaSuccess;
-    ok = (cudaStreamSynchronize(s) == cudaSuccess) && ok;
-    if (!ok) {
+    CUDA_TRY(cudaEventSynchronize(p->ev_loaded));
+    if (cudaMemcpyAsync(p->load_A, A, a_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
+        cudaMemcpyAsync(p->load_B, B, b_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
+        cudaStreamSynchronize(p->load_stream) != cudaSuccess) {
         cudaGetLastError();
         return LORA_ERR_CUDA;
     }
+    int32_t *srow = nullptr;
+    lora_status st = stage_row_ready(p, slot, &srow);
+    if (st != LORA_OK) return st;
+    int32_t *pages = srow + p->slot_stride;
+    std::fill(srow, srow + p->slot_stride + p->max_pages, 0);
+    for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
+    srow[SLOT_RANK] = rank;
+    srow[SLOT_NPAGES] = npages;
+    const float scale = alpha / (float)rank;
+    std::memcpy(&srow[SLOT_SCALE], &scale, sizeof(float));
+    for (int q = 0; q < npages; ++q) {
+        srow[SLOT_PAGES + q] = pages[q];
+        std::memcpy(&srow[slot_page_scale(p->max_pages, q)], &scale, sizeof(float));
+    }
+    // Pages and table row on the copy stream: after every call enqueued on the pool so
+    // far (a free page may still be read by a call enqueued before its unload), and
+    // before every call enqueued from now on.
+    cudaStream_t s = p->copy_stream;
+    if (cudaMemcpyAsync(p->d_page_list, pages, sizeof(int32_t) * npages, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess ||
+        launch_pack_adapter(p->load_A, p->load_B, rank, p->d_page_list, npages, pool_view(p),
+                            p->A_pages, p->B_pages, s) != cudaSuccess ||
+        cudaEventRecord(p->ev_loaded, s) != cudaSuccess) {
+        cudaGetLastError();
+        return LORA_ERR_CUDA;
+    }
+    if ((st = enqueue_row(p, slot, srow)) != LORA_OK) return st;
     p->free_pages.resize(p->free_pages.size() - npages);
-    std::copy(new_row.begin(), new_row.end(), row);
+    std::copy(srow, srow + p->slot_stride, row);
     p->n_loads += 1;
     return LORA_OK;
 }
@@ -524,13 +624,13 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
     if (row[SLOT_RANK] == 0) return LORA_ERR_SLOT_EMPTY;
     if (p->chain_refs[slot] > 0) return LORA_ERR_IN_USE;  // a chain still lists it
     if (slot_is_held(p, slot)) return LORA_ERR_IN_USE;    // acquired from the host tier
-    CUDA_TRY(cudaDeviceSynchronize());
-    std::vector<int32_t> zero(p->slot_stride, 0);
-    if (cudaMemcpyAsync(p->d_slots + (size_t)slot * p->slot_stride, zero.data(),
-                        sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice,
-                        p->copy_stream) != cudaSuccess ||
-        cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
-        return LORA_ERR_CUDA;
+    // the empty row goes in on the copy stream, after the calls enqueued so far; the
+    // pages return to the free list now, and whatever reuses them next writes them on
+    // the same stream, after this
+    int32_t *zero = nullptr;
+    lora_status st = stage_row_ready(p, p->max_adapters, &zero);
+    if (st != LORA_OK) return st;
+    if ((st = enqueue_row(p, slot, zero)) != LORA_OK) return st;
     const int npages = row[SLOT_NPAGES];
     if (row[SLOT_MEMBERS] > 0) {
         // a chain owns no pages: release its members
@@ -575,13 +675,12 @@ lora_status lora_define_chain(lora_pool_t p, int chain_slot, const int *member_s
     new_row[SLOT_NPAGES] = npages;
     new_row[SLOT_SCALE] = p->h_slots[(size_t)member_slots[0] * p->slot_stride + SLOT_SCALE];
     new_row[SLOT_MEMBERS] = n;
-    // calls already enqueued keep seeing the old table
-    CUDA_TRY(cudaDeviceSynchronize());
-    if (cudaMemcpyAsync(p->d_slots + (size_t)chain_slot * p->slot_stride, new_row.data(),
-                        sizeof(int32_t) * p->slot_stride, cudaMemcpyHostToDevice,
-                        p->copy_stream) != cudaSuccess ||
-        cudaStreamSynchronize(p->copy_stream) != cudaSuccess)
-        return LORA_ERR_CUDA;
+    // the row goes in on the copy stream: calls enqueued before see the slot empty
+    int32_t *srow = nullptr;
+    lora_status st = stage_row_ready(p, chain_slot, &srow);
+    if (st != LORA_OK) return st;
+    std::copy(new_row.begin(), new_row.end(), srow);
+    if ((st = enqueue_row(p, chain_slot, srow)) != LORA_OK) return st;
     std::copy(new_row.begin(), new_row.end(), row);
     std::vector<int> &members = p->chain_members[chain_slot];
     members.assign(member_slots, member_slots + n);
@@ -628,6 +727,7 @@ lora_status lora_linear_grouped(int n, const lora_pool_t *pools, const void *con
     }
     for (int m = 0; m < n; ++m) {
         lora_status st = ensure_scratch(pools[m], T);
+        if (st == LORA_OK) st = order_after_changes(pools[m], s);
         if (st != LORA_OK) return st;
     }
     CallMarks marks{pools[0], s};
@@ -708,11 +808,16 @@ lora_status lora_test_delayed_copy(const int32_t *src, int32_t *dst, int n, int 
 lora_status lora_pool_check_errors(lora_pool_t p)
 {
     if (!p) return LORA_ERR_ARG;
-    if (cudaDeviceSynchronize() != cudaSuccess) return LORA_ERR_CUDA;
-    int word = 0;
-    CUDA_TRY(cudaMemcpy(&word, p->d_err, sizeof(int), cudaMemcpyDeviceToHost));
-    CUDA_TRY(cudaMemset(p->d_err, 0, sizeof(int)));
-    CUDA_TRY(cudaDeviceSynchronize());
+    // on the copy stream, which follows every call enqueued on the pool: the word is
+    // read and cleared in one atomic step (a kernel still running on another stream
+    // cannot set a bit between the read and the clear and have it lost)
+    cudaStream_t s = p->copy_stream;
+    read_clear_kernel<<<1, 1, 0, s>>>(p->d_err);
+    if (cudaGetLastError() != cudaSuccess ||
+        cudaMemcpyAsync(p->h_err, p->d_err + 1, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return LORA_ERR_CUDA;
+    const int word = *p->h_err;
     if (word & kErrBadIdBit) return LORA_ERR_BAD_ADAPTER_ID;
     if (word & kErrTimeoutBit) return LORA_ERR_TIMEOUT;
     return LORA_OK;
@@ -732,6 +837,7 @@ lora_status lora_build_segments(lora_pool_t p, const int32_t *ids, int T, int32_
         return LORA_OK;
     }
     lora_status st = ensure_scratch(p, T);
+    if (st == LORA_OK) st = order_after_changes(p, s);
     if (st != LORA_OK) return st;
     const SegTables tabs = seg_tables(p);
     CUDA_TRY(launch_seg_build(ids, T, pool_view(p), tabs, p->d_err, nullptr, 0, s));
@@ -741,7 +847,7 @@ lora_status lora_build_segments(lora_pool_t p, const int32_t *ids, int T, int32_
     CUDA_TRY(cudaMemcpyAsync(num_seg, p->hdr + HDR_NUMSEG, sizeof(int32_t), cudaMemcpyDeviceToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(seg_start, p->seg_start, sizeof(int32_t) * se, cudaMemcpyDeviceToDevice, s));
     CUDA_TRY(cudaMemcpyAsync(seg_slot, p->seg_slot, sizeof(int32_t) * (se - 1), cudaMemcpyDeviceToDevice, s));
-    return LORA_OK;
+    return note_call(p, s);
 }
 
 lora_status lora_pool_stats(lora_pool_t p, int64_t *out)
@@ -785,6 +891,15 @@ lora_status lora_pool_kernel_times(lora_pool_t p, float *ms)
         ms[k] = t;
         prev = k + 1;
     }
+    return LORA_OK;
+}
+
+lora_status lora_pool_set_trace(lora_pool_t p, uint64_t *buf, int n_calls)
+{
+    if (!p || (buf && n_calls < 1)) return LORA_ERR_ARG;
+    p->trace = buf;
+    p->trace_calls = buf ? n_calls : 0;
+    p->trace_k = 0;
     return LORA_OK;
 }
 

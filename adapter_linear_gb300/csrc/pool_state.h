@@ -51,10 +51,20 @@ struct lora_pool {
     std::vector<int32_t> free_pages;  // stack; back() is taken first
     std::vector<int32_t> chain_refs;  // per slot: chains that list it as a member
     std::map<int, std::vector<int>> chain_members;  // chain slot -> member slots
-    int *d_err = nullptr;
-    uint16_t *stage_A = nullptr, *stage_B = nullptr;
+    int *d_err = nullptr;             // [0] the error word, [1] its value at the last read
+    int *h_err = nullptr;             // pinned copy of d_err[1]
+    uint16_t *stage_A = nullptr, *stage_B = nullptr;  // swap-ins of the host tier
+    uint16_t *load_A = nullptr, *load_B = nullptr;    // lora_load_adapter's copy of A, B
     int32_t *d_page_list = nullptr;
+    // Changes of pages and table rows (loads, unloads, chains, swap-ins) run on the
+    // copy stream, which waits for every layer call enqueued on the pool before them;
+    // layer calls enqueued after a change wait for the copy stream (ev_copy).
     cudaStream_t copy_stream = nullptr;
+    cudaStream_t load_stream = nullptr;   // caller's A, B -> load_A, load_B
+    cudaEvent_t ev_loaded = nullptr;      // the last packing of load_A, load_B
+    uint64_t copy_epoch = 0;              // changes enqueued on the copy stream so far
+    uint64_t waited_epoch = 0;            // ... that waited_stream was last made to wait for
+    cudaStream_t waited_stream = nullptr;
     CUtensorMap tmA;   // A arena [num_pages*8 rows x d_in], box 8 x 64
     CUtensorMap tmAw;  // the same, box round16(8 * max_pages) x 64
     CUtensorMap tmB;   // B arena as [num_pages*d_out rows x 8], box 128 x 8, no swizzle
@@ -82,24 +92,30 @@ struct lora_pool {
     cudaEvent_t ev[LORA_KERNEL_SLOTS + 1] = {};
     bool ev_used[LORA_KERNEL_SLOTS] = {};
     int ev_last = 0;  // index of the last event the last timed call recorded
+    // span trace (lora_pool_set_trace): call k of the pool since it was set writes
+    // its kernels' (first entry, last exit) into trace[(k % trace_calls)][slot][2]
+    uint64_t *trace = nullptr;
+    int trace_calls = 0;
+    int64_t trace_k = 0;
     int64_t n_loads = 0, n_unloads = 0, n_calls = 0;
     size_t bytes_held = 0;
 
     // marks each layer call enqueued directly on a stream (not inside a graph
-    // capture) for the copy stream to wait on: asynchronous swap-ins start after it
+    // capture) for the copy stream to wait on: every later change starts after it
     cudaEvent_t ev_call = nullptr;
 
     // host tier (cache.cu): key -> host copy; per slot the cached key it holds
-    // (kNoKey: a manual or empty slot), acquisitions outstanding, last use, and
-    // the swap-in that last wrote it (its pinned staging row is reused only after
-    // that copy has run)
+    // (kNoKey: a manual or empty slot), acquisitions outstanding and last use.
+    // Per slot (all slots, manual ones included): the copy that last wrote its
+    // table row from its pinned staging row (reused only after that copy has run)
     std::unordered_map<int64_t, HostAdapter> host_tier;
     std::vector<int64_t> slot_key;
     std::vector<int32_t> slot_pins;
     std::vector<uint64_t> slot_tick;
     std::vector<cudaEvent_t> slot_copy_ev;
-    int32_t *stage_rows = nullptr;  // pinned [max_adapters][slot_stride + max_pages]
-    cudaEvent_t ev_copy = nullptr;  // the last swap-in enqueued on copy_stream
+    int32_t *stage_rows = nullptr;  // pinned [max_adapters + 1][slot_stride + max_pages];
+                                    // the last row stays all zero (empty slot)
+    cudaEvent_t ev_copy = nullptr;  // the last change enqueued on copy_stream
     uint64_t tick = 0;
     int64_t cache_hits = 0, cache_misses = 0, cache_evictions = 0;
 };
@@ -108,8 +124,17 @@ namespace lora {
 lora_status alloc_dev(lora_pool *p, void **ptr, size_t bytes);
 void free_dev(lora_pool *p, void *ptr, size_t bytes);
 PoolDev pool_view(const lora_pool *p);
-// After a layer call on `stream`: remember it for the swap-ins of the host tier.
+// Before a layer call on `stream`: order it after the page and table changes
+// enqueued on the copy stream so far.
+lora_status order_after_changes(lora_pool *p, cudaStream_t stream);
+// After a layer call on `stream`: later changes on the copy stream wait for it.
 lora_status note_call(lora_pool *p, cudaStream_t stream);
+// The pinned staging row of `slot` (slot == max_adapters: the all-zero row), once
+// the copy that last read it has run.
+lora_status stage_row_ready(lora_pool *p, int slot, int32_t **row);
+// Enqueue the copy of a staging row into the device table row of `slot` on the
+// copy stream; later layer calls are ordered after it.
+lora_status enqueue_row(lora_pool *p, int slot, const int32_t *row);
 // Free the host tier's pinned memory and events (pool destruction).
 void destroy_host_tier(lora_pool *p);
 // A slot the host tier holds for an outstanding acquisition?

@@ -40,9 +40,11 @@ __device__ __forceinline__ int token_key(int id, const PoolDev &pool, bool &bad)
 template <int kSegWarps>
 __global__ void __launch_bounds__(kSegWarps * 32, 1)
     seg_build_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
-                     int *__restrict__ err, int cache_keys, uint16_t *__restrict__ vhl, int ldh)
+                     int *__restrict__ err, int cache_keys, uint16_t *__restrict__ vhl, int ldh,
+                     uint64_t *trace)
 {
     constexpr int kSegThreads = kSegWarps * 32;
+    trace_enter_released(trace);
     extern __shared__ uint32_t seg_smem[];
     const int K = pool.max_adapters + 1;
     uint32_t *cnt = seg_smem;                          // [K][kSegWarps]
@@ -201,6 +203,10 @@ __global__ void __launch_bounds__(kSegWarps * 32, 1)
         }
         if (lane == 0) tabs.tile_info[tile] = hi < 0 ? kTileNoAdapter : (lo == hi ? hi : kTileMixed);
     }
+    if (trace) {
+        __syncthreads();
+        trace_exit(trace);
+    }
 }
 
 }  // namespace
@@ -215,14 +221,14 @@ namespace {
 
 template <int W>
 cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs, int *err,
-                               uint16_t *vhl, int ldh, cudaStream_t stream)
+                               uint16_t *vhl, int ldh, cudaStream_t stream, uint64_t *trace)
 {
     size_t smem = seg_build_smem_bytes(pool.max_adapters, W);
     const int cache_keys = smem + (size_t)T * sizeof(int) <= kSegSmemLimit;
     if (cache_keys) smem += (size_t)T * sizeof(int);
     cudaError_t e = ensure_smem_attr((const void *)seg_build_kernel<W>, smem);
     if (e != cudaSuccess) return e;
-    seg_build_kernel<W><<<1, W * 32, smem, stream>>>(ids, T, pool, tabs, err, cache_keys, vhl, ldh);
+    seg_build_kernel<W><<<1, W * 32, smem, stream>>>(ids, T, pool, tabs, err, cache_keys, vhl, ldh, trace);
     return cudaGetLastError();
 }
 
@@ -231,11 +237,11 @@ cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, S
 // 32 warps (each walks a 32nd of the tokens) when their counters and the cached keys
 // fit in shared memory; 8 warps otherwise (large pools).
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
-                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream)
+                             int *err, uint16_t *vhl, int ldh, cudaStream_t stream, uint64_t *trace)
 {
     if (seg_build_smem_bytes(pool.max_adapters, 32) + (size_t)T * sizeof(int) <= kSegSmemLimit)
-        return launch_seg_build_w<32>(ids, T, pool, tabs, err, vhl, ldh, stream);
-    return launch_seg_build_w<8>(ids, T, pool, tabs, err, vhl, ldh, stream);
+        return launch_seg_build_w<32>(ids, T, pool, tabs, err, vhl, ldh, stream, trace);
+    return launch_seg_build_w<8>(ids, T, pool, tabs, err, vhl, ldh, stream, trace);
 }
 
 }  // namespace lora

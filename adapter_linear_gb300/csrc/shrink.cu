@@ -64,8 +64,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap tmAw,
                      const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
                      uint16_t *__restrict__ Vhl, int ldh, int nmax, int stages, uint32_t tmem_cols,
-                     int *err)
+                     int *err, uint64_t *trace)
 {
+    trace_enter_released(trace);
     extern __shared__ uint8_t shrink_smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(shrink_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem, tmem_cols);
     }
+    trace_exit(trace);
 }
 
 uint32_t pow2_cols(uint32_t n)
@@ -298,7 +300,7 @@ uint32_t pow2_cols(uint32_t n)
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
                              const CUtensorMap &tmAw, const uint16_t *X,
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,
-                             int num_sms, int *err, cudaStream_t stream)
+                             int num_sms, int *err, cudaStream_t stream, uint64_t *trace)
 {
     const int nmax = ((pool.max_pages * kRankPage + 15) / 16) * 16;
     const size_t stage_bytes = kSBoxes * (kXTileBytes + (size_t)nmax * 128);
@@ -314,7 +316,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
     cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
     shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, tmAw, X, pool, tabs, Vhl, ldh, nmax,
-                                                          stages, tmem_cols, err);
+                                                          stages, tmem_cols, err, trace);
     return cudaGetLastError();
 }
 

@@ -108,8 +108,11 @@ typedef enum { LORA_PREFILL_AUTO = 0, LORA_PREFILL_SINGLE = 1, LORA_PREFILL_PAIR
 lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out,
                              lora_pool_t *out);
 
-/* Wait for the pool's in-flight work, then free all its device memory.
- * The handle is invalid afterwards. NULL returns LORA_ERR_ARG. */
+/* Wait for the device to finish all work (every stream: graph replays that
+ * use the pool are not tracked), then free all of the pool's device memory.
+ * The handle is invalid afterwards. NULL returns LORA_ERR_ARG. The pages have
+ * no counterpart for this call beyond the unified pool itself (vLLM tutorial,
+ * "vLLM 的 Multi-LoRA 怎么实现", item 1): it is the pool's destructor. */
 lora_status lora_pool_destroy(lora_pool_t pool);
 
 /*
@@ -131,17 +134,30 @@ lora_status lora_pool_reserve(lora_pool_t pool, int max_tokens);
  *   must be complete before the call (no stream ordering is applied).
  *   alpha: the adapter's scale numerator; the pool stores s = alpha / rank
  *   (fp32), rank being the rank passed here.
- * Host-blocking. Before touching pages or the slot table it waits for every
- * lora_linear call already enqueued on this pool, so earlier calls see the
- * old state. Loading into an occupied slot is an error: a hot swap is
- * unload, then load.
- * Errors: SLOT_RANGE, SLOT_OCCUPIED, RANK, ARG (null A/B), CUDA.
+ * Ordering without a device-wide stall (icman.com.cn Multi-LoRA article,
+ * section 4.2: a cold adapter load must not hold up the requests already
+ * running): the call waits on the host only for its own copy of A and B into
+ * pool-owned memory. The pages and the table row are then written on the
+ * pool's internal copy stream, after every layer call already enqueued on this
+ * pool (on any stream; they keep seeing the old state), and every layer call
+ * enqueued on the pool after the return waits for them on the GPU. Other
+ * streams and other pools are not held up (on the GPU, the changes of a pool
+ * used on the legacy default stream also follow other streams' earlier work:
+ * see lora_pool_check_errors). Calls replayed from a CUDA graph
+ * are not tracked: a graph that uses the pool must have finished (or be
+ * ordered by the caller) before a load, unload or chain definition, and
+ * changes must be made before the capture.
+ * Loading into an occupied slot is an error: a hot swap is unload, then load.
+ * Errors: SLOT_RANGE, SLOT_OCCUPIED, RANK, ARG (null A/B), OOM (no free
+ * pages), CUDA.
  */
 lora_status lora_load_adapter(lora_pool_t pool, int slot, const void *A, const void *B,
                               int rank, float alpha);
 
-/* Unload ("unload_adapter", same sections): waits for enqueued calls, returns
- * the slot's pages to the free list and marks it empty. Host-blocking.
+/* Unload ("unload_adapter", same sections): returns the slot's pages to the
+ * free list and marks it empty. Ordered like a load, without waiting on the
+ * host: calls enqueued on the pool before it still see the adapter, calls
+ * enqueued after it see an empty slot (an id naming it is then a bad id).
  * Unloading a chain slot releases its members and frees no pages; unloading a
  * slot the host tier filled drops it from the cache (the key stays registered).
  * Errors: SLOT_RANGE, SLOT_EMPTY, IN_USE (a chain still lists the adapter, or
@@ -163,7 +179,7 @@ lora_status lora_unload_adapter(lora_pool_t pool, int slot);
  *   member_slots: HOST array of n >= 1 distinct slots that hold adapters (not
  *   chains); their pages together must fit one slot (sum of ceil(r_m / 8)
  *   pages <= ceil(max_rank / 8)). chain_slot must be empty.
- * Host-blocking; like a load, it waits for the calls already enqueued. While
+ * Ordered like a load (calls enqueued before it see an empty chain slot). While
  * a chain lists an adapter, unloading that adapter fails with IN_USE.
  * Errors: ARG (null list, n < 1, a repeated member, a member that is itself a
  * chain or the chain slot), SLOT_RANGE, SLOT_OCCUPIED (chain_slot), SLOT_EMPTY
@@ -312,9 +328,9 @@ lora_status lora_base_linear(lora_pool_t pool, const void *X, const void *W_base
  * callers that must never block on an allocator). It needs no pool and
  * allocates nothing (no cudaMalloc, no cudaFree, no allocating library call):
  * the same decode kernels as lora_base_linear take their split-K scratch from
- * a fixed __device__ array compiled into the library (16 MiB of partial sums
- * plus a 256-byte head), which every GPU that loads the library holds until
- * the process exits.
+ * a fixed __device__ array compiled into the library (16 MiB: 4,194,304 fp32
+ * partial sums), which every GPU that loads the library holds until the
+ * process exits.
  *   X: device bf16 T x d_in, W_base: device bf16 d_out x d_in, Y: device bf16
  *   T x d_out; 0 <= T <= 256; d_in, d_out positive multiples of 8 up to
  *   LORA_MAX_DIM. Asynchronous on `stream`.
@@ -325,18 +341,31 @@ lora_status lora_base_linear(lora_pool_t pool, const void *X, const void *W_base
  * overlap on the GPU (other streams, or concurrent replays) race on it and
  * must be serialised by the caller.
  * Errors: ARG (null pointers, T outside [0, 256]), SHAPE (bad d_in / d_out,
- * or T x d_out too large for the fixed scratch: the call needs
- * 256 * T * G floats with G >= d_out / 128; T = 256 works up to d_out = 8192),
- * UNSUPPORTED (device not compute capability 10.3), CUDA. A kernel wait that
- * times out is not reported by this call.
+ * or T x d_out too large for the fixed scratch). The partial sums take
+ * G * S * T * 128 floats for G CTAs each touching at most S tiles of 128
+ * output rows; when that exceeds the array the call runs with fewer CTAs,
+ * down to one CTA over all ceil(d_out / 128) tiles, so it succeeds exactly
+ * when ceil(d_out / 128) * 128 * T <= 4,194,304 (T = 256: d_out up to 16384;
+ * T = 64: up to 65536). UNSUPPORTED (device not compute capability 10.3),
+ * CUDA. A kernel wait that times out is not reported by this call (the
+ * kernels are given no error word); its Y is then incomplete.
  */
 lora_status lora_base_linear_noalloc(const void *X, const void *W_base, int T, int d_in,
                                      int d_out, void *Y, lora_stream_t stream);
 
 /*
- * Wait for the pool's last enqueued call, read and clear the device error
- * word. Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID or LORA_ERR_TIMEOUT (the
- * first of these present), or LORA_ERR_CUDA if the device reported an error.
+ * Strict-mode report (icman.com.cn Multi-LoRA article, section 4.1: an unknown
+ * adapter must surface as an error, not fall back to the base output
+ * silently). Waits for the layer calls enqueued on this pool (graph replays
+ * are not tracked: synchronise their stream first), then reads and clears the
+ * pool's device error word in one atomic step, so a bit set meanwhile by a
+ * kernel on another stream is never lost. Other streams are not waited for,
+ * with one exception that CUDA defines: an event recorded on the legacy
+ * default stream (NULL) completes only after all earlier work of the context,
+ * so the calls of a pool used on that stream also wait for other streams' work
+ * enqueued before them.
+ * Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID or LORA_ERR_TIMEOUT (the first of
+ * these present), or LORA_ERR_CUDA if the device reported an error.
  */
 lora_status lora_pool_check_errors(lora_pool_t pool);
 
@@ -381,7 +410,10 @@ lora_status lora_test_delayed_copy(const int32_t *src, int32_t *dst, int n, int 
                                    lora_stream_t stream);
 
 /*
- * Test hook: run only the segment builder on device ids[T] and copy its
+ * Test hook: run only the segment builder of the prefill path -- the grouping
+ * of a batch by adapter id of the LoRA-Land blog, section 核心实现解析 / 2.
+ * 多 LoRA 批处理调度 ("Grouped Multi-LoRA Execution": the batch is grouped by
+ * LoRA ID and each group run with its own A, B) -- on device ids[T] and copy its
  * tables out (device pointers): order[T] (token indices stably sorted by id,
  * base-only tokens first), *n_base, *num_seg, seg_start[num_seg + 1] (offsets
  * into order; seg_start[0] = n_base, seg_start[num_seg] = T) and
@@ -395,7 +427,9 @@ lora_status lora_build_segments(lora_pool_t pool, const int32_t *ids, int T, int
 
 /* Pool counters, written to out[0..LORA_STATS_COUNT):
  * loaded slots, free pages, total pages, loads, unloads, linear calls,
- * bytes of device memory held. */
+ * bytes of device memory held. The counterpart in the pages is the startup
+ * check of icman.com.cn Multi-LoRA article, section 4.1 (confirm from the logs
+ * which adapters are loaded); the counters read the host mirror, no GPU work. */
 #define LORA_STATS_COUNT 7
 lora_status lora_pool_stats(lora_pool_t pool, int64_t *out);
 
@@ -411,6 +445,24 @@ lora_status lora_pool_stats(lora_pool_t pool, int64_t *out);
 #define LORA_KERNEL_SLOTS 4
 lora_status lora_pool_enable_timing(lora_pool_t pool, int enable);
 lora_status lora_pool_kernel_times(lora_pool_t pool, float *ms);
+
+/*
+ * Measurement hook that keeps programmatic dependent launch intact (no events
+ * between the kernels; no counterpart in the pages). While buf is set, the
+ * k-th layer call on the pool after this call (k = 0, 1, ...; a grouped call
+ * counts on its first pool) writes, for each kernel it launches, four global
+ * timer values (ns) into
+ *   buf[((k % n_calls) * LORA_KERNEL_SLOTS + slot) * 4 + {0, 1, 2, 3}]
+ * (slots as for lora_pool_kernel_times): {0} its first CTA's entry (atomic
+ * min), {1} its last CTA's exit (atomic max), {2, 3} the first and the last
+ * moment a CTA got past its wait on the kernel before it in the stream (for a
+ * kernel that does not wait, its CTAs' entries). The caller sets each group to
+ * {UINT64_MAX, 0, UINT64_MAX, 0} before the calls and reads them after.
+ * buf: DEVICE memory of n_calls * LORA_KERNEL_SLOTS * 4 uint64. Calls captured
+ * into a CUDA graph keep the entries they were captured with. NULL turns it
+ * off. Errors: ARG (n_calls < 1 with a buffer).
+ */
+lora_status lora_pool_set_trace(lora_pool_t pool, uint64_t *buf, int n_calls);
 
 /* Force a kernel family (lora_path); LORA_PATH_AUTO restores the default. */
 lora_status lora_pool_set_path(lora_pool_t pool, int path);

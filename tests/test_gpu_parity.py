@@ -105,35 +105,6 @@ def test_llama3_modules(module):
         assert_parity(got_p, ref, f"llama3/{module}/prefill")
 
 
-def prefill_rows(T, seq_len):
-    rows = set()
-    for s in range(0, T, seq_len):
-        rows.update([s, s + 1, s + 127, s + 128, s + seq_len // 2, s + seq_len - 1])
-    return np.array(sorted(r for r in rows if r < T))
-
-
-def test_prefill_mixed_ranks_and_padding():
-    prob = L.prefill_mixed()
-    pool = load_pool(al, prob)
-    Y = run_dev(pool, prob, PATHS["prefill"])
-    rows = prefill_rows(prob.T, 2048)
-    got = to_host_f64(Y[torch.from_numpy(rows).cuda()])
-    ref, base = ref_of(prob, rows)
-    assert_parity(got, ref, "prefill sampled rows")
-    assert_routing(got, ref, base, prob.ids[rows], "prefill sampled rows")
-    pool.close()
-
-    padded = L.prefill_mixed(padded=True)
-    pool_p = load_pool(al, padded)
-    Yp = run_dev(pool_p, padded, PATHS["prefill"])
-    # zero padding only adds exact zeros: the whole output agrees within tolerance
-    a, b = Yp.float(), Y.float()
-    assert bool(torch.all((a - b).abs() <= 1e-2 + 1e-2 * b.abs()))
-    ref_p, _ = ref_of(padded, rows)
-    assert np.array_equal(ref_p, ref)  # the oracle: bitwise
-    assert_parity(to_host_f64(Yp[torch.from_numpy(rows).cuda()]), ref_p, "padded sampled rows")
-
-
 def test_hotswap_stream():
     prob, sched = L.hotswap()
     pool = load_pool(al, prob)
@@ -141,7 +112,6 @@ def test_hotswap_stream():
     current = dict(prob.adapters)
     swaps = {c: (slot, gen) for c, slot, gen in sched.swaps}
     check = {0, sched.calls - 1} | {c + 1 for c in swaps} | set(range(0, sched.calls, 100))
-    rows = np.arange(0, prob.T, 17)
     pool.set_path(1)
     outs, states = {}, {}
     for c in range(sched.calls):
@@ -160,8 +130,8 @@ def test_hotswap_stream():
     for c in sorted(outs):
         p = L.Problem("hs", prob.d_in, prob.d_out, prob.X, prob.W, sched.ids[c], states[c],
                       prob.max_adapters, prob.max_rank, prob.seed)
-        ref, _ = ref_of(p, rows)
-        assert_parity(to_host_f64(outs[c])[rows], ref, f"hotswap call {c}")
+        ref, _ = ref_of(p)
+        assert_parity(to_host_f64(outs[c]), ref, f"hotswap call {c}")
     assert pool.stats()["loads"] == 2000 + len(sched.swaps)
 
 
