@@ -756,22 +756,7 @@ template <int NP>
 DecodePlanT<NP> narrow_plan(const DecodePlan &p)
 {
     DecodePlanT<NP> q{};
-    q.n = p.n;
-    q.T = p.T;
-    q.ntok = p.ntok;
-    q.U = p.U;
-    q.G = p.G;
-    q.grid = p.grid;
-    q.max_seg = p.max_seg;
-    q.n_acc = p.n_acc;
-    q.stages = p.stages;
-    q.pairs = p.pairs;
-    q.col_blocks = p.col_blocks;
-    q.tight = p.tight;
-    q.prefetch_a = p.prefetch_a;
-    q.trace = p.trace;
-    q.tmem_cols = p.tmem_cols;
-    q.smem_bytes = p.smem_bytes;
+    static_cast<DecodePlanHead &>(q) = static_cast<const DecodePlanHead &>(p);
     for (int m = 0; m < NP; ++m) q.prob[m] = p.prob[m];
     return q;
 }

@@ -279,13 +279,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         idesc, (kb | kk) != 0);
                     } else {
                         // A: [hi j0..15 | hi j16..31 | lo j0..15 | lo j16..31]; B: page slices
-                        // (0,1) hold j0..15, (2,3) hold j16..31
+                        // (0,1) hold j0..15, (2,3) hold j16..31. When the block's pages 2,3
+                        // are past the adapter (zero pages), their two K-steps add nothing.
+                        const bool upper = (kb - a.KB) * kPagesPerBlock + 2 < tl.npages;
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32),
-                                        sdesc_k_none(wa + (kk & 1) * 2 * kPageSliceBytes,
-                                                     kPageSliceBytes, 128),
-                                        idesc, 1u);
+                            if (!(kk & 1) || upper)
+                                mma_bf16_ss(d, sdesc_k_sw128(xa + kk * 32),
+                                            sdesc_k_none(wa + (kk & 1) * 2 * kPageSliceBytes,
+                                                         kPageSliceBytes, 128),
+                                            idesc, 1u);
                     }
                     mma_commit(&empty[s]);
                 }
@@ -641,11 +644,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < kPKps; ++j) {
                             if (j >= nj) break;
                             const uint32_t xa = sa + j * kPBlockBytes, wa = xa + kPHalfBytes;
+                            // (the single-CTA kernel's layout; the zero pages' K-steps skipped)
+                            const int e = (st - sb) * kPKps + j;
+                            const bool upper = e * kPagesPerBlock + 2 < cur.tl.npages;
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32),
-                                                 sdesc_k_none(wa + (kk & 1) * 2 * kPSliceBytes, kPSliceBytes, 128),
-                                                 idesc, 1u);
+                                if (!(kk & 1) || upper)
+                                    mma_bf16_ss_pair(d, sdesc_k_sw128(xa + kk * 32),
+                                                     sdesc_k_none(wa + (kk & 1) * 2 * kPSliceBytes, kPSliceBytes, 128),
+                                                     idesc, 1u);
                         }
                     }
                     mma_commit_pair(&empty[s], 0x3);

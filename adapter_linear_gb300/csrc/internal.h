@@ -54,7 +54,13 @@ struct SegTables {
     int32_t *tile_info;  // [ceil(T / 128)]  adapters of each 128-token tile in token
                          // order: the slot if all its tokens with an adapter share one,
                          // kTileNoAdapter, or kTileMixed
+    // the multi-CTA builder's scratch (nullptr: the single-CTA builder runs)
+    int32_t *keys;       // [T] sort key of every token (id + 1, 0 = base only)
+    int32_t *chist;      // [K][chunks] tokens per (key, chunk), then [K] first position per key
+    int32_t *ticket;     // [1] chunks done (zero between calls)
 };
+constexpr int kSegChunk = 256;       // tokens per CTA of the multi-CTA segment builder
+constexpr int kSegMultiMaxKeys = 1024;  // keys (max_adapters + 1) up to which it is used
 constexpr int kTileNoAdapter = -1;
 constexpr int kTileMixed = -2;
 
@@ -109,12 +115,10 @@ struct DecodeProblem {
     int col_blk_begin;      // first block of the finishing grid
 };
 
-// The plan of one decode call. Kernels take a copy sized for the problems it
-// holds (NP = 1 for a single layer, kMaxGroup otherwise) to keep their
-// parameter block small.
-template <int NP>
-struct DecodePlanT {
-    static constexpr int kNP = NP;
+// The plan of one decode call: the fields below, then its problem table. Kernels
+// take a copy sized for the problems it holds (NP = 1 for a single layer,
+// kMaxGroup otherwise) to keep their parameter block small.
+struct DecodePlanHead {
     int n, T, ntok;
     int U, G;               // units, CTAs (stream-K ranges)
     int grid;               // CTAs launched (>= G: the rest only run shrink pairs)
@@ -128,6 +132,11 @@ struct DecodePlanT {
     uint64_t *trace;        // measurement hook: LORA_KERNEL_SLOTS x 4 words (see trace_enter), or nullptr
     uint32_t tmem_cols;
     size_t smem_bytes;
+};
+
+template <int NP>
+struct DecodePlanT : DecodePlanHead {
+    static constexpr int kNP = NP;
     DecodeProblem prob[NP];
 };
 using DecodePlan = DecodePlanT<kMaxGroup>;

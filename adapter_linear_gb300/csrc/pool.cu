@@ -109,6 +109,15 @@ namespace {
 
 size_t seg_entries(const lora_pool *p, int T) { return (size_t)std::min(T, p->max_adapters) + 1; }
 
+// The multi-CTA segment builder's count table: (key, chunk) counts, then one row of
+// first positions (pools of up to kSegMultiMaxKeys keys; else 0: not used).
+size_t seg_chist_ints(const lora_pool *p, int T)
+{
+    const size_t K = (size_t)p->max_adapters + 1;
+    if (K > (size_t)kSegMultiMaxKeys) return 0;
+    return K * ((size_t)(T + kSegChunk - 1) / kSegChunk + 1);
+}
+
 void free_scratch(lora_pool *p)
 {
     const int T = p->cap_T;
@@ -120,6 +129,10 @@ void free_scratch(lora_pool *p)
     free_dev(p, p->seg_ublk, sizeof(int32_t) * seg_entries(p, T));
     free_dev(p, p->tile_info, sizeof(int32_t) * (size_t)((T + 127) / 128));
     p->tile_info = nullptr;
+    free_dev(p, p->seg_keys, sizeof(int32_t) * T);
+    free_dev(p, p->seg_chist, sizeof(int32_t) * seg_chist_ints(p, T));
+    free_dev(p, p->seg_ticket, sizeof(int32_t));
+    p->seg_keys = p->seg_chist = p->seg_ticket = nullptr;
     free_dev(p, p->V, sizeof(float) * (size_t)T * p->ldv);
     free_dev(p, p->Vhl, sizeof(uint16_t) * (size_t)T * p->ldh);
     p->Vhl = nullptr;
@@ -158,6 +171,15 @@ lora_status ensure_scratch(lora_pool *p, int T)
     }
     p->cap_T = T;
     p->partials_floats = pf;
+    if (seg_chist_ints(p, T) > 0) {
+        if ((st = alloc_dev(p, (void **)&p->seg_keys, sizeof(int32_t) * T)) ||
+            (st = alloc_dev(p, (void **)&p->seg_chist, sizeof(int32_t) * seg_chist_ints(p, T))) ||
+            (st = alloc_dev(p, (void **)&p->seg_ticket, sizeof(int32_t)))) {
+            free_scratch(p);
+            return st;
+        }
+        CUDA_TRY(cudaMemset(p->seg_ticket, 0, sizeof(int32_t)));
+    }
     return LORA_OK;
 }
 
@@ -170,6 +192,9 @@ SegTables seg_tables(const lora_pool *p)
     t.seg_slot = p->seg_slot;
     t.seg_ublk = p->seg_ublk;
     t.tile_info = p->tile_info;
+    t.keys = p->seg_keys;
+    t.chist = p->seg_chist;
+    t.ticket = p->seg_ticket;
     return t;
 }
 

@@ -74,6 +74,7 @@ struct lora_pool {
     int cap_T = 0;
     int32_t *order = nullptr, *hdr = nullptr, *seg_start = nullptr, *seg_slot = nullptr,
             *seg_ublk = nullptr, *tile_info = nullptr;
+    int32_t *seg_keys = nullptr, *seg_chist = nullptr, *seg_ticket = nullptr;  // multi-CTA builder
     float *V = nullptr;
     uint16_t *Vhl = nullptr;
     float *partials = nullptr;

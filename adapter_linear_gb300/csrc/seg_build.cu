@@ -13,6 +13,16 @@
 //   C. each warp walks its chunk again in token order and scatters; within a
 //      32-token step equal keys are ranked by lane, so ties keep token order.
 // The result is unique (a stable sort), so it is compared bit for bit.
+//
+// For pools of up to kSegMultiMaxKeys keys the same tables come from two kernels
+// spread over the SMs (one CTA alone is bound by its own instruction issue):
+//   1. seg_count_kernel, one CTA per kSegChunk tokens: keys, the chunk's per-key
+//      counts, the per-tile adapter table and the zeroed shrink rows; the last CTA
+//      to finish (an atomic ticket, nothing waits) turns the counts into each
+//      (key, chunk)'s first position by a scan over chunks and then over keys, and
+//      writes the segment tables;
+//   2. seg_scatter_kernel, one CTA per chunk: its warps place their tokens in turn,
+//      ties ranked by lane, so the order is stable across and within chunks.
 #include "device_common.cuh"
 
 namespace lora {
@@ -57,9 +67,35 @@ __global__ void __launch_bounds__(kSegWarps * 32, 1)
     for (int i = tid; i < K * kSegWarps; i += kSegThreads) cnt[i] = 0;
     if (tid == 0) any_bad = 0;
     bool bad = false;
-    // keys computed once, by all threads in parallel (independent loads), when they fit
-    if (cache_keys)
-        for (int t = tid; t < T; t += kSegThreads) keys[t] = token_key(ids[t], pool, bad);
+    // keys computed once, by all threads in parallel, when they fit: each thread loads
+    // kKeyBatch ids, then their slots' rank words, with all loads of a batch in flight
+    // (two dependent round trips per batch instead of two per token)
+    if (cache_keys) {
+        constexpr int kKeyBatch = 8;
+        for (int t0 = tid; t0 < T; t0 += kSegThreads * kKeyBatch) {
+            int id[kKeyBatch], rk[kKeyBatch];
+#pragma unroll
+            for (int j = 0; j < kKeyBatch; ++j) {
+                const int t = t0 + j * kSegThreads;
+                id[j] = t < T ? ids[t] : -1;
+            }
+#pragma unroll
+            for (int j = 0; j < kKeyBatch; ++j)
+                rk[j] = (id[j] >= 0 && id[j] < pool.max_adapters)
+                            ? pool.slots[(size_t)id[j] * pool.slot_stride + SLOT_RANK] : 0;
+#pragma unroll
+            for (int j = 0; j < kKeyBatch; ++j) {
+                const int t = t0 + j * kSegThreads;
+                if (t >= T) continue;
+                int key = 0;  // as token_key: -1 -> 0, a loaded slot -> id + 1, else bad
+                if (id[j] != -1) {
+                    if (rk[j] > 0) key = id[j] + 1;
+                    else bad = true;
+                }
+                keys[t] = key;
+            }
+        }
+    }
     __syncthreads();
 
     const int chunk = (T + kSegWarps - 1) / kSegWarps;
@@ -209,6 +245,194 @@ __global__ void __launch_bounds__(kSegWarps * 32, 1)
     }
 }
 
+// ------------------------------------------------------- multi-CTA builder
+
+// Exclusive scan of (tokens, segments, 128-row units) over the K keys by all
+// kSegChunk threads of the CTA, key 0 (base only) forming no segment; the segment
+// tables and the header are written, and `first` receives each key's first position.
+__device__ __forceinline__ void scan_keys(const int *total, int K, int T, SegTables tabs, int *first)
+{
+    constexpr int kWarps = kSegChunk / 32;
+    __shared__ uint32_t warp_tot[3][kWarps];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int per = (K + kSegChunk - 1) / kSegChunk;
+    const int k_lo = min(K, tid * per), k_hi = min(K, k_lo + per);
+    uint32_t sc = 0, ss = 0, su = 0;
+    for (int k = k_lo; k < k_hi; ++k) {
+        const uint32_t tot = (uint32_t)total[k];
+        sc += tot;
+        if (k >= 1 && tot > 0) {
+            ss += 1;
+            su += (tot + kShrinkRows - 1) / kShrinkRows;
+        }
+    }
+    uint32_t ic = sc, is = ss, iu = su;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t c = __shfl_up_sync(0xffffffffu, ic, o);
+        const uint32_t v = __shfl_up_sync(0xffffffffu, is, o);
+        const uint32_t u = __shfl_up_sync(0xffffffffu, iu, o);
+        if (lane >= o) {
+            ic += c;
+            is += v;
+            iu += u;
+        }
+    }
+    if (lane == 31) {
+        warp_tot[0][warp] = ic;
+        warp_tot[1][warp] = is;
+        warp_tot[2][warp] = iu;
+    }
+    __syncthreads();
+    uint32_t wc = 0, ws = 0, wu = 0, all_s = 0, all_u = 0;
+    for (int w = 0; w < kWarps; ++w) {
+        if (w < warp) {
+            wc += warp_tot[0][w];
+            ws += warp_tot[1][w];
+            wu += warp_tot[2][w];
+        }
+        all_s += warp_tot[1][w];
+        all_u += warp_tot[2][w];
+    }
+    uint32_t pc = wc + ic - sc, ps = ws + is - ss, pu = wu + iu - su;  // exclusive
+    for (int k = k_lo; k < k_hi; ++k) {
+        const uint32_t tot = (uint32_t)total[k];
+        first[k] = (int)pc;
+        if (k >= 1 && tot > 0) {
+            tabs.seg_start[ps] = (int32_t)pc;
+            tabs.seg_slot[ps] = k - 1;
+            tabs.seg_ublk[ps] = (int32_t)pu;
+            ps += 1;
+            pu += (tot + kShrinkRows - 1) / kShrinkRows;
+        }
+        pc += tot;
+    }
+    if (tid == 0) {
+        tabs.hdr[HDR_NBASE] = total[0];
+        tabs.hdr[HDR_NUMSEG] = (int32_t)all_s;
+        tabs.hdr[HDR_UNITS] = (int32_t)all_u;
+        tabs.seg_start[all_s] = T;
+        tabs.seg_ublk[all_s] = (int32_t)all_u;
+    }
+}
+
+__global__ void __launch_bounds__(kSegChunk)
+    seg_count_kernel(const int32_t *__restrict__ ids, int T, PoolDev pool, SegTables tabs,
+                     int *__restrict__ err, uint16_t *__restrict__ vhl, int ldh, uint64_t *trace)
+{
+    trace_enter_released(trace);
+    constexpr int kWarps = kSegChunk / 32;
+    extern __shared__ int hist[];  // [K]: this chunk's counts, then (last CTA) the totals
+    __shared__ int lo_w[kWarps], hi_w[kWarps];
+    __shared__ int is_last;
+    const int K = pool.max_adapters + 1, chunks = (int)gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int k = tid; k < K; k += kSegChunk) hist[k] = 0;
+    __syncthreads();
+
+    const int t = (int)blockIdx.x * kSegChunk + tid;
+    bool bad = false;
+    int key = -1;
+    if (t < T) {
+        key = token_key(ids[t], pool, bad);
+        tabs.keys[t] = key;
+        atomicAdd(&hist[key], 1);
+        if (key == 0 && vhl != nullptr) {  // the expand reads these rows inside one-adapter tiles
+            uint4 *row = reinterpret_cast<uint4 *>(vhl + (size_t)t * ldh);
+            for (int i = 0; i < ldh / 8; ++i) row[i] = make_uint4(0, 0, 0, 0);
+        }
+    }
+    if (bad) atomicOr(err, kErrBadIdBit);
+    // adapters of the chunk's two 128-token tiles (four warps each)
+    int lo = key > 0 ? key - 1 : 0x7fffffff, hi = key > 0 ? key - 1 : -1;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) {
+        lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        hi = max(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+    if (lane == 0) {
+        lo_w[warp] = lo;
+        hi_w[warp] = hi;
+    }
+    __syncthreads();
+    if (tid < kSegChunk / 128) {
+        const int tile = (int)blockIdx.x * (kSegChunk / 128) + tid;
+        if (tile * 128 < T) {
+            int l = 0x7fffffff, h = -1;
+            for (int w = tid * 4; w < tid * 4 + 4; ++w) {
+                l = min(l, lo_w[w]);
+                h = max(h, hi_w[w]);
+            }
+            tabs.tile_info[tile] = h < 0 ? kTileNoAdapter : (l == h ? h : kTileMixed);
+        }
+    }
+    for (int k = tid; k < K; k += kSegChunk) tabs.chist[(size_t)k * chunks + blockIdx.x] = hist[k];
+
+    // the last chunk to finish turns the counts into positions
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) is_last = atomicAdd(tabs.ticket, 1) == chunks - 1;
+    __syncthreads();
+    if (!is_last) {
+        trace_exit(trace);
+        return;
+    }
+    __threadfence();
+    // per key: exclusive scan over the chunks (a warp per key, 32 chunks per step),
+    // the key's total into hist[]
+    for (int k = warp; k < K; k += kWarps) {
+        int32_t *row = tabs.chist + (size_t)k * chunks;
+        int carry = 0;
+        for (int c0 = 0; c0 < chunks; c0 += 32) {
+            const int c = c0 + lane;
+            const int v = c < chunks ? __ldcg(row + c) : 0;
+            int inc = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int n = __shfl_up_sync(0xffffffffu, inc, o);
+                if (lane >= o) inc += n;
+            }
+            if (c < chunks) row[c] = carry + inc - v;
+            carry += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) hist[k] = carry;
+    }
+    __syncthreads();
+    scan_keys(hist, K, T, tabs, tabs.chist + (size_t)K * chunks);
+    if (tid == 0) *tabs.ticket = 0;  // for the next call (after this kernel completes)
+    __syncthreads();
+    trace_exit(trace);
+}
+
+__global__ void __launch_bounds__(kSegChunk)
+    seg_scatter_kernel(int T, int K, SegTables tabs, uint64_t *trace)
+{
+    trace_enter_released(trace);
+    constexpr int kWarps = kSegChunk / 32;
+    extern __shared__ int run[];  // [K] the next position of each key in this chunk
+    const int chunks = (int)gridDim.x;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t *first = tabs.chist + (size_t)K * chunks;
+    for (int k = tid; k < K; k += kSegChunk) run[k] = first[k] + tabs.chist[(size_t)k * chunks + blockIdx.x];
+    const int t = (int)blockIdx.x * kSegChunk + tid;
+    const int key = t < T ? tabs.keys[t] : 0;
+    __syncthreads();
+    // warps in turn (token order), lanes ranked within a warp: a stable order
+    for (int w = 0; w < kWarps; ++w) {
+        if (warp == w) {
+            const unsigned active = __ballot_sync(0xffffffffu, t < T);
+            if (t < T) {
+                const unsigned same = __match_any_sync(active, key);
+                tabs.order[run[key] + __popc(same & lanemask_lt())] = t;
+                __syncwarp(active);
+                if (lane == __ffs(same) - 1) run[key] += __popc(same);
+            }
+        }
+        __syncthreads();
+    }
+    trace_exit(trace);
+}
+
 }  // namespace
 
 size_t seg_build_smem_bytes(int max_adapters, int warps)
@@ -239,6 +463,17 @@ cudaError_t launch_seg_build_w(const int32_t *ids, int T, const PoolDev &pool, S
 cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, SegTables tabs,
                              int *err, uint16_t *vhl, int ldh, cudaStream_t stream, uint64_t *trace)
 {
+    const int K = pool.max_adapters + 1;
+    if (tabs.chist != nullptr && K <= kSegMultiMaxKeys) {
+        const int chunks = (T + kSegChunk - 1) / kSegChunk;
+        const size_t smem = (size_t)K * sizeof(int);
+        cudaError_t e = ensure_smem_attr((const void *)seg_count_kernel, smem);
+        if (e == cudaSuccess) e = ensure_smem_attr((const void *)seg_scatter_kernel, smem);
+        if (e != cudaSuccess) return e;
+        seg_count_kernel<<<chunks, kSegChunk, smem, stream>>>(ids, T, pool, tabs, err, vhl, ldh, trace);
+        seg_scatter_kernel<<<chunks, kSegChunk, smem, stream>>>(T, K, tabs, trace);
+        return cudaGetLastError();
+    }
     if (seg_build_smem_bytes(pool.max_adapters, 32) + (size_t)T * sizeof(int) <= kSegSmemLimit)
         return launch_seg_build_w<32>(ids, T, pool, tabs, err, vhl, ldh, stream, trace);
     return launch_seg_build_w<8>(ids, T, pool, tabs, err, vhl, ldh, stream, trace);

@@ -405,18 +405,6 @@ class Kit:
             out.append(self.time_once(prog))
         return out
 
-    def overhead(self, base_prog, lora_prog, min_ms=MIN_TIMED_MS):
-        """LoRA and base-only programs in the order base, LoRA, LoRA, base, repeated until
-        min_ms of LoRA time: both kinds see the same clocks on average."""
-        b, l_ = [], []
-        base_prog()
-        while len(l_) < 4 or sum(l_) < min_ms:
-            b.append(self.time_once(base_prog))
-            l_.append(self.time_once(lora_prog))
-            l_.append(self.time_once(lora_prog))
-            b.append(self.time_once(base_prog))
-        return sum(l_) / len(l_), sum(b) / len(b)
-
     def spans(self, calls_of_pools, capture_fn, K, R, replays=3):
         """Per-kernel times from the span trace of one K-step program.
 
@@ -446,6 +434,8 @@ class Kit:
         span = {s: [] for s in KERNEL_SLOTS}
         active = {s: [] for s in KERNEL_SLOTS}
         windows = []
+        periods = {}  # step index -> its periods (last exit minus the step before's), ms
+        step_share = {}  # step index -> {kernel slot -> its shares}
         big = 2 ** 63 - 1
         for _ in range(replays):
             buf[..., 0].fill_(big)
@@ -467,9 +457,11 @@ class Kit:
                 if not u or not up:
                     continue
                 prev_exit = ep[up[-1], 1]
+                periods.setdefault(k, []).append((e[u[-1], 1] - prev_exit) * 1e-6)
                 for si in u:
                     name = KERNEL_SLOTS[si]
                     share[name].append((e[si, 1] - prev_exit) * 1e-6)
+                    step_share.setdefault(k, {}).setdefault(name, []).append((e[si, 1] - prev_exit) * 1e-6)
                     span[name].append((e[si, 1] - e[si, 0]) * 1e-6)
                     active[name].append((e[si, 1] - e[si, 2]) * 1e-6)
                     prev_exit = e[si, 1]
@@ -478,7 +470,43 @@ class Kit:
         def means(d):
             return {s: (statistics.mean(v) if v else 0.0) for s, v in d.items()}
         return {"share": means(share), "span": means(span), "active": means(active),
-                "step_window": statistics.mean(windows) if windows else 0.0}
+                "step_window": statistics.mean(windows) if windows else 0.0, "periods": periods,
+                "step_share": step_share}
+
+    def paired_overhead(self, pools, capture_alt, K, R):
+        """LoRA overhead from one graph whose steps alternate base-only (even k) and LoRA
+        (odd k) calls: every step's period comes from the span trace, so both kinds are
+        measured under the same clocks (a long prefill run lowers them under the power
+        cap). Returns (LoRA / base - 1, mean LoRA period, mean base period) in ms."""
+        tr = self.spans(pools, capture_alt, K, R, replays=5)
+        lo = [v for k, vs in tr["periods"].items() if k % 2 == 1 for v in vs]
+        ba = [v for k, vs in tr["periods"].items() if k % 2 == 0 for v in vs]
+        if not lo or not ba:
+            return None, None, None, {}
+        ml, mb = statistics.mean(lo), statistics.mean(ba)
+
+        def by_kernel(parity):
+            acc = {}
+            for k, d in tr["step_share"].items():
+                if k % 2 == parity:
+                    for name, vs in d.items():
+                        acc.setdefault(name, []).extend(vs)
+            return {name: statistics.mean(vs) for name, vs in acc.items()}
+        return ml / mb - 1.0, ml, mb, {"lora": by_kernel(1), "base": by_kernel(0)}
+
+    def replay_overhead(self, base_prog, lora_prog, min_ms=MIN_TIMED_MS):
+        """LoRA and base-only K-step graphs replayed in the order base, LoRA, LoRA, base
+        until min_ms of LoRA time (decode steps overlap their neighbours under
+        programmatic dependent launch, so their periods cannot be paired step by step;
+        they are short enough not to move the clocks). Returns mean ms per replay."""
+        b, l_ = [], []
+        base_prog()
+        while len(l_) < 4 or sum(l_) < min_ms:
+            b.append(self.time_once(base_prog))
+            l_.append(self.time_once(lora_prog))
+            l_.append(self.time_once(lora_prog))
+            b.append(self.time_once(base_prog))
+        return sum(l_) / len(l_), sum(b) / len(b)
 
     def iso_call(self, one_step, n):
         prog = self.capture(lambda k: one_step(), 1)
@@ -562,7 +590,6 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
         base_step(k)
     kit.barrier()
     lora_prog = kit.capture(lora_step, K)
-    base_prog = kit.capture(base_step, K)
     kit.capture(lora_step, args.warmup)()
     kit.barrier()
 
@@ -574,8 +601,25 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
     total_ms = statistics.median(reps)
     value = job_tokens_per_s(p.T * K, kit.ws, total_ms)
 
-    lora_ms, base_ms = kit.overhead(base_prog, lora_prog)
-    overhead = lora_ms / base_ms - 1.0
+    def alt_step(k):  # even steps base-only, odd steps LoRA
+        (base_step if k % 2 == 0 else lora_step)(k)
+
+    decode = p.T <= 256
+    Kp = max(K, 20)
+    paired_kernels = None
+    if decode:
+        base_prog = kit.capture(base_step, K)
+        lora_rep, base_rep = kit.replay_overhead(base_prog, lora_prog)
+        lora_ms, base_ms = lora_rep / K, base_rep / K
+        overhead = lora_ms / base_ms - 1.0
+        overhead_how = ("base-only, LoRA, LoRA, base-only replays of the K-step graphs, repeated "
+                        f"to >= {MIN_TIMED_MS:.0f} ms of LoRA time")
+    else:
+        overhead, lora_ms, base_ms, paired_kernels = kit.paired_overhead(
+            [pool for pool, _ in layers], lambda: kit.capture(alt_step, Kp), Kp, R)
+        overhead_how = (f"one graph of {Kp} steps alternating base-only and LoRA calls (5 "
+                        "replays); each step's period from the span trace, so both kinds run "
+                        "under the same clocks")
     tr = kit.spans([pool for pool, _ in layers], lambda: kit.capture(lora_step, K), K, R)
     base_tr = kit.spans([pool for pool, _ in layers], lambda: kit.capture(base_step, K), K, R)
     iso_ms = kit.iso_call(lambda: lora_step(0), min(K, 50))
@@ -605,7 +649,6 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
     kit.barrier()
 
     ab = algorithmic_bytes(p)
-    decode = p.T <= 256
     step_ms = total_ms / K
     gemm_share = tr["share"]["base_gemm"]
     if decode:
@@ -626,7 +669,7 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
                      "frac": fl / (step_ms * 1e-3) / 1e12 / kit.peaks["bf16_tflops"],
                      "algorithmic_flops": fl,
                      "per_unit": "2 T d_in d_out + the low-rank flops of every adapter token"}
-    extra_ms = lora_ms / K - base_ms / K
+    extra_ms = lora_ms - base_ms
     rec = {
         "metric": METRIC, "value": value, "unit": UNIT, "ms_per_step": step_ms,
         "tokens_per_step": p.T,
@@ -642,9 +685,10 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
                            else (algorithmic_flops(p) - 2.0 * p.T * p.d_in * p.d_out) /
                            (2.0 * p.T * p.d_in * p.d_out)),
         "overhead_floor_kind": "adapter bytes / base bytes" if decode else "LoRA flops / base flops",
-        "base_only_ms_per_step": base_ms / K,
-        "overhead_measured_on": "base-only, LoRA, LoRA, base-only replays of the K-step graphs, "
-                                f"repeated to >= {MIN_TIMED_MS:.0f} ms of LoRA time",
+        "base_only_ms_per_step": base_ms,
+        "lora_ms_per_step_in_overhead_run": lora_ms,
+        "overhead_measured_on": overhead_how,
+        "paired_kernel_ms": paired_kernels,
         "isolated_call_ms": iso_ms,
         "adapter_path_gbs": ab["adapters"] / (extra_ms * 1e-3) / 1e9 if (decode and extra_ms > 0) else None,
         "kernel_ms": {k: v for k, v in tr["share"].items() if v > 0},
@@ -723,7 +767,6 @@ def measure_grouped_layer(kit: Kit, K: int):
         grouped_base_step(k)
     kit.barrier()
     g_prog = kit.capture(grouped_step, K)
-    gb_prog = kit.capture(grouped_base_step, K)
     s_prog = kit.capture(separate_step, K)
     kit.capture(grouped_step, args.warmup)()
     kit.barrier()
@@ -733,7 +776,10 @@ def measure_grouped_layer(kit: Kit, K: int):
         reps = kit.time_replays(g_prog)
     total_ms = statistics.median(reps)
     sep_ms = statistics.median(kit.time_replays(s_prog))
-    lora_ms, base_ms = kit.overhead(gb_prog, g_prog)
+    gb_prog = kit.capture(grouped_base_step, K)
+    lora_rep, base_rep = kit.replay_overhead(gb_prog, g_prog)
+    lora_ms, base_ms = lora_rep / K, base_rep / K
+    overhead = lora_ms / base_ms - 1.0
     tr = kit.spans([pools[0] for pools, _ in layers], lambda: kit.capture(grouped_step, K), K, R)
 
     # e2e: pinned host inputs copied in, the grouped call, outputs copied back
@@ -790,9 +836,10 @@ def measure_grouped_layer(kit: Kit, K: int):
         "timing": {"replays": len(reps), "replay_ms_median": total_ms,
                    "rule": f"median of replays of the K-step graph, >= {MIN_TIMED_MS:.0f} ms timed"},
         "separate_calls_ms_per_step": sep_ms / K,
-        "base_only_ms_per_step": base_ms / K,
-        "overhead_vs_base": lora_ms / base_ms - 1.0,
-        "overhead_measured_on": "grouped base-only, LoRA, LoRA, base-only replays",
+        "base_only_ms_per_step": base_ms,
+        "overhead_vs_base": overhead,
+        "overhead_measured_on": "grouped base-only, LoRA, LoRA, base-only replays of the K-step "
+                                f"graphs, repeated to >= {MIN_TIMED_MS:.0f} ms of LoRA time",
         "overhead_floor": ad_all / (w_b + x_b + y_b),
         "overhead_floor_kind": "adapter bytes / base bytes",
         "kernel_ms": {k: v for k, v in tr["share"].items() if v > 0},

@@ -147,8 +147,11 @@ def seg_cases():
     cases.append(("max_slot", np.array([49, -1, 49, 0, 49] * 20, np.int32), 50))
     cases.append(("zipf", L.zipf_ids(5, 4096, 2000), 2000))
     cases.append(("sorted_runs", np.repeat(np.arange(8, dtype=np.int32), 2048), 8))
-    # too many tokens for 32 warps' counters and cached keys: 8 warps, keys not cached
+    # many chunks of the multi-CTA builder (235 x 256 tokens)
     cases.append(("rand60000", g.integers(-1, 50, size=60000).astype(np.int32), 50))
+    # more keys than the multi-CTA builder takes (1101 > 1024): one CTA of 32 warps;
+    # the Zipf case above (2001 keys) runs the 8-warp single-CTA builder
+    cases.append(("wide_pool", g.integers(-1, 1100, size=3000).astype(np.int32), 1100))
     return cases
 
 
