@@ -1002,6 +1002,34 @@ def run_reference(args):
     }), flush=True)
 
 
+def run_profile_calls(args):
+    """N plain calls of one single-layer workload and nothing else: a short program for
+    a profiler to attach to (ncu -k <kernel> -s <skip> -c <count> ...)."""
+    import torch
+    import adapter_linear_gb300 as al
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    name = "q_proj_decode" if args.workload == "all" else args.workload
+    p, _ = workload(name)
+
+    def t(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    pool = al.LoraPool(p.max_adapters, p.max_rank, p.d_in, p.d_out)
+    for slot, ad in p.adapters.items():
+        pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
+    pool.reserve(p.T)
+    X, W, ids = t(p.X), t(p.W), t(p.ids)
+    Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=dev)
+    for _ in range(args.profile):
+        pool.linear(X, W, ids, Y)
+    torch.cuda.synchronize(dev)
+    assert pool.check_errors() == al.LORA_OK
+    pool.close()
+    print(json.dumps({"profile_calls": args.profile, "workload": name}), flush=True)
+
+
 def run_cpu_probe(args):
     """Child process of the one-core CPU baseline (OMP_NUM_THREADS set by the parent)."""
     p, _ = workload(args.cpu_probe)
@@ -1025,6 +1053,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--cpu-tokens", type=int, default=16)
     ap.add_argument("--cpu-probe", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--profile", type=int, default=0,
+                    help="run this many plain calls of --workload and exit (for profilers)")
     ap.add_argument("--ref-tokens", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
@@ -1035,6 +1065,8 @@ def main():
 
     if args.cpu_probe:
         return run_cpu_probe(args)
+    if args.profile > 0:
+        return run_profile_calls(args)
     if args.impl == "reference":
         return run_reference(args)
 
