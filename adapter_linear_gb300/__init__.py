@@ -15,7 +15,10 @@ import os
 from typing import Dict, Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "liblora_linear.so")
+# ADAPTER_LINEAR_CHECKED=1 selects the build with range checks in every kernel
+# (liblora_linear_check.so, the same ABI; see LORA_ERR_RANGE)
+CHECKED = os.environ.get("ADAPTER_LINEAR_CHECKED", "0") == "1"
+LIB_PATH = os.path.join(HERE, "liblora_linear_check.so" if CHECKED else "liblora_linear.so")
 
 LORA_OK = 0
 STATUS_NAMES = {
@@ -23,7 +26,7 @@ STATUS_NAMES = {
     4: "LORA_ERR_SLOT_OCCUPIED", 5: "LORA_ERR_SLOT_EMPTY", 6: "LORA_ERR_RANK",
     7: "LORA_ERR_BAD_ADAPTER_ID", 8: "LORA_ERR_CUDA", 9: "LORA_ERR_OOM", 10: "LORA_ERR_TIMEOUT",
     11: "LORA_ERR_UNSUPPORTED",
-    12: "LORA_ERR_IN_USE",
+    12: "LORA_ERR_IN_USE", 13: "LORA_ERR_RANGE",
 }
 globals().update({v: k for k, v in STATUS_NAMES.items()})
 LORA_PATH_AUTO, LORA_PATH_DECODE, LORA_PATH_PREFILL = 0, 1, 2

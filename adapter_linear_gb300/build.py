@@ -1,7 +1,9 @@
 """Build the CUDA library in-tree: nvcc for sm_103a, one object per .cu file
-compiled in parallel, linked into adapter_linear_gb300/liblora_linear.so.
+compiled in parallel, linked into adapter_linear_gb300/liblora_linear.so; and the
+checked build (LORA_CHECK defined: every gathered index range-checked in the
+kernels) into adapter_linear_gb300/liblora_linear_check.so.
 
-Usage: python -m adapter_linear_gb300.build   (or __graft_entry__.build()).
+Usage: python -m adapter_linear_gb300.build [--check-only]   (or __graft_entry__.build()).
 """
 from __future__ import annotations
 
@@ -17,6 +19,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liblora_linear.so")
+OBJ_CHECK = os.path.join(HERE, "_build_check")
+LIB_CHECK = os.path.join(HERE, "liblora_linear_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -43,12 +47,16 @@ def needs_build() -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=()) -> str:
-    os.makedirs(OBJ, exist_ok=True)
+def build(verbose: bool = False, extra_flags=(), check: bool = False) -> str:
+    """Compile and link one library; check=True: the LORA_CHECK build."""
+    obj_dir, lib = (OBJ_CHECK, LIB_CHECK) if check else (OBJ, LIB)
+    if check:
+        extra_flags = (*extra_flags, "-DLORA_CHECK")
+    os.makedirs(obj_dir, exist_ok=True)
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJ, os.path.basename(src) + ".o")
+        obj = os.path.join(obj_dir, os.path.basename(src) + ".o")
         cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -60,16 +68,29 @@ def build(verbose: bool = False, extra_flags=()) -> str:
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
+
+
+def build_all(verbose: bool = False) -> None:
+    """Both libraries, at the same time (twice the translation units in flight)."""
+    with cf.ThreadPoolExecutor(max_workers=2) as ex:
+        for f in [ex.submit(build, verbose), ex.submit(build, verbose, (), True)]:
+            f.result()
 
 
 if __name__ == "__main__":
     v = "-v" in sys.argv
     flags = ["-Xptxas", "-v"] if "--ptxas" in sys.argv else []
-    print(build(verbose=v or bool(flags), extra_flags=flags))
+    if "--check-only" in sys.argv:
+        print(build(verbose=v, check=True))
+    elif flags:
+        print(build(verbose=True, extra_flags=flags))
+    else:
+        build_all(verbose=v)
+        print(LIB, LIB_CHECK)

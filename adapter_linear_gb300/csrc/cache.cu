@@ -114,7 +114,7 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
     CUDA_TRY(cudaMemcpyAsync(p->d_page_list, pages, sizeof(int32_t) * npages,
                              cudaMemcpyHostToDevice, s));
     CUDA_TRY(launch_pack_adapter(p->stage_A, p->stage_B, h.rank, p->d_page_list, npages,
-                                 pool_view(p), p->A_pages, p->B_pages, s));
+                                 pool_view(p), p->A_pages, p->B_pages, p->d_err, s));
     if ((st = enqueue_row(p, slot, row)) != LORA_OK) return st;
 
     p->free_pages.resize(p->free_pages.size() - npages);

@@ -123,6 +123,25 @@ __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
     return r;
 }
 
+// ------------------------------------------------- checked build (LORA_CHECK)
+//
+// Built with LORA_CHECK defined, every index a kernel gathers through a table is
+// tested before use: out of range, it sets kErrRangeBit in the error word and is
+// replaced by a safe one (the zero page, token 0, ...); otherwise these compile to
+// nothing. The result of a call that met such an index is unspecified, but no access
+// leaves its buffer.
+#ifdef LORA_CHECK
+__device__ __forceinline__ bool check_range(int v, int lo, int hi, int *err)
+{
+    if (v >= lo && v < hi) return true;
+    if (err) atomicOr(err, kErrRangeBit);
+    return false;
+}
+#define LORA_CHECKED(v, lo, hi, err, safe) (check_range((v), (lo), (hi), (err)) ? (v) : (safe))
+#else
+#define LORA_CHECKED(v, lo, hi, err, safe) (v)
+#endif
+
 // Is `id` a loaded slot of the table?  (rank field > 0)
 __device__ __forceinline__ bool slot_loaded(const int32_t *slots, int slot_stride,
                                             int max_adapters, int id)

@@ -372,13 +372,17 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
                 const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
                 if (q >= row[SLOT_NPAGES]) continue;
                 const float scale = __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]);
+                const int page = LORA_CHECKED(row[SLOT_PAGES + q], 0, pr.pool.num_pages, pr.err, 0);
                 if (by_warp)
-                    shrink_pair_warp(t, row[SLOT_PAGES + q], scale, pr, q);
+                    shrink_pair_warp(t, page, scale, pr, q);
                 else
-                    shrink_pair(t, row[SLOT_PAGES + q], scale, pr, q, red);
+                    shrink_pair(t, page, scale, pr, q, red);
             }
         }
         for (int seg = 0; seg < nseg; ++seg) {
+#ifdef LORA_CHECK
+            if (!check_range(seg, 0, p.max_seg, err)) break;
+#endif
             const int a = seg % n_acc;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[a], (uint32_t)(seg / n_acc) & 1u, &abort_flag, err);
@@ -440,17 +444,20 @@ __device__ __forceinline__ int finish_adapter(const PoolDev &pool, int id, const
 // The B words of columns n0..n0+7 of the first kPrefetchPages pages into registers,
 // the later pages' line into L2.
 __device__ __forceinline__ void finish_b_words(const PoolDev &pool, const int32_t *pages, int np,
-                                               int n0, uint4 (&b)[kPrefetchPages][8])
+                                               int n0, uint4 (&b)[kPrefetchPages][8], int *err)
 {
 #pragma unroll
     for (int q = 0; q < kPrefetchPages; ++q)
         if (q < np) {
-            const uint16_t *src = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+            const int page = LORA_CHECKED(pages[q], 0, pool.num_pages, err, 0);
+            const uint16_t *src = pool.B_pages + ((size_t)page * pool.d_out + n0) * kRankPage;
 #pragma unroll
             for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
         }
     for (int q = kPrefetchPages; q < np; ++q)
-        prefetch_l2(pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage);
+        prefetch_l2(pool.B_pages +
+                    ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, err, 0) * pool.d_out + n0) *
+                        kRankPage);
 }
 
 // The sums of one thread's 8 columns of token t (see finish_decode_body).
@@ -520,7 +527,8 @@ __device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const D
         v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
         {
             uint4 bq[8];
-            const uint16_t *bsrc = pool.B_pages + ((size_t)pages[q] * pool.d_out + n0) * kRankPage;
+            const int page = LORA_CHECKED(pages[q], 0, pool.num_pages, pr.err, 0);
+            const uint16_t *bsrc = pool.B_pages + ((size_t)page * pool.d_out + n0) * kRankPage;
 #pragma unroll
             for (int c = 0; c < 8; ++c) bq[c] = ldg_nc_v4(bsrc + c * kRankPage);
             expand8(acc, v, bq);
@@ -566,7 +574,7 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     if (LORA && pool.slots != nullptr) {
         id = ids[t];
         np = finish_adapter(pool, id, pages);
-        if (col_ok) finish_b_words(pool, pages, np, n0, b);
+        if (col_ok) finish_b_words(pool, pages, np, n0, b, pr.err);
     }
     // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
     // can have started before the tile; its partial for the tile is its segment
@@ -579,7 +587,16 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     while (((c_lo + 1) * p.U) / p.G <= ub) ++c_lo;
     int c_hi = c_lo;
     while (c_hi + 1 < p.G && ((c_hi + 1) * p.U) / p.G < ue) ++c_hi;
-    const int seg_lo = pr.g_begin + tile - unit_tile(p, (c_lo * p.U) / p.G);
+    int seg_lo = pr.g_begin + tile - unit_tile(p, (c_lo * p.U) / p.G);
+#ifdef LORA_CHECK
+    // the split-K slots this thread reads: contributors within the ranges, the first
+    // one's segment within its partials
+    if (col_ok && (!check_range(c_lo, 0, p.G, pr.err) || !check_range(c_hi, c_lo, p.G, pr.err) ||
+                   !check_range(seg_lo, 0, p.max_seg, pr.err))) {
+        c_lo = c_hi = 0;
+        seg_lo = 0;
+    }
+#endif
 
     // ---- partials and V are written by the GEMM kernel
     pdl_wait_prior();

@@ -78,6 +78,17 @@ struct TileLora {
     const int32_t *pages;
 };
 
+// Checked build: a tile's slot and page count within the pool (else no expand).
+__device__ __forceinline__ bool tile_slot_ok(int slot, const PoolDev &pool, int *err)
+{
+#ifdef LORA_CHECK
+    if (!check_range(slot, 0, pool.max_adapters, err)) return false;
+    return check_range(pool.slots[(size_t)slot * pool.slot_stride + SLOT_NPAGES], 0, pool.max_pages + 1, err);
+#else
+    return true;
+#endif
+}
+
 __device__ __forceinline__ TileLora tile_lora(int m, const PrefillArgs &a, const PoolDev &pool)
 {
     TileLora r{0, -1, 0, 0, nullptr};
@@ -88,6 +99,7 @@ __device__ __forceinline__ TileLora tile_lora(int m, const PrefillArgs &a, const
         r.mode = 2;
         return r;
     }
+    if (!tile_slot_ok(ti, pool, a.err)) return r;
     const int32_t *row = pool.slots + (size_t)ti * pool.slot_stride;
     r.mode = 1;
     r.slot = ti;
@@ -137,7 +149,7 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tmem_buf, int quarter, in
                                  bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
                                  bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
                                  bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
-            const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
+            const uint16_t *bp = pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + ncol) * kRankPage;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 if (ncol + j < a.d_out) {
@@ -234,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_2d(xs, &tmV, &full[s], e * 64, m * kBM);
                         for (int i = 0; i < kPagesPerBlock; ++i) {
                             const int q = e * kPagesPerBlock + i;
-                            const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
+                            const int page = q < tl.npages
+                                                 ? LORA_CHECKED(tl.pages[q], 0, pool.num_pages, a.err, 0)
+                                                 : 0;  // page 0 is zeros
                             bulk_load(xs + kXTileBytes + i * kPageSliceBytes,
                                       pool.B_pages + ((size_t)page * a.d_out + n0) * kRankPage,
                                       slice_bytes, &full[s]);
@@ -393,7 +407,7 @@ __device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quar
                                      bf16_lo(h.y) + bf16_lo(l.y), bf16_hi(h.y) + bf16_hi(l.y),
                                      bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
                                      bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
-                const uint16_t *bp = pool.B_pages + ((size_t)pages[q] * a.d_out + ncol) * kRankPage;
+                const uint16_t *bp = pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + ncol) * kRankPage;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
                     if (ncol + j < a.d_out) {
@@ -470,6 +484,7 @@ __device__ __forceinline__ TileLora pair_tile_lora(int m, uint32_t rank, const P
         return r;
     }
     if (slot < 0) return r;
+    if (!tile_slot_ok(slot, pool, a.err)) return r;
     const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
     r.mode = 1;
     r.slot = slot;
@@ -587,7 +602,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_2d_pair(bs, &tmV, fb, e * 64, r0);
                             for (int i = 0; i < kPagesPerBlock; ++i) {
                                 const int q = e * kPagesPerBlock + i;
-                                const int page = q < tl.npages ? tl.pages[q] : 0;  // page 0 is zeros
+                                const int page = q < tl.npages
+                                                     ? LORA_CHECKED(tl.pages[q], 0, pool.num_pages, a.err, 0)
+                                                     : 0;  // page 0 is zeros
                                 tma_load_2d_pair(bs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
                                                  page * a.d_out + n0);
                             }

@@ -41,6 +41,7 @@ constexpr int kDecodeMaxT = 256;       // largest batch of the decode path
 // Device error word bits.
 constexpr int kErrBadIdBit = 1;
 constexpr int kErrTimeoutBit = 2;
+constexpr int kErrRangeBit = 4;   // checked build (LORA_CHECK): an index out of range
 
 // Every mbarrier wait gives up after this long (then flags kErrTimeoutBit).
 constexpr uint64_t kWaitTimeoutNs = 2000000000ull;
@@ -176,7 +177,7 @@ cudaError_t launch_gemm_prefill(const CUtensorMap &tmX, const CUtensorMap &tmW,
 // Pack a row-major A (d_in x rank) and B (rank x d_out) into pool pages.
 cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,
                                 int npages, const PoolDev &pool, uint16_t *A_pages,
-                                uint16_t *B_pages, cudaStream_t stream);
+                                uint16_t *B_pages, int *err, cudaStream_t stream);
 
 // Host: on the current device, give a kernel the largest shared-memory carveout
 // and raise its dynamic shared-memory limit to at least `bytes` (remembered

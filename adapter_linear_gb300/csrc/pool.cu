@@ -222,7 +222,7 @@ const CUtensorMap *tmap_for(lora_pool *p, const void *base, uint64_t inner, uint
 __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
                                     int rank, const int32_t *__restrict__ pages, int npages, int d_in,
                                     int d_out, uint16_t *__restrict__ A_pages,
-                                    uint16_t *__restrict__ B_pages)
+                                    uint16_t *__restrict__ B_pages, int num_pages, int *err)
 {
     const size_t totA = (size_t)npages * kRankPage * d_in;
     const size_t totB = (size_t)npages * d_out * kRankPage;
@@ -234,6 +234,9 @@ __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16
             const size_t rem = i % per_page;
             const int jj = (int)(rem / d_in), k = (int)(rem % d_in);
             const int j = q * kRankPage + jj;
+#ifdef LORA_CHECK
+            if (!check_range(pages[q], 1, num_pages, err)) continue;  // never the zero page
+#endif
             A_pages[(size_t)pages[q] * per_page + rem] = (j < rank) ? A[(size_t)k * rank + j] : 0;
         } else {
             const size_t i2 = i - totA;
@@ -242,6 +245,9 @@ __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16
             const size_t rem = i2 % per_page;
             const int n = (int)(rem / kRankPage), jj = (int)(rem % kRankPage);
             const int j = q * kRankPage + jj;
+#ifdef LORA_CHECK
+            if (!check_range(pages[q], 1, num_pages, err)) continue;
+#endif
             B_pages[(size_t)pages[q] * per_page + rem] = (j < rank) ? B[(size_t)j * d_out + n] : 0;
         }
     }
@@ -450,6 +456,7 @@ const char *lora_status_string(lora_status s)
     case LORA_ERR_TIMEOUT: return "a kernel wait timed out";
     case LORA_ERR_UNSUPPORTED: return "device is not compute capability 10.3";
     case LORA_ERR_IN_USE: return "a chain still lists this adapter";
+    case LORA_ERR_RANGE: return "a checked kernel met an index out of range";
     }
     return "unknown status";
 }
@@ -629,7 +636,7 @@ lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void
     if (cudaMemcpyAsync(p->d_page_list, pages, sizeof(int32_t) * npages, cudaMemcpyHostToDevice, s) !=
             cudaSuccess ||
         launch_pack_adapter(p->load_A, p->load_B, rank, p->d_page_list, npages, pool_view(p),
-                            p->A_pages, p->B_pages, s) != cudaSuccess ||
+                            p->A_pages, p->B_pages, p->d_err, s) != cudaSuccess ||
         cudaEventRecord(p->ev_loaded, s) != cudaSuccess) {
         cudaGetLastError();
         return LORA_ERR_CUDA;
@@ -845,6 +852,7 @@ lora_status lora_pool_check_errors(lora_pool_t p)
     const int word = *p->h_err;
     if (word & kErrBadIdBit) return LORA_ERR_BAD_ADAPTER_ID;
     if (word & kErrTimeoutBit) return LORA_ERR_TIMEOUT;
+    if (word & kErrRangeBit) return LORA_ERR_RANGE;
     return LORA_OK;
 }
 
@@ -951,14 +959,14 @@ namespace lora {
 
 cudaError_t launch_pack_adapter(const uint16_t *A, const uint16_t *B, int rank, const int32_t *pages,
                                 int npages, const PoolDev &pool, uint16_t *A_pages,
-                                uint16_t *B_pages, cudaStream_t stream)
+                                uint16_t *B_pages, int *err, cudaStream_t stream)
 {
     cudaError_t e = ensure_smem_attr((const void *)pack_adapter_kernel, 0);
     if (e != cudaSuccess) return e;
     const size_t total = (size_t)npages * kRankPage * (pool.d_in + pool.d_out);
     int grid = (int)std::min<size_t>((total + 255) / 256, 4096);
     pack_adapter_kernel<<<grid, 256, 0, stream>>>(A, B, rank, pages, npages, pool.d_in, pool.d_out,
-                                                  A_pages, B_pages);
+                                                  A_pages, B_pages, pool.num_pages, err);
     return cudaGetLastError();
 }
 

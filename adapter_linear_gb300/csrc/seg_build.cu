@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(kSegWarps * 32, 1)
             const unsigned same = __match_any_sync(active, key);
             const uint32_t pos =
                 koff[key] + cnt[key * kSegWarps + warp] + __popc(same & lanemask_lt());
-            tabs.order[pos] = t;
+#ifdef LORA_CHECK
+            if (check_range((int)pos, 0, T, err))
+#endif
+                tabs.order[pos] = t;
             __syncwarp(active);
             if (lane == __ffs(same) - 1) cnt[key * kSegWarps + warp] += __popc(same);
         }
@@ -405,7 +408,7 @@ __global__ void __launch_bounds__(kSegChunk)
 }
 
 __global__ void __launch_bounds__(kSegChunk)
-    seg_scatter_kernel(int T, int K, SegTables tabs, uint64_t *trace)
+    seg_scatter_kernel(int T, int K, SegTables tabs, int *err, uint64_t *trace)
 {
     trace_enter_released(trace);
     constexpr int kWarps = kSegChunk / 32;
@@ -423,7 +426,11 @@ __global__ void __launch_bounds__(kSegChunk)
             const unsigned active = __ballot_sync(0xffffffffu, t < T);
             if (t < T) {
                 const unsigned same = __match_any_sync(active, key);
-                tabs.order[run[key] + __popc(same & lanemask_lt())] = t;
+                const int pos = run[key] + __popc(same & lanemask_lt());
+#ifdef LORA_CHECK
+                if (check_range(pos, 0, T, err))
+#endif
+                    tabs.order[pos] = t;
                 __syncwarp(active);
                 if (lane == __ffs(same) - 1) run[key] += __popc(same);
             }
@@ -471,7 +478,7 @@ cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, Seg
         if (e == cudaSuccess) e = ensure_smem_attr((const void *)seg_scatter_kernel, smem);
         if (e != cudaSuccess) return e;
         seg_count_kernel<<<chunks, kSegChunk, smem, stream>>>(ids, T, pool, tabs, err, vhl, ldh, trace);
-        seg_scatter_kernel<<<chunks, kSegChunk, smem, stream>>>(T, K, tabs, trace);
+        seg_scatter_kernel<<<chunks, kSegChunk, smem, stream>>>(T, K, tabs, err, trace);
         return cudaGetLastError();
     }
     if (seg_build_smem_bytes(pool.max_adapters, 32) + (size_t)T * sizeof(int) <= kSegSmemLimit)

@@ -39,7 +39,8 @@ struct UnitInfo {
     const int32_t *scales;  // fp32 bits, one per page (up to n / 8 entries readable)
 };
 
-__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs)
+__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs, int T,
+                                              int *err)
 {
     // segment s: largest s with seg_ublk[s] <= u (seg_ublk ascending, [num_seg + 1])
     int lo = 0, hi = tabs.hdr[HDR_NUMSEG];
@@ -51,8 +52,20 @@ __device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const 
     UnitInfo r;
     r.p0 = tabs.seg_start[s] + (u - tabs.seg_ublk[s]) * kShrinkRows;
     r.p1 = min(r.p0 + kShrinkRows, tabs.seg_start[s + 1]);
-    const int32_t *row = pool.slots + (size_t)tabs.seg_slot[s] * pool.slot_stride;
+    int slot = tabs.seg_slot[s];
+#ifdef LORA_CHECK
+    // a unit outside the tokens or a slot outside the pool: an empty unit of slot 0
+    if (!check_range(r.p0, 0, T, err) || !check_range(r.p1, r.p0, T + 1, err) ||
+        !check_range(slot, 0, pool.max_adapters, err)) {
+        r.p0 = r.p1 = 0;
+        slot = 0;
+    }
+#endif
+    const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
     r.npages = row[SLOT_NPAGES];
+#ifdef LORA_CHECK
+    if (!check_range(r.npages, 1, pool.max_pages + 1, err)) r.npages = 1;
+#endif
     r.n = ((r.npages * kRankPage + 15) / 16) * 16;
     r.pages = row + SLOT_PAGES;
     r.scales = row + slot_page_scale(pool.max_pages, 0);
@@ -64,7 +77,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap tmAw,
                      const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
                      uint16_t *__restrict__ Vhl, int ldh, int nmax, int stages, uint32_t tmem_cols,
-                     int *err, uint64_t *trace)
+                     int *err, uint64_t *trace, int T)
 {
     trace_enter_released(trace);
     extern __shared__ uint8_t shrink_smem_raw[];
@@ -117,8 +130,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ producer
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(u, pool, tabs);
-            const int row0 = tabs.order[ui.p0];
+            const UnitInfo ui = unit_info(u, pool, tabs, T, err);
+            const int row0 = LORA_CHECKED(tabs.order[ui.p0], 0, T, err, 0);
             bool contiguous = true;
             for (int r = lane; r < ui.p1 - ui.p0; r += 32)
                 contiguous &= (tabs.order[ui.p0 + r] == row0 + r);
@@ -144,7 +157,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     // gather 128 rows x 64 bf16 per box into the 128-byte-swizzled layout
                     for (int r = lane; r < 128; r += 32) {
                         const int p = ui.p0 + r;
-                        const int tok = (p < ui.p1) ? tabs.order[p] : -1;
+                        const int tok = (p < ui.p1) ? LORA_CHECKED(tabs.order[p], 0, T, err, -1) : -1;
 #pragma unroll
                         for (int b = 0; b < kSBoxes; ++b)
 #pragma unroll
@@ -165,10 +178,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                         const int k0 = (kb * kSBoxes + b) * 64;
                         if (contiguous) tma_load_2d(xs + b * kXTileBytes, &tmX, &full[s], k0, row0);
                         if (wide) {
-                            tma_load_2d(ps + b * p_bytes, &tmAw, &full[s], k0, ui.pages[0] * kRankPage);
+                            tma_load_2d(ps + b * p_bytes, &tmAw, &full[s], k0,
+                                        LORA_CHECKED(ui.pages[0], 0, pool.num_pages, err, 0) * kRankPage);
                         } else {
                             for (int q = 0; q < npad; ++q) {
-                                const int page = q < ui.npages ? ui.pages[q] : 0;
+                                const int page = q < ui.npages ? LORA_CHECKED(ui.pages[q], 0, pool.num_pages, err, 0) : 0;
                                 tma_load_2d(ps + b * p_bytes + q * 1024, &tmA, &full[s], k0,
                                             page * kRankPage);
                             }
@@ -193,7 +207,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int it = 0, uc = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
-                const UnitInfo ui = unit_info(u, pool, tabs);
+                const UnitInfo ui = unit_info(u, pool, tabs, T, err);
                 const int buf = uc & 1;
                 ok = mbar_wait(&acc_empty[buf], ((uint32_t)(uc >> 1) & 1u) ^ 1u, &abort_flag, err);
                 if (!ok) break;
@@ -227,7 +241,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ epilogue
         int uc = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
-            const UnitInfo ui = unit_info(u, pool, tabs);
+            const UnitInfo ui = unit_info(u, pool, tabs, T, err);
             const int buf = uc & 1;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(uc >> 1) & 1u, &abort_flag, err);
@@ -237,7 +251,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             const int r = warp * 32 + lane;
             const int p = ui.p0 + r;
             const bool valid = p < ui.p1;
-            const int tok = valid ? tabs.order[p] : 0;
+            const int tok = valid ? LORA_CHECKED(tabs.order[p], 0, T, err, 0) : 0;
             // s * (X A) as a bf16 pair hi + lo (hi = bf16(v), lo = bf16(v - hi)), grouped
             // per 32 rank columns: [hi 0..31 | lo 0..31] [hi 32..63 | lo 32..63] ...
             uint16_t *hrow = Vhl + (size_t)tok * ldh;
@@ -316,7 +330,7 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
     cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
     shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, tmAw, X, pool, tabs, Vhl, ldh, nmax,
-                                                          stages, tmem_cols, err, trace);
+                                                          stages, tmem_cols, err, trace, T);
     return cudaGetLastError();
 }
 

@@ -29,6 +29,12 @@
  *  - Only GB300-class devices (compute capability 10.3) are supported; on any
  *    other device lora_pool_create returns LORA_ERR_UNSUPPORTED. There is no
  *    CPU fall-back.
+ *  - The library is also built with LORA_CHECK defined (liblora_linear_check.so,
+ *    the same ABI): there every index a kernel gathers through a table (page
+ *    ids, token positions, slot ids, segment and tile entries, split-K partial
+ *    slots) is range-checked first; an index out of range sets the pool's error
+ *    word (LORA_ERR_RANGE) and the access is skipped or redirected to the zero
+ *    page, never made. It stands in for a memory checker and runs slower.
  */
 #ifndef LORA_LINEAR_H
 #define LORA_LINEAR_H
@@ -66,7 +72,10 @@ typedef enum {
     LORA_ERR_TIMEOUT = 10,        /* a kernel's bounded wait ran out (reported
                                      by lora_pool_check_errors)                */
     LORA_ERR_UNSUPPORTED = 11,    /* no compute-capability-10.3 device         */
-    LORA_ERR_IN_USE = 12          /* unload of an adapter a chain still lists  */
+    LORA_ERR_IN_USE = 12,         /* unload of an adapter a chain still lists  */
+    LORA_ERR_RANGE = 13           /* a kernel of the checked build (LORA_CHECK)
+                                     met an index outside its table or buffer
+                                     (reported by lora_pool_check_errors)      */
 } lora_status;
 
 /* Limits. */
@@ -364,8 +373,9 @@ lora_status lora_base_linear_noalloc(const void *X, const void *W_base, int T, i
  * default stream (NULL) completes only after all earlier work of the context,
  * so the calls of a pool used on that stream also wait for other streams' work
  * enqueued before them.
- * Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID or LORA_ERR_TIMEOUT (the first of
- * these present), or LORA_ERR_CUDA if the device reported an error.
+ * Returns LORA_OK, LORA_ERR_BAD_ADAPTER_ID, LORA_ERR_TIMEOUT or LORA_ERR_RANGE
+ * (the first of these present), or LORA_ERR_CUDA if the device reported an
+ * error.
  */
 lora_status lora_pool_check_errors(lora_pool_t pool);
 

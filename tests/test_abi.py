@@ -42,8 +42,21 @@ def test_library_exports_every_declared_symbol(lib):
     assert lib.lora_abi_version() == 1
 
 
+def test_checked_build_exports_every_declared_symbol(lib):
+    """The range-checked build (LORA_CHECK) has the same ABI."""
+    path = os.path.join(os.path.dirname(al.__file__), "liblora_linear_check.so")
+    if not os.path.exists(path):
+        from adapter_linear_gb300 import build as cuda_build
+        cuda_build.build(check=True)
+    checked = ctypes.CDLL(path)
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    checked.lora_status_string.restype = ctypes.c_char_p
+    assert checked.lora_status_string(13) == b"a checked kernel met an index out of range"
+
+
 def test_status_strings(lib):
-    for code in range(0, 12):
+    for code in range(0, 14):
         s = al.lora_status_string(code)
         assert isinstance(s, str) and s and s != "unknown status"
     assert al.lora_status_string(99) == "unknown status"
