@@ -64,6 +64,8 @@ def load(path: Optional[str] = None) -> ctypes.CDLL:
     lib.oracle_lora_linear_chains.argtypes = [vp, vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, vp,
                                               vp]
     lib.oracle_lora_linear_chains.restype = ctypes.c_int
+    lib.oracle_dequant_q4.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    lib.oracle_dequant_q4.restype = ctypes.c_int
     if path == LIB:
         _lib = lib
     return lib
@@ -184,6 +186,33 @@ def chain_lists(ids: np.ndarray, chains: Dict[int, Sequence[int]]) -> List[List[
         else:
             out.append([i])
     return out
+
+
+def dequant_q4(Wq: np.ndarray, scales: np.ndarray, zeros: np.ndarray, d_in: int,
+               group: int = 128, lib=None) -> np.ndarray:
+    """The 4-bit base weight as bf16 bits [d_out, d_in]: bf16(s (q - z)) per group.
+
+    Wq: uint8 [d_out, d_in / 2] (even k in the low nibble); scales: uint16 bf16 bits
+    [d_in / group, d_out]; zeros: uint8 [d_in / group, d_out] in 0..15.
+    """
+    lib = lib or load()
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.uint16)
+    zeros = np.ascontiguousarray(zeros, dtype=np.uint8)
+    d_out = Wq.shape[0]
+    assert Wq.shape == (d_out, d_in // 2) and scales.shape == zeros.shape == (d_in // group, d_out)
+    W = np.empty((d_out, d_in), np.uint16)
+    rc = lib.oracle_dequant_q4(_ptr(Wq), _ptr(scales), _ptr(zeros), d_out, d_in, group, _ptr(W))
+    if rc != OK:
+        raise OracleError(rc)
+    return W
+
+
+def lora_linear_q4(X: np.ndarray, Wq: np.ndarray, scales: np.ndarray, zeros: np.ndarray,
+                   ids: np.ndarray, adapters, n_slots: int, group: int = 128, lib=None) -> np.ndarray:
+    """The layer over the dequantised 4-bit base: lora_linear(X, dequant_q4(...), ...)."""
+    W = dequant_q4(Wq, scales, zeros, X.shape[1], group, lib=lib)
+    return lora_linear(X, W, ids, adapters, n_slots, lib=lib)
 
 
 def problem_adapters(problem) -> Dict[int, Tuple[np.ndarray, np.ndarray, int, float]]:

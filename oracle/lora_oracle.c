@@ -272,3 +272,57 @@ int oracle_lora_linear_chains(const uint16_t *X, const uint16_t *W, const int32_
     }
     return ORACLE_OK;
 }
+
+/* ------------------------------------------------------ quantised base (4-bit) */
+
+/*
+ * A base weight stored group-wise in 4 bits, dequantised to the activation type
+ * (bfloat16) before the layer's product:
+ *
+ *   W[n,k] = bf16( s[g][n] * (q[n,k] - z[g][n]) ),   g = k / group
+ *
+ * Source: "多 LoRA 热插拔: 一模型服多租户" (vLLM tutorial), section 性能注意事项: the
+ * base may be quantised to 4 bits (AWQ-INT4) while the adapters stay in bf16. The
+ * pages give no format; the reading used: q an unsigned 4-bit code, two per byte
+ * along k in the nn.Linear layout (Wq[n * d_in/2 + k/2], the even k in the low
+ * nibble); per (group of `group` inputs, output row) one bf16 scale s and one
+ * unsigned 4-bit zero point z (scales [d_in/group][d_out] as bf16 bits, zeros
+ * [d_in/group][d_out] as bytes 0..15). The product s * (q - z) is exact in double
+ * (an 8-bit significand times an integer of magnitude <= 15); it is rounded once to
+ * bfloat16, to nearest with ties to even, as a dequantising kernel does before a
+ * bf16 matrix product.
+ * W receives d_out x d_in bf16 bit patterns. Returns ORACLE_ERR_ARG for a shape
+ * that the groups do not divide or a zero point above 15.
+ */
+static uint16_t bf16_round_nearest_even(double v)
+{
+    float f = (float)v; /* exact: v has at most 12 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return 0x7FC0; /* NaN */
+    /* round half to even on the 16 bits that are dropped */
+    const uint32_t lsb = (u >> 16) & 1u;
+    return (uint16_t)((u + 0x7FFFu + lsb) >> 16);
+}
+
+int oracle_dequant_q4(const uint8_t *Wq, const uint16_t *scales, const uint8_t *zeros,
+                      int64_t d_out, int64_t d_in, int64_t group, uint16_t *W)
+{
+    if (d_out <= 0 || d_in <= 0 || group <= 0 || d_in % group != 0 || d_in % 2 != 0)
+        return ORACLE_ERR_ARG;
+    const int64_t groups = d_in / group;
+    for (int64_t g = 0; g < groups; ++g)
+        for (int64_t n = 0; n < d_out; ++n)
+            if (zeros[g * d_out + n] > 15) return ORACLE_ERR_ARG;
+    for (int64_t n = 0; n < d_out; ++n) {
+        for (int64_t k = 0; k < d_in; ++k) {
+            const uint8_t byte = Wq[n * (d_in / 2) + k / 2];
+            const int q = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);
+            const int64_t g = k / group;
+            const int z = zeros[g * d_out + n];
+            const double s = bf16_value(scales[g * d_out + n]);
+            W[n * d_in + k] = bf16_round_nearest_even(s * (double)(q - z));
+        }
+    }
+    return ORACLE_OK;
+}

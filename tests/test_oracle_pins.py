@@ -284,10 +284,93 @@ def pin_chain_order_and_reduction(lib):
         oracle.lora_linear_chains(X, W, [[0, 7]] + lists[1:], ads, 4, lib=lib)
 
 
+# ------------------------------------------------ quantised base (4-bit codes)
+
+GOLDEN_Q4 = os.path.join(os.path.dirname(__file__), "golden", "q4_hand_example.json")
+
+
+def pin_q4_golden(lib):
+    """The hand-worked example (tests/golden/q4_hand_example.json): codes, zero points
+    and scales per group, a value that needs the rounding to bf16, and the layer."""
+    g = json.load(open(GOLDEN_Q4))
+    Wq = np.array(g["Wq_bytes"], np.uint8)
+    codes = np.array(g["codes"])
+    assert np.array_equal(Wq[:, ::1] & 0x0F, codes[:, 0::2]) and np.array_equal(Wq >> 4, codes[:, 1::2])
+    W = oracle.dequant_q4(Wq, bits(g["scales"]), np.array(g["zeros"], np.uint8), g["d_in"],
+                          group=g["group"], lib=lib)
+    assert np.array_equal(val(W), np.array(g["W"], np.float64))
+    ad = g["adapter"]
+    ads = {0: (bits(ad["A"]), bits(ad["B"]), ad["rank"], ad["alpha"])}
+    Y = oracle.lora_linear_q4(bits(g["X"]), Wq, bits(g["scales"]), np.array(g["zeros"], np.uint8),
+                              np.array(g["ids"], np.int32), ads, 1, group=g["group"], lib=lib)
+    assert np.array_equal(Y, np.array(g["Y"], np.float64))
+
+
+def q4_random(seed, d_out=40, d_in=256, group=128, pow2=False):
+    rng = np.random.default_rng(seed)
+    Wq = rng.integers(0, 256, size=(d_out, d_in // 2), dtype=np.uint8)
+    zeros = rng.integers(0, 16, size=(d_in // group, d_out), dtype=np.uint8)
+    if pow2:
+        s = np.ldexp(1.0, rng.integers(-9, -3, size=zeros.shape)) * rng.choice([-1, 1], size=zeros.shape)
+    else:
+        s = rng.normal(0.0, 0.01, size=zeros.shape)
+    return Wq, bits(s), zeros
+
+
+def pin_q4_numpy_route(lib):
+    """An independent route: numpy unpacks the nibbles, forms s (q - z) in float32
+    (exact: 8-bit significand times a 4-bit integer) and rounds it to bf16 with the
+    input generator's round-to-nearest-even; the oracle must agree bit for bit."""
+    Wq, sc, z = q4_random(31)
+    d_out, d_in = Wq.shape[0], 2 * Wq.shape[1]
+    q = np.empty((d_out, d_in), np.int32)
+    q[:, 0::2] = Wq & 0x0F
+    q[:, 1::2] = Wq >> 4
+    g = np.arange(d_in) // 128
+    s = L.bf16_bits_to_f32(sc)[g, :].T                     # [d_out, d_in]
+    zz = z[g, :].T.astype(np.int32)
+    ref = L.f32_to_bf16_bits((s * (q - zz).astype(np.float32)).astype(np.float32))
+    assert np.array_equal(oracle.dequant_q4(Wq, sc, z, d_in, lib=lib), ref)
+
+
+def pin_q4_exact_scales_layer(lib):
+    """Power-of-two scales make s (q - z) exact: the layer over the 4-bit base equals
+    numpy's fp64 product with that weight on base-only rows, and the bf16 layer with
+    the same weight written out directly, adapters included."""
+    Wq, sc, z = q4_random(32, pow2=True)
+    d_out, d_in = Wq.shape[0], 2 * Wq.shape[1]
+    q = np.empty((d_out, d_in), np.int64)
+    q[:, 0::2] = Wq & 0x0F
+    q[:, 1::2] = Wq >> 4
+    g = np.arange(d_in) // 128
+    Wexact = val(sc)[g, :].T * (q - z[g, :].T.astype(np.int64))
+    X = L.normal_bf16(32, L.ROLE_X, 0, (9, d_in), 1.0)
+    ads = {0: (L.normal_bf16(32, L.ROLE_A, 0, (d_in, 4), 0.1), L.normal_bf16(32, L.ROLE_B, 0, (4, d_out), 0.1),
+               4, 8.0)}
+    ids = np.array([-1, 0, -1, 0, 0, -1, 0, -1, 0], np.int32)
+    Y = oracle.lora_linear_q4(X, Wq, sc, z, ids, ads, 1, lib=lib)
+    base = ids < 0
+    np.testing.assert_allclose(Y[base], val(X)[base] @ Wexact.T, rtol=1e-12, atol=1e-12)
+    np.testing.assert_array_equal(Y, oracle.lora_linear(X, bits(Wexact), ids, ads, 1, lib=lib))
+
+
+def pin_q4_strict(lib):
+    Wq, sc, z = q4_random(33)
+    z2 = z.copy()
+    z2[0, 3] = 16                                           # not a 4-bit zero point
+    with pytest.raises(oracle.OracleError):
+        oracle.dequant_q4(Wq, sc, z2, 2 * Wq.shape[1], lib=lib)
+    # groups that do not divide d_in (120 inputs, groups of 128): an error from the C side
+    out = np.empty((Wq.shape[0], 120), np.uint16)
+    assert lib.oracle_dequant_q4(Wq.ctypes.data, sc.ctypes.data, z.ctypes.data, Wq.shape[0], 120, 128,
+                                 out.ctypes.data) == 1
+
+
 PINS = [pin_golden, pin_basis_rows, pin_base_rows_match_numpy, pin_zero_B_is_base,
         pin_merge_mode, pin_rank_padding, pin_permutation, pin_linearity, pin_scale,
         pin_strict_ids, pin_segments_bruteforce, pin_chain_merge_mode, pin_chain_concatenation,
-        pin_chain_order_and_reduction]
+        pin_chain_order_and_reduction, pin_q4_golden, pin_q4_numpy_route, pin_q4_exact_scales_layer,
+        pin_q4_strict]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -320,6 +403,13 @@ MUTATIONS = {
                            "branch += low[j] * bf16_value(B[c][n * rc + j]);"),
     "chain_W_transposed": ("acc += bf16_value(xt[k]) * bf16_value(W[n * d_in + k]);",
                            "acc += bf16_value(xt[k]) * bf16_value(W[k * d_out + n]);"),
+    "q4_nibbles_swapped": ("const int q = (k % 2 == 0) ? (byte & 0x0F) : (byte >> 4);",
+                           "const int q = (k % 2 == 0) ? (byte >> 4) : (byte & 0x0F);"),
+    "q4_zero_point_dropped": ("s * (double)(q - z)", "s * (double)q"),
+    "q4_group_by_row": ("const int64_t g = k / group;", "const int64_t g = n % groups;"),
+    "q4_truncated": ("return (uint16_t)((u + 0x7FFFu + lsb) >> 16);", "return (uint16_t)(u >> 16);"),
+    "q4_scales_transposed": ("const double s = bf16_value(scales[g * d_out + n]);",
+                             "const double s = bf16_value(scales[n * groups + g]);"),
     "lenient_segment_ids": ("if (ids[t] < -1 || ids[t] >= n_slots) return ORACLE_ERR_BAD_ADAPTER_ID;",
                             "if (ids[t] < -1) return ORACLE_ERR_BAD_ADAPTER_ID;"),
 }
