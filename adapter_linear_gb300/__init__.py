@@ -43,7 +43,7 @@ EXPORTS = (
     "lora_base_linear_noalloc", "lora_linear_grouped", "lora_define_chain",
     "lora_host_register", "lora_host_unregister", "lora_acquire", "lora_prefetch", "lora_release",
     "lora_cache_stats", "lora_pool_selftest_wait", "lora_decode_plan_info", "lora_test_delayed_copy",
-    "lora_pool_set_trace",
+    "lora_pool_set_trace", "lora_linear_q4", "lora_base_linear_q4", "lora_dequant_q4",
 )
 PLAN_INFO_FIELDS = ("units", "G", "grid", "max_seg", "n_acc", "stages", "tmem_cols", "smem_bytes",
                     "pairs", "col_blocks", "tight", "ntok", "partials_floats", "prefetch_a")
@@ -107,6 +107,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
         "lora_decode_plan_info": [i32, i32, vp, vp, vp, i32, vp],
         "lora_test_delayed_copy": [vp, vp, i32, i32, vp],
         "lora_pool_set_trace": [vp, vp, i32],
+        "lora_linear_q4": [vp, vp, vp, vp, vp, vp, i32, vp, vp],
+        "lora_base_linear_q4": [vp, vp, vp, vp, vp, i32, vp, vp],
+        "lora_dequant_q4": [vp, vp, vp, i32, i32, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -267,6 +270,21 @@ def lora_pool_set_trace(pool: int, buf, n_calls: int) -> int:
     return load_library().lora_pool_set_trace(pool, _ptr(buf), n_calls)
 
 
+def lora_linear_q4(pool: int, X, Wq, scales, zeros, ids, T: int, Y, stream=None) -> int:
+    return load_library().lora_linear_q4(pool, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zeros), _ptr(ids), T,
+                                         _ptr(Y), _stream(stream))
+
+
+def lora_base_linear_q4(pool: int, X, Wq, scales, zeros, T: int, Y, stream=None) -> int:
+    return load_library().lora_base_linear_q4(pool, _ptr(X), _ptr(Wq), _ptr(scales), _ptr(zeros), T,
+                                              _ptr(Y), _stream(stream))
+
+
+def lora_dequant_q4(Wq, scales, zeros, d_out: int, d_in: int, W, stream=None) -> int:
+    return load_library().lora_dequant_q4(_ptr(Wq), _ptr(scales), _ptr(zeros), d_out, d_in, _ptr(W),
+                                          _stream(stream))
+
+
 def lora_status_string(status: int) -> str:
     return load_library().lora_status_string(status).decode()
 
@@ -371,6 +389,23 @@ class LoraPool:
         _check(lora_linear_grouped([p.handle for p in pools], Xs, Ws, ids, T, Ys, stream),
                "lora_linear_grouped")
         return Ys
+
+    def linear_q4(self, X, Wq, scales, zeros, ids, Y=None, stream=None):
+        """The layer over a 4-bit base (codes, bf16 scales, 4-bit zero points per 128 inputs)."""
+        import torch
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=X.device)
+        _check(lora_linear_q4(self.handle, X, Wq, scales, zeros, ids, T, Y, stream), "lora_linear_q4")
+        return Y
+
+    def base_linear_q4(self, X, Wq, scales, zeros, Y=None, stream=None):
+        import torch
+        T = X.shape[0]
+        if Y is None:
+            Y = torch.empty((T, self.d_out), dtype=torch.bfloat16, device=X.device)
+        _check(lora_base_linear_q4(self.handle, X, Wq, scales, zeros, T, Y, stream), "lora_base_linear_q4")
+        return Y
 
     def base_linear(self, X, W, Y=None, stream=None):
         import torch

@@ -102,6 +102,38 @@ __device__ __forceinline__ float dot8_f32_bf16(const float *v, const uint4 &b, f
     return acc;
 }
 
+// Eight 4-bit codes (w: code j in bits 4j..4j+3, the lowest first) to the eight bf16
+// values bf16(s * (q_j - z)), as four bf16x2 words in element order. 128 + q is exact
+// in bf16 (bits 0x4300 | q), so (128 + q) - (128 + z) is the exact integer q - z, and
+// one bf16 multiply rounds the exact product s (q - z) to nearest, ties to even.
+// zz holds 128 + z twice, ss the scale twice.
+__device__ __forceinline__ uint4 dequant8_q4(uint32_t w, __nv_bfloat162 zz, __nv_bfloat162 ss)
+{
+    uint32_t o[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint32_t b = (w >> (8 * p)) & 0xFFu;
+        const uint32_t bits = 0x43004300u | (b & 0xFu) | ((b >> 4) << 16);
+        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&bits);
+        v = __hmul2(__hsub2(v, zz), ss);
+        o[p] = *reinterpret_cast<const uint32_t *>(&v);
+    }
+    return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// 128 + z (z a 4-bit zero point) twice, and a bf16 scale twice, as bf16x2.
+__device__ __forceinline__ __nv_bfloat162 q4_zero_pair(uint32_t z)
+{
+    const uint32_t bits = (0x4300u | z) * 0x10001u;
+    return *reinterpret_cast<const __nv_bfloat162 *>(&bits);
+}
+
+__device__ __forceinline__ __nv_bfloat162 q4_scale_pair(uint16_t s)
+{
+    const uint32_t bits = (uint32_t)s * 0x10001u;
+    return *reinterpret_cast<const __nv_bfloat162 *>(&bits);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // round to nearest even

@@ -33,6 +33,7 @@
 //    in CTA order (deterministic), the low-rank expand s_i V[t,:] B_i[:,n] is
 //    added from the interleaved B pages (one 16-byte load = 8 rank rows of one
 //    column; V already carries s_i), and the sum is rounded once to bf16.
+#include <algorithm>
 #include <utility>
 
 #include "device_common.cuh"
@@ -169,6 +170,95 @@ struct UnitCursor {
         while (u >= next_ub) load(p, m + 1);
     }
 };
+
+// Warps 0-3 of a decode GEMM kernel (either base format): after the setup barrier
+// over `threads` threads, the shrink pairs dealt to this CTA (after the wait on the
+// previous kernel), then each of its segments' accumulators read out of TMEM into the
+// split-K partial sums.
+template <int NP>
+__device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const int32_t *__restrict__ ids,
+                                                float *__restrict__ partials, int *err, int c, int nseg,
+                                                uint64_t *acc_full, uint64_t *acc_empty,
+                                                volatile int *abort_flag_p, float (*red)[kRankPage],
+                                                const uint32_t *tmem_slot, uint32_t threads)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_acc = p.n_acc;
+    named_bar_sync(kBarSetup, threads);
+    tc_fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    // Before the wait on the previous kernel: the A pages of this CTA's shrink pairs
+    // into L2 (line prefetches, so the TMA engine keeps serving the W ring), where
+    // the plan says it pays. The ids read here may still be written by an earlier
+    // kernel in the stream, so they only steer these requests; the pairs below
+    // read the ids again after the wait.
+    if (ids != nullptr && p.prefetch_a) {
+        int m = 0;
+        for (int u = c; u < p.pairs; u += (int)gridDim.x) {
+            while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
+            const DecodeProblem &pr = p.prob[pick<NP>(m)];
+            const int lp = u - pr.pair_begin;
+            const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
+            const int id = ids[t];
+            if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
+            const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
+            if (q >= row[SLOT_NPAGES]) continue;
+            const int page = row[SLOT_PAGES + q];
+            if (page < 0 || page >= pr.pool.num_pages) continue;
+            const uint8_t *Ap = reinterpret_cast<const uint8_t *>(pr.pool.A_pages) +
+                                (size_t)page * kRankPage * pr.pool.d_in * 2;
+            for (int i = threadIdx.x; i < kRankPage * pr.pool.d_in * 2 / 128; i += 128)
+                prefetch_l2(Ap + (size_t)i * 128);
+        }
+    }
+    pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
+    if (ids != nullptr) {
+        // this CTA's pairs: c, c + grid, c + 2 grid, ...; with more than one of them
+        // on average the four warps take every fourth pair each, else all 128
+        // threads work on one pair at a time
+        const int stride = (int)gridDim.x;
+        const bool by_warp = p.pairs > stride;
+        int m = 0;
+        for (int u = by_warp ? c + warp * stride : c; u < p.pairs; u += by_warp ? 4 * stride : stride) {
+            while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
+            const DecodeProblem &pr = p.prob[pick<NP>(m)];
+            const int lp = u - pr.pair_begin;
+            const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
+            const int id = ids[t];
+            if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
+            const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
+            if (q >= row[SLOT_NPAGES]) continue;
+            const float scale = __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]);
+            const int page = LORA_CHECKED(row[SLOT_PAGES + q], 0, pr.pool.num_pages, pr.err, 0);
+            if (by_warp)
+                shrink_pair_warp(t, page, scale, pr, q);
+            else
+                shrink_pair(t, page, scale, pr, q, red);
+        }
+    }
+    for (int seg = 0; seg < nseg; ++seg) {
+#ifdef LORA_CHECK
+        if (!check_range(seg, 0, p.max_seg, err)) break;
+#endif
+        const int a = seg % n_acc;
+        bool ok = true;
+        if (lane == 0) ok = mbar_wait(&acc_full[a], (uint32_t)(seg / n_acc) & 1u, abort_flag_p, err);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
+        tc_fence_after_sync();
+        float *out = partials + ((size_t)c * p.max_seg + seg) * p.T * 128 + warp * 32 + lane;
+        for (int col = 0; col < p.ntok; col += 16) {
+            uint32_t v[16];
+            tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * p.ntok + col), v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (col + j < p.T) out[(size_t)(col + j) * 128] = __uint_as_float(v[j]);
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acc_empty[a]);
+    }
+}
 
 template <int NP>
 __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, const DecodePlanT<NP> &p,
@@ -327,80 +417,8 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         __syncwarp();
     } else {
         // ------------------------------------- warps 0-3: shrink, then epilogue
-        named_bar_sync(kBarSetup, kThreads);
-        tc_fence_after_sync();
-        const uint32_t tmem = *tmem_slot;
-        // Before the wait on the previous kernel: the A pages of this CTA's shrink pairs
-        // into L2 (line prefetches, so the TMA engine keeps serving the W ring), where
-        // the plan says it pays. The ids read here may still be written by an earlier
-        // kernel in the stream, so they only steer these requests; the pairs below
-        // read the ids again after the wait.
-        if (ids != nullptr && p.prefetch_a) {
-            int m = 0;
-            for (int u = c; u < p.pairs; u += (int)gridDim.x) {
-                while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
-                const DecodeProblem &pr = p.prob[pick<NP>(m)];
-                const int lp = u - pr.pair_begin;
-                const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
-                const int id = ids[t];
-                if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
-                const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
-                if (q >= row[SLOT_NPAGES]) continue;
-                const int page = row[SLOT_PAGES + q];
-                if (page < 0 || page >= pr.pool.num_pages) continue;
-                const uint8_t *Ap = reinterpret_cast<const uint8_t *>(pr.pool.A_pages) +
-                                    (size_t)page * kRankPage * pr.pool.d_in * 2;
-                for (int i = threadIdx.x; i < kRankPage * pr.pool.d_in * 2 / 128; i += 128)
-                    prefetch_l2(Ap + (size_t)i * 128);
-            }
-        }
-        pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
-        if (ids != nullptr) {
-            // this CTA's pairs: c, c + grid, c + 2 grid, ...; with more than one of them
-            // on average the four warps take every fourth pair each, else all 128
-            // threads work on one pair at a time
-            const int stride = (int)gridDim.x;
-            const bool by_warp = p.pairs > stride;
-            int m = 0;
-            for (int u = by_warp ? c + warp * stride : c; u < p.pairs; u += by_warp ? 4 * stride : stride) {
-                while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
-                const DecodeProblem &pr = p.prob[pick<NP>(m)];
-                const int lp = u - pr.pair_begin;
-                const int t = lp / pr.pool.max_pages, q = lp - t * pr.pool.max_pages;
-                const int id = ids[t];
-                if (!slot_loaded(pr.pool.slots, pr.pool.slot_stride, pr.pool.max_adapters, id)) continue;
-                const int32_t *row = pr.pool.slots + (size_t)id * pr.pool.slot_stride;
-                if (q >= row[SLOT_NPAGES]) continue;
-                const float scale = __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]);
-                const int page = LORA_CHECKED(row[SLOT_PAGES + q], 0, pr.pool.num_pages, pr.err, 0);
-                if (by_warp)
-                    shrink_pair_warp(t, page, scale, pr, q);
-                else
-                    shrink_pair(t, page, scale, pr, q, red);
-            }
-        }
-        for (int seg = 0; seg < nseg; ++seg) {
-#ifdef LORA_CHECK
-            if (!check_range(seg, 0, p.max_seg, err)) break;
-#endif
-            const int a = seg % n_acc;
-            bool ok = true;
-            if (lane == 0) ok = mbar_wait(&acc_full[a], (uint32_t)(seg / n_acc) & 1u, &abort_flag, err);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) break;
-            tc_fence_after_sync();
-            float *out = partials + ((size_t)c * p.max_seg + seg) * p.T * 128 + warp * 32 + lane;
-            for (int col = 0; col < p.ntok; col += 16) {
-                uint32_t v[16];
-                tmem_ld16_wait(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(a * p.ntok + col), v);
-#pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    if (col + j < p.T) out[(size_t)(col + j) * 128] = __uint_as_float(v[j]);
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[a]);
-        }
+        decode_epilogue<NP>(p, ids, partials, err, c, nseg, acc_full, acc_empty, &abort_flag, red, tmem_slot,
+                            kThreads);
     }
 
     tc_fence_before_sync();
@@ -410,6 +428,252 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         tmem_dealloc(*tmem_slot, p.tmem_cols);
     }
     trace_exit(trace);
+}
+
+// ------------------------------------------------------------- 4-bit base
+//
+// gemm_decode_q4_kernel: the same stream-K split, accumulator ring, shrink and split-K
+// partial sums as gemm_decode_kernel (one layer), for a base stored as 4-bit codes
+// with one bf16 scale and one 4-bit zero point per (group of 128 inputs, output row):
+// W = bf16(s (q - z)). W is a quarter of the bytes, and the MMA still takes bf16, so
+// the tiles are dequantised in shared memory:
+//  * warp 4 streams the codes of each (tile, k-block) unit (128 rows x 64 bytes) with
+//    its 128 scales and zero points into a deep ring of 9 KB stages; they are weights,
+//    so nothing waits on the previous kernel;
+//  * warps 7-10 (32 rows each) turn a unit's codes into the bf16 W tile of an operand
+//    stage, in the 128-byte-swizzled layout a TMA load would have written (one thread
+//    per 16-byte chunk: 4 code bytes -> 8 values, by dequant8_q4);
+//  * warp 6 loads X into the same operand stage after the wait on the previous kernel;
+//    the stage is full when its X bytes have landed and the four dequant warps have
+//    arrived;
+//  * warp 5 issues the MMAs exactly as for a bf16 base; warps 0-3 as there.
+// The first operand stages are dequantised before the previous kernel ends.
+constexpr int kQ4Threads = 352;
+constexpr int kQ4CodeBytes = 128 * 64;          // one unit's codes
+constexpr int kQ4RawBytes = 9216;               // codes + 128 scales + 128 zero points, 1 KB aligned
+
+__device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, const DecodePlanT<1> &p,
+                                                    const int32_t *__restrict__ ids,
+                                                    float *__restrict__ partials, int *err)
+{
+    extern __shared__ uint8_t dec_smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dec_smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t x_box = (uint32_t)p.ntok * 128;
+    const uint32_t w_bytes = kBoxes * kWTileBytes;
+    const uint32_t stage_bytes = w_bytes + kBoxes * x_box;
+    const int stages = p.stages, raw = p.raw_stages, n_acc = p.n_acc;
+    uint8_t *rawbuf = smem + (size_t)stages * stage_bytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(rawbuf + (size_t)raw * kQ4RawBytes);
+    uint64_t *empty = full + stages;
+    uint64_t *raw_full = empty + stages;     // [raw]
+    uint64_t *raw_empty = raw_full + raw;    // [raw]
+    uint64_t *acc_full = raw_empty + raw;    // [n_acc]
+    uint64_t *acc_empty = acc_full + n_acc;  // [n_acc]
+    uint64_t *drain = acc_empty + n_acc;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+    __shared__ int abort_flag;
+    __shared__ float red[4][kRankPage];
+
+    pdl_launch_dependents();  // the finishing kernel reads nothing before its own wait
+    uint64_t *const trace = p.trace ? p.trace + 2 * kTraceWords : nullptr;  // kernel slot 2
+    trace_enter(trace);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = blockIdx.x;
+    const bool ranged = c < p.G;
+    const int u0 = ranged ? cta_start(c, p.U, p.G) : 0, u1 = ranged ? cta_start(c + 1, p.U, p.G) : 0;
+    const int KB = p.prob[0].KB;
+    const int g0 = u0 / KB;
+    const int nseg = u1 > u0 ? (u1 - 1) / KB - g0 + 1 : 0;
+
+    if (warp == 4) {
+        // ------------------------------------------------------- codes producer
+        if (lane == 0) {
+            for (int i = 0; i < stages; ++i) {
+                mbar_init(&full[i], 1 + 4);  // X producer (with its bytes) + four dequant warps
+                mbar_init(&empty[i], 1);
+            }
+            for (int i = 0; i < raw; ++i) {
+                mbar_init(&raw_full[i], 1);
+                mbar_init(&raw_empty[i], 4);
+            }
+            for (int i = 0; i < n_acc; ++i) {
+                mbar_init(&acc_full[i], 1);
+                mbar_init(&acc_empty[i], 4);
+            }
+            mbar_init(drain, 1);
+            abort_flag = 0;
+            fence_mbar_init();
+            tma_prefetch_map(&maps.Wq);
+            tma_prefetch_map(&maps.S);
+            tma_prefetch_map(&maps.Z);
+            tma_prefetch_map(&maps.X);
+        }
+        __syncwarp();
+        named_bar_arrive(kBarSetup, kQ4Threads);
+        if (lane == 0) {
+            const uint64_t pol = policy_evict_first();  // read exactly once
+            int it = 0;
+            for (int u = u0; u < u1; ++u, ++it) {
+                const int i = it % raw;
+                if (it >= raw && !mbar_wait(&raw_empty[i], ((uint32_t)(it / raw) & 1u) ^ 1u, &abort_flag, err))
+                    break;
+                const int tile = u / KB, kb = u - tile * KB;
+                uint8_t *rb = rawbuf + (size_t)i * kQ4RawBytes;
+                mbar_arrive_expect_tx(&raw_full[i], kQ4CodeBytes + 128 * 2 + 128);
+                tma_load_2d_hint(rb, &maps.Wq, &raw_full[i], kb * 64, tile * 128, pol);
+                tma_load_2d(rb + kQ4CodeBytes, &maps.S, &raw_full[i], tile * 128, kb);
+                tma_load_2d(rb + kQ4CodeBytes + 256, &maps.Z, &raw_full[i], tile * 128, kb);
+            }
+            for (int i = 0; i < raw && i < it; ++i) {  // no exit while copies are in flight
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait(&raw_full[j % raw], (uint32_t)(j / raw) & 1u, &dummy, err);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 6) {
+        // ----------------------------------------------------------- X producer
+        named_bar_sync(kBarSetup, kQ4Threads);
+        if (lane == 0) {
+            pdl_wait_prior();  // X belongs to the stream's order
+            trace_release(trace);
+            int it = 0;
+            for (int u = u0; u < u1; ++u, ++it) {
+                const int st = it % stages;
+                if (it >= stages &&
+                    !mbar_wait(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err))
+                    break;
+                const int kb = u % KB;
+                uint8_t *xs = smem + (size_t)st * stage_bytes + w_bytes;
+                mbar_arrive_expect_tx(&full[st], kBoxes * x_box);
+                for (int b = 0; b < kBoxes; ++b)
+                    tma_load_2d(xs + b * x_box, &maps.X, &full[st], (kb * kBoxes + b) * 64, 0);
+            }
+            for (int i = 0; i < stages && i < it; ++i) {
+                const int j = it - 1 - i;
+                int dummy = 0;
+                mbar_wait(&full[j % stages], (uint32_t)(j / stages) & 1u, &dummy, err);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 7) {
+        // ------------------------------------------------------- dequant warps
+        named_bar_sync(kBarSetup, kQ4Threads);
+        const int dw = warp - 7;  // rows 32 dw .. 32 dw + 31 of each tile
+        int it = 0;
+        for (int u = u0; u < u1; ++u, ++it) {
+            const int i = it % raw, st = it % stages;
+            bool ok = true;
+            if (lane == 0) {
+                ok = mbar_wait(&raw_full[i], (uint32_t)(it / raw) & 1u, &abort_flag, err);
+                if (ok && it >= stages)
+                    ok = mbar_wait(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err);
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) break;
+            const uint8_t *rb = rawbuf + (size_t)i * kQ4RawBytes;
+            const uint16_t *sc = reinterpret_cast<const uint16_t *>(rb + kQ4CodeBytes);
+            const uint8_t *zp = rb + kQ4CodeBytes + 256;
+            uint8_t *ws = smem + (size_t)st * stage_bytes;
+#pragma unroll 4
+            for (int j = 0; j < 16; ++j) {
+                // lanes 0-15 one row, 16-31 the next; lane & 15 = the row's 16-byte chunk
+                const int row = dw * 32 + 2 * j + (lane >> 4), ch = lane & 15;
+                const uint32_t w = *reinterpret_cast<const uint32_t *>(rb + row * 64 + ch * 4);
+                const uint4 v = dequant8_q4(w, q4_zero_pair(zp[row]), q4_scale_pair(sc[row]));
+                const int b = ch >> 3, cc = ch & 7;
+                *reinterpret_cast<uint4 *>(ws + b * kWTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();  // the tensor cores read what the threads wrote
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&full[st]);
+                mbar_arrive(&raw_empty[i]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ----------------------------------------------------------------- MMA
+        tmem_alloc(tmem_slot, p.tmem_cols);
+        tmem_relinquish();
+        tc_fence_before_sync();
+        named_bar_sync(kBarSetup, kQ4Threads);
+        tc_fence_after_sync();
+        const uint32_t tmem = *tmem_slot;
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(128, p.ntok);
+            int it = 0;
+            uint32_t d = tmem;
+            for (int u = u0; u < u1; ++u, ++it) {
+                const int tile = u / KB, kb = u - tile * KB;
+                const int seg = tile - g0;
+                const bool seg_first = (kb == 0) || (u == u0);
+                if (seg_first) {
+                    const int a = seg % n_acc;
+                    if (!mbar_wait(&acc_empty[a], ((uint32_t)(seg / n_acc) & 1u) ^ 1u, &abort_flag, err))
+                        break;
+                    tc_fence_after_sync();
+                    d = tmem + (uint32_t)(a * p.ntok);
+                }
+                const int st = it % stages;
+                if (!mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, &abort_flag, err)) break;
+                tc_fence_after_sync();
+                const uint32_t wa = smem_u32(smem + (size_t)st * stage_bytes);
+                const uint32_t xa = wa + w_bytes;
+#pragma unroll
+                for (int b = 0; b < kBoxes; ++b)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ss(d, sdesc_k_sw128(wa + b * kWTileBytes + kk * 32),
+                                    sdesc_k_sw128(xa + b * x_box + kk * 32), idesc,
+                                    (seg_first && b == 0 && kk == 0) ? 0u : 1u);
+                mma_commit(&empty[st]);
+                if (u == u1 - 1 || kb == KB - 1) mma_commit(&acc_full[seg % n_acc]);
+            }
+            mma_commit(drain);
+            int dummy = 0;
+            mbar_wait(drain, 0, &dummy, err);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------- warps 0-3: shrink, then epilogue
+        decode_epilogue<1>(p, ids, partials, err, c, nseg, acc_full, acc_empty, &abort_flag, red, tmem_slot,
+                           kQ4Threads);
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after_sync();
+        tmem_dealloc(*tmem_slot, p.tmem_cols);
+    }
+    trace_exit(trace);
+}
+
+__global__ void __launch_bounds__(kQ4Threads, 1)
+    gemm_decode_q4_kernel(const __grid_constant__ DecodeMapsQ4 maps, const __grid_constant__ DecodePlanT<1> p,
+                          const int32_t *__restrict__ ids, float *__restrict__ partials, int *err)
+{
+    gemm_decode_q4_body(maps, p, ids, partials, err);
+}
+
+// The 4-bit base to bf16, one thread per 8 consecutive inputs of one row (prefill).
+__global__ void dequant_q4_kernel(const uint8_t *__restrict__ Wq, const uint16_t *__restrict__ scales,
+                                  const uint8_t *__restrict__ zeros, int d_out, int d_in,
+                                  uint16_t *__restrict__ W)
+{
+    const int chunks = d_in / 8;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)d_out * chunks;
+         i += (size_t)gridDim.x * blockDim.x) {
+        const int n = (int)(i / chunks), ch = (int)(i % chunks);
+        const int g = ch * 8 / kQ4Group;
+        const uint32_t w = *reinterpret_cast<const uint32_t *>(Wq + (size_t)n * (d_in / 2) + ch * 4);
+        const uint4 v = dequant8_q4(w, q4_zero_pair(zeros[(size_t)g * d_out + n]),
+                                    q4_scale_pair(scales[(size_t)g * d_out + n]));
+        *reinterpret_cast<uint4 *>(W + (size_t)n * d_in + ch * 8) = v;
+    }
 }
 
 constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
@@ -821,6 +1085,46 @@ cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, 
 {
     if (plan.n == 1) return launch_finish_decode_n<1>(plan, partials, ids, stream);
     return launch_finish_decode_n<kMaxGroup>(plan, partials, ids, stream);
+}
+
+bool plan_decode_q4(DecodePlan *plan)
+{
+    DecodePlan &p = *plan;
+    if (p.n != 1 || p.prob[0].KB * 128 != p.prob[0].pool.d_in) return false;
+    constexpr size_t kMaxSmem = 232448;  // per CTA on this GPU
+    const size_t stage_bytes = kBoxes * (kWTileBytes + (size_t)p.ntok * 128);
+    for (int stages = 3; stages >= 2; --stages) {
+        const size_t fixed = 1024 + stages * stage_bytes + 512;
+        if (fixed + 2 * kQ4RawBytes > kMaxSmem) continue;
+        int raw = (int)((kMaxSmem - fixed) / kQ4RawBytes);
+        if (raw > 8) raw = 8;
+        p.stages = stages;
+        p.raw_stages = raw;
+        p.smem_bytes = 1024 + stages * stage_bytes + (size_t)raw * kQ4RawBytes +
+                       (2 * stages + 2 * raw + 2 * p.n_acc + 1) * 8 + 16;
+        return p.smem_bytes <= kMaxSmem;
+    }
+    return false;
+}
+
+cudaError_t launch_gemm_decode_q4(const DecodeMapsQ4 &maps, const DecodePlan &plan, const int32_t *ids,
+                                  float *partials, int *err, cudaStream_t stream)
+{
+    cudaError_t e = ensure_smem_attr((const void *)gemm_decode_q4_kernel, plan.smem_bytes);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(gemm_decode_q4_kernel, dim3(plan.grid), dim3(kQ4Threads), plan.smem_bytes, stream, maps,
+                      narrow_plan<1>(plan), ids, partials, err);
+}
+
+cudaError_t launch_dequant_q4(const uint8_t *Wq, const uint16_t *scales, const uint8_t *zeros, int d_out,
+                              int d_in, uint16_t *W, cudaStream_t stream)
+{
+    cudaError_t e = ensure_smem_attr((const void *)dequant_q4_kernel, 0);
+    if (e != cudaSuccess) return e;
+    const size_t chunks = (size_t)d_out * (d_in / 8);
+    const int grid = (int)std::min<size_t>((chunks + 255) / 256, 152 * 16);
+    dequant_q4_kernel<<<grid, 256, 0, stream>>>(Wq, scales, zeros, d_out, d_in, W);
+    return cudaGetLastError();
 }
 
 }  // namespace lora

@@ -133,6 +133,7 @@ struct DecodePlanHead {
     uint64_t *trace;        // measurement hook: LORA_KERNEL_SLOTS x 4 words (see trace_enter), or nullptr
     uint32_t tmem_cols;
     size_t smem_bytes;
+    int raw_stages;         // 4-bit base: stages of the ring of codes (0: a bf16 base)
 };
 
 template <int NP>
@@ -149,6 +150,13 @@ struct DecodeMapsT {
 };
 using DecodeMaps = DecodeMapsT<kMaxGroup>;
 
+// The 4-bit base (one layer): codes [d_out][d_in/2] bytes, box 64 B x 128 rows; scales
+// [d_in/128][d_out] bf16 and zeros [d_in/128][d_out] bytes, boxes 128 x 1.
+constexpr int kQ4Group = 128;
+struct DecodeMapsQ4 {
+    CUtensorMap Wq, S, Z, X;
+};
+
 // Shapes and the stream-K split (pointers left for the caller to fill);
 // max_G bounds the number of ranges. False when the shapes are out of range.
 bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max_pages, int max_G,
@@ -158,6 +166,15 @@ size_t decode_partials_floats(const DecodePlan &p);
 // pool (ids == nullptr: no shrink). err takes the timeout bit.
 cudaError_t launch_gemm_decode(const DecodeMaps &maps, const DecodePlan &plan, const int32_t *ids,
                                float *partials, int *err, cudaStream_t stream);
+// The same kernel's plan and launch for a 4-bit base (one layer): the W tiles are
+// dequantised in shared memory (plan_decode_q4 sets the stage counts; false when they
+// do not fit).
+bool plan_decode_q4(DecodePlan *plan);
+cudaError_t launch_gemm_decode_q4(const DecodeMapsQ4 &maps, const DecodePlan &plan, const int32_t *ids,
+                                  float *partials, int *err, cudaStream_t stream);
+// The 4-bit base to bf16 [d_out][d_in] (prefill path; d_in % 128 == 0).
+cudaError_t launch_dequant_q4(const uint8_t *Wq, const uint16_t *scales, const uint8_t *zeros, int d_out,
+                              int d_in, uint16_t *W, cudaStream_t stream);
 // Y_m = bf16(sum of split-K partials + s_i V_m[t] B_i); ids == nullptr: no branch.
 // Launched with programmatic stream serialization after launch_gemm_decode.
 cudaError_t launch_finish_decode(const DecodePlan &plan, const float *partials, const int32_t *ids,
@@ -190,5 +207,8 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t bytes);
 bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
                        uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows,
                        bool swizzle128 = true);
+// The same for a byte tensor (no swizzle).
+bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                     uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows);
 
 }  // namespace lora

@@ -382,6 +382,66 @@ lora_status run_decode(lora_pool *const *pools, int n, const void *const *X, con
 }
 
 lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t *ids, int T,
+                       void *Y, cudaStream_t stream, bool with_lora);
+
+// The layer over a 4-bit base: decode-sized batches run the GEMM kernel that
+// dequantises W tiles in shared memory; larger ones dequantise W into pool scratch and
+// run the bf16 prefill path.
+lora_status run_linear_q4(lora_pool *p, const void *X, const void *Wq, const void *S, const void *Z,
+                          const int32_t *ids, int T, void *Y, cudaStream_t stream, bool with_lora)
+{
+    if (!p || !X || !Wq || !S || !Z || !Y || (with_lora && !ids) || T < 0) return LORA_ERR_ARG;
+    if (p->d_in % kQ4Group != 0 || p->d_out % 16 != 0) return LORA_ERR_SHAPE;
+    if (((uintptr_t)Wq | (uintptr_t)S | (uintptr_t)Z) & 15) return LORA_ERR_ARG;  // 16-byte loads
+    int path = p->path;
+    if (path == LORA_PATH_AUTO) path = T <= kDecodeMaxT ? LORA_PATH_DECODE : LORA_PATH_PREFILL;
+    if (path == LORA_PATH_DECODE && T > kDecodeMaxT) return LORA_ERR_ARG;
+    if (T == 0) return LORA_OK;
+    if (path == LORA_PATH_PREFILL) {
+        if (!p->wdq) {
+            lora_status st = alloc_dev(p, (void **)&p->wdq, (size_t)p->d_out * p->d_in * 2);
+            if (st != LORA_OK) return st;
+        }
+        CUDA_TRY(launch_dequant_q4(static_cast<const uint8_t *>(Wq), static_cast<const uint16_t *>(S),
+                                   static_cast<const uint8_t *>(Z), p->d_out, p->d_in, p->wdq, stream));
+        return run_linear(p, X, p->wdq, ids, T, Y, stream, with_lora);
+    }
+    lora_status st = ensure_scratch(p, T);
+    if (st == LORA_OK) st = order_after_changes(p, stream);
+    if (st != LORA_OK) return st;
+    const int no_pages = 0;
+    DecodePlan plan;
+    if (!plan_decode(1, T, &p->d_in, &p->d_out, with_lora ? &p->max_pages : &no_pages, p->num_sms, &plan))
+        return LORA_ERR_SHAPE;
+    plan.prob[0].pool = pool_view(p);
+    if (!plan_decode_q4(&plan)) return LORA_ERR_SHAPE;
+    if ((st = ensure_partials(p, decode_partials_floats(plan))) != LORA_OK) return st;
+    DecodeMapsQ4 maps;
+    const int groups = p->d_in / kQ4Group;
+    if (!make_tmap_u8_2d(&maps.Wq, Wq, p->d_in / 2, p->d_out, p->d_in / 2, 64, 128) ||
+        !make_tmap_bf16_2d(&maps.S, S, p->d_out, groups, (uint64_t)p->d_out * 2, 128, 1, false) ||
+        !make_tmap_u8_2d(&maps.Z, Z, p->d_out, groups, p->d_out, 128, 1) ||
+        !make_tmap_bf16_2d(&maps.X, X, p->d_in, T, (uint64_t)p->d_in * 2, 64, plan.ntok))
+        return LORA_ERR_ARG;
+    DecodeProblem &q = plan.prob[0];
+    q.X = static_cast<const uint16_t *>(X);
+    q.V = p->V;
+    q.ldv = p->ldv;
+    q.Y = static_cast<uint16_t *>(Y);
+    q.err = p->d_err;
+    plan.trace = next_trace(p);
+    const int32_t *tids = with_lora ? ids : nullptr;
+    CallMarks marks{p, stream};
+    if (!marks.begin()) return LORA_ERR_CUDA;
+    CUDA_TRY(launch_gemm_decode_q4(maps, plan, tids, p->partials, p->d_err, stream));
+    if (!marks.mark(2)) return LORA_ERR_CUDA;
+    CUDA_TRY(launch_finish_decode(plan, p->partials, tids, stream));
+    if (!marks.mark(3)) return LORA_ERR_CUDA;
+    p->n_calls += 1;
+    return note_call(p, stream);
+}
+
+lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t *ids, int T,
                        void *Y, cudaStream_t stream, bool with_lora)
 {
     if (!p || !X || !W || !Y || (with_lora && !ids) || T < 0) return LORA_ERR_ARG;
@@ -571,6 +631,7 @@ lora_status lora_pool_destroy(lora_pool_t p)
     free_dev(p, p->stage_A, 0);
     free_dev(p, p->stage_B, 0);
     free_dev(p, p->load_A, 0);
+    free_dev(p, p->wdq, 0);
     free_dev(p, p->load_B, 0);
     free_dev(p, p->d_page_list, 0);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
@@ -730,6 +791,31 @@ lora_status lora_base_linear(lora_pool_t p, const void *X, const void *W_base, i
                              lora_stream_t stream)
 {
     return run_linear(p, X, W_base, nullptr, T, Y, (cudaStream_t)stream, false);
+}
+
+lora_status lora_linear_q4(lora_pool_t p, const void *X, const void *Wq, const void *scales,
+                           const void *zeros, const int32_t *token_adapter_ids, int T, void *Y,
+                           lora_stream_t stream)
+{
+    return run_linear_q4(p, X, Wq, scales, zeros, token_adapter_ids, T, Y, (cudaStream_t)stream, true);
+}
+
+lora_status lora_base_linear_q4(lora_pool_t p, const void *X, const void *Wq, const void *scales,
+                                const void *zeros, int T, void *Y, lora_stream_t stream)
+{
+    return run_linear_q4(p, X, Wq, scales, zeros, nullptr, T, Y, (cudaStream_t)stream, false);
+}
+
+lora_status lora_dequant_q4(const void *Wq, const void *scales, const void *zeros, int d_out, int d_in,
+                            void *W, lora_stream_t stream)
+{
+    if (!Wq || !scales || !zeros || !W) return LORA_ERR_ARG;
+    if (!dims_ok(d_in) || !dims_ok(d_out) || d_in % kQ4Group != 0) return LORA_ERR_SHAPE;
+    if (((uintptr_t)Wq | (uintptr_t)W) & 15) return LORA_ERR_ARG;  // 4- and 16-byte accesses
+    CUDA_TRY(launch_dequant_q4(static_cast<const uint8_t *>(Wq), static_cast<const uint16_t *>(scales),
+                               static_cast<const uint8_t *>(zeros), d_out, d_in, static_cast<uint16_t *>(W),
+                               (cudaStream_t)stream));
+    return LORA_OK;
 }
 
 lora_status lora_linear_grouped(int n, const lora_pool_t *pools, const void *const *X,
@@ -1001,8 +1087,7 @@ cudaError_t ensure_smem_attr(const void *kernel, size_t bytes)
     return e;
 }
 
-bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+static PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder()
 {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     static std::once_flag once;
@@ -1014,6 +1099,27 @@ bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint6
             q == cudaDriverEntryPointSuccess)
             encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     });
+    return encode;
+}
+
+bool make_tmap_u8_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                     uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
+    if (!encode || rows == 0) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tmap_bf16_2d(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                       uint64_t row_pitch_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tmap_encoder();
     if (!encode || rows == 0) return false;
     const cuuint64_t dims[2] = {inner, rows};
     const cuuint64_t strides[1] = {row_pitch_bytes};

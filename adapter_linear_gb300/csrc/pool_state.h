@@ -55,6 +55,7 @@ struct lora_pool {
     int *h_err = nullptr;             // pinned copy of d_err[1]
     uint16_t *stage_A = nullptr, *stage_B = nullptr;  // swap-ins of the host tier
     uint16_t *load_A = nullptr, *load_B = nullptr;    // lora_load_adapter's copy of A, B
+    uint16_t *wdq = nullptr;  // a 4-bit base dequantised to bf16 for the prefill path (first use)
     int32_t *d_page_list = nullptr;
     // Changes of pages and table rows (loads, unloads, chains, swap-ins) run on the
     // copy stream, which waits for every layer call enqueued on the pool before them;

@@ -330,6 +330,44 @@ lora_status lora_base_linear(lora_pool_t pool, const void *X, const void *W_base
                              void *Y, lora_stream_t stream);
 
 /*
+ * The layer over a 4-bit quantised base ("多 LoRA 热插拔: 一模型服多租户" (vLLM
+ * tutorial), section 性能注意事项: a base quantised to 4 bits, AWQ-INT4, serves the
+ * bf16 adapters unchanged). The pages give no format; this one is used:
+ *   Wq: device bytes [d_out][d_in / 2], two unsigned 4-bit codes per byte along the
+ *       input dimension (the even input in the low nibble): the nn.Linear layout;
+ *   scales: device bf16 [d_in / 128][d_out], one per (group of 128 inputs, output row);
+ *   zeros: device bytes [d_in / 128][d_out], the 4-bit zero points (0..15);
+ *   W[n][k] = bf16(scales[k/128][n] * (q[n][k] - zeros[k/128][n])): the exact product,
+ *   rounded once to bf16 (to nearest, ties to even), as a kernel that dequantises to
+ *   the activation type before its bf16 product would. Then Y as lora_linear computes
+ *   it, with the same ids, pool and rules. d_in must be a multiple of 128 and d_out of
+ *   16 (the pool's shapes).
+ * Decode-sized batches (T <= 256) stream the codes (a quarter of a bf16 base's bytes)
+ * and dequantise W tiles in shared memory on the way to the tensor cores; larger batches
+ * dequantise W into pool scratch (d_out x d_in bf16, allocated on the first such call,
+ * which then synchronises like a scratch growth) and run the bf16 prefill path.
+ * Wq, scales and zeros must start on 16-byte boundaries.
+ * Errors: as lora_linear; SHAPE when d_in % 128 or d_out % 16 is not zero; ARG for a
+ * pointer that is null or not 16-byte aligned.
+ */
+lora_status lora_linear_q4(lora_pool_t pool, const void *X, const void *Wq, const void *scales,
+                           const void *zeros, const int32_t *token_adapter_ids, int T, void *Y,
+                           lora_stream_t stream);
+
+/* The base product over the 4-bit base only (no adapters; the reference point of the
+ * adapters' overhead on that base). Same arguments and rules as lora_linear_q4. */
+lora_status lora_base_linear_q4(lora_pool_t pool, const void *X, const void *Wq, const void *scales,
+                                const void *zeros, int T, void *Y, lora_stream_t stream);
+
+/* The 4-bit base (the format of lora_linear_q4, device pointers) dequantised to bf16
+ * W [d_out][d_in], asynchronously on `stream`. Needs no pool.
+ * Wq and W must start on 16-byte boundaries.
+ * Errors: ARG (null or misaligned pointers), SHAPE (d_in not a multiple of 128, or a dimension
+ * outside 8..LORA_MAX_DIM or not a multiple of 8), CUDA. */
+lora_status lora_dequant_q4(const void *Wq, const void *scales, const void *zeros, int d_out, int d_in,
+                            void *W, lora_stream_t stream);
+
+/*
  * Base product Y = X W_base^T for callers that cannot allocate device memory.
  * The pages have no counterpart for this call: it exists for users of this
  * library who may not call cudaMalloc (code living inside another framework's

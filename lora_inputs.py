@@ -126,6 +126,21 @@ def zipf_ids(seed: int, n: int, n_slots: int, s: float = 1.0, index: int = 0) ->
     return np.searchsorted(cdf, u, side="right").clip(0, n_slots - 1).astype(np.int32)
 
 
+def q4_weight(seed: int, d_out: int, d_in: int, std: float, index: int = 0, group: int = 128):
+    """A random 4-bit base of the layout lora_linear_q4 takes: codes uniform over
+    0..15 packed two per byte (the even input in the low nibble), zero points 7 or 8,
+    bf16 scales near std / 4.6 (the codes minus the zero point have a spread of ~4.6),
+    so that the dequantised weights have about the standard deviation std.
+    Returns (Wq uint8 [d_out, d_in/2], scales uint16 bf16 bits [d_in/group, d_out],
+    zeros uint8 [d_in/group, d_out])."""
+    g = rng_for(seed, ROLE_W, 1000 + index)
+    codes = g.integers(0, 16, size=(d_out, d_in), dtype=np.uint8)
+    Wq = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    zeros = g.integers(7, 9, size=(d_in // group, d_out), dtype=np.uint8)
+    s = (std / 4.6) * (1.0 + 0.1 * g.standard_normal(size=zeros.shape))
+    return Wq, f32_to_bf16_bits(s.astype(np.float32)), zeros
+
+
 # ---------------------------------------------------------------- workloads
 
 def tiny(seed: int = 0, T: int = 64) -> Problem:
