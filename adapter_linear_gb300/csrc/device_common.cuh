@@ -109,12 +109,16 @@ __device__ __forceinline__ float dot8_f32_bf16(const float *v, const uint4 &b, f
 // zz holds 128 + z twice, ss the scale twice.
 __device__ __forceinline__ uint4 dequant8_q4(uint32_t w, __nv_bfloat162 zz, __nv_bfloat162 ss)
 {
+    // byte j of w: input 2j in the low nibble, 2j + 1 in the high one
+    const uint32_t x = w & 0x0F0F0F0Fu, y = (w >> 4) & 0x0F0F0F0Fu;
+    const uint32_t t01 = __byte_perm(x, y, 0x5140);  // q0 q1 q2 q3 as bytes
+    const uint32_t t23 = __byte_perm(x, y, 0x7362);  // q4 q5 q6 q7
+    const uint32_t bits[4] = {__byte_perm(t01, 0x43u, 0x4140), __byte_perm(t01, 0x43u, 0x4342),
+                              __byte_perm(t23, 0x43u, 0x4140), __byte_perm(t23, 0x43u, 0x4342)};
     uint32_t o[4];
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint32_t b = (w >> (8 * p)) & 0xFFu;
-        const uint32_t bits = 0x43004300u | (b & 0xFu) | ((b >> 4) << 16);
-        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&bits);
+    for (int p = 0; p < 4; ++p) {  // bf16 pairs (128 + q_2p, 128 + q_2p+1)
+        __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162 *>(&bits[p]);
         v = __hmul2(__hsub2(v, zz), ss);
         o[p] = *reinterpret_cast<const uint32_t *>(&v);
     }

@@ -440,9 +440,11 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
 //  * warp 4 streams the codes of each (tile, k-block) unit (128 rows x 64 bytes) with
 //    its 128 scales and zero points into a deep ring of 9 KB stages; they are weights,
 //    so nothing waits on the previous kernel;
-//  * warps 7-10 (32 rows each) turn a unit's codes into the bf16 W tile of an operand
-//    stage, in the 128-byte-swizzled layout a TMA load would have written (one thread
-//    per 16-byte chunk: 4 code bytes -> 8 values, by dequant8_q4);
+//  * warps 7-10 turn a unit's codes into the bf16 W tile of an operand stage, in the
+//    128-byte-swizzled layout a TMA load would have written: one thread per W row, its
+//    64 code bytes read as four 16-byte words issued together (in an order rotated by
+//    lane pair, so that 8 lanes touch 8 different bank groups), 8 values per 4 bytes by
+//    dequant8_q4, stored as 16 chunks (conflict-free through the swizzle);
 //  * warp 6 loads X into the same operand stage after the wait on the previous kernel;
 //    the stage is full when its X bytes have landed and the four dequant warps have
 //    arrived;
@@ -561,7 +563,8 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
     } else if (warp >= 7) {
         // ------------------------------------------------------- dequant warps
         named_bar_sync(kBarSetup, kQ4Threads);
-        const int dw = warp - 7;  // rows 32 dw .. 32 dw + 31 of each tile
+        const int row = (warp - 7) * 32 + lane;  // this thread's W row of each tile
+        const int rot = (lane >> 1) & 3;
         int it = 0;
         for (int u = u0; u < u1; ++u, ++it) {
             const int i = it % raw, st = it % stages;
@@ -574,17 +577,24 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
             const uint8_t *rb = rawbuf + (size_t)i * kQ4RawBytes;
-            const uint16_t *sc = reinterpret_cast<const uint16_t *>(rb + kQ4CodeBytes);
-            const uint8_t *zp = rb + kQ4CodeBytes + 256;
-            uint8_t *ws = smem + (size_t)st * stage_bytes;
-#pragma unroll 4
-            for (int j = 0; j < 16; ++j) {
-                // lanes 0-15 one row, 16-31 the next; lane & 15 = the row's 16-byte chunk
-                const int row = dw * 32 + 2 * j + (lane >> 4), ch = lane & 15;
-                const uint32_t w = *reinterpret_cast<const uint32_t *>(rb + row * 64 + ch * 4);
-                const uint4 v = dequant8_q4(w, q4_zero_pair(zp[row]), q4_scale_pair(sc[row]));
-                const int b = ch >> 3, cc = ch & 7;
-                *reinterpret_cast<uint4 *>(ws + b * kWTileBytes + row * 128 + ((cc ^ (row & 7)) << 4)) = v;
+            const __nv_bfloat162 ss =
+                q4_scale_pair(reinterpret_cast<const uint16_t *>(rb + kQ4CodeBytes)[row]);
+            const __nv_bfloat162 zz = q4_zero_pair(rb[kQ4CodeBytes + 256 + row]);
+            const uint4 *codes = reinterpret_cast<const uint4 *>(rb + row * 64);
+            uint4 cw[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) cw[q] = codes[(q + rot) & 3];
+            uint8_t *wrow = smem + (size_t)st * stage_bytes + row * 128;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int qq = (q + rot) & 3;  // inputs 32 qq .. 32 qq + 31 of the unit
+                const uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int ch = qq * 4 + h;  // inputs 8 ch .. 8 ch + 7
+                    *reinterpret_cast<uint4 *>(wrow + (ch >> 3) * kWTileBytes + (((ch & 7) ^ (row & 7)) << 4)) =
+                        dequant8_q4(words[h], zz, ss);
+                }
             }
             fence_proxy_async_smem();  // the tensor cores read what the threads wrote
             __syncwarp();

@@ -73,6 +73,12 @@ def workload(name: str):
         p = L.q_proj_decode()
         return p, {"workload": "Llama-2-7B q_proj decode", "T": 64, "d_in": 4096, "d_out": 4096,
                    "adapters": 200, "rank": 16, "alpha": 32, "ids": "uniform 0..199"}
+    if name == "q_proj_decode_q4":
+        p = L.q_proj_decode()
+        return p, {"workload": "Llama-2-7B q_proj decode over a 4-bit base", "T": 64, "d_in": 4096,
+                   "d_out": 4096, "adapters": 200, "rank": 16, "alpha": 32, "ids": "uniform 0..199",
+                   "base": "4-bit codes, bf16 scale and 4-bit zero point per 128 inputs per row "
+                           "(AWQ-INT4 layout); bf16 adapters"}
     if name == "hotswap_T256":
         p, _ = L.hotswap()
         return p, {"workload": "q_proj decode, 2000 paged adapters, Zipf ids", "T": 256,
@@ -106,12 +112,20 @@ def workload(name: str):
     raise SystemExit(f"unknown workload {name}")
 
 
-def algorithmic_bytes(p):
-    """Bytes the layer must move once: X, W, Y, ids and the distinct adapters' A and B."""
+def q4_base(p):
+    """The 4-bit base of a q4 workload: codes, scales, zero points (weight std 1/64)."""
+    return L.q4_weight(p.seed, p.d_out, p.d_in, 1.0 / 64)
+
+
+def algorithmic_bytes(p, q4=False):
+    """Bytes the layer must move once: X, W, Y, ids and the distinct adapters' A and B.
+    A 4-bit W is its codes (half a byte per weight) and one bf16 scale and one byte of
+    zero point per 128 weights."""
     T = p.T
     distinct = set(int(i) for i in p.ids if i >= 0)
+    w = p.d_out * p.d_in // 2 + (p.d_in // 128) * p.d_out * 3 if q4 else p.d_out * p.d_in * 2
     return {
-        "x": T * p.d_in * 2, "w": p.d_out * p.d_in * 2, "y": T * p.d_out * 2, "ids": T * 4,
+        "x": T * p.d_in * 2, "w": w, "y": T * p.d_out * 2, "ids": T * 4,
         "adapters": sum(p.adapters[i].rank * (p.d_in + p.d_out) * 2 for i in distinct),
         "adapter_A": sum(p.adapters[i].rank * p.d_in * 2 for i in distinct),
         "adapter_B": sum(p.adapters[i].rank * p.d_out * 2 for i in distinct),
@@ -517,10 +531,10 @@ class Kit:
         return statistics.median(iso)
 
 
-def roofline_decode(ab, gemm_ms, peaks, traffic):
+def roofline_decode(ab, gemm_ms, peaks, traffic, kernel="gemm_decode_kernel"):
     gemm_bytes = ab["w"] + ab["x"] + ab["adapter_A"]
     achieved = gemm_bytes / (gemm_ms * 1e-3) / 1e9 if gemm_ms > 0 else None
-    return {"kernel": "gemm_decode_kernel", "bound": "hbm", "achieved": achieved,
+    return {"kernel": kernel, "bound": "hbm", "achieved": achieved,
             "peak": peaks["hbm_gbs"], "unit": "GB/s",
             "frac": achieved / peaks["hbm_gbs"] if achieved else None, "traffic": traffic,
             "algorithmic_bytes": gemm_bytes,
@@ -555,6 +569,9 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
     """A record for one single-layer workload (one lora_linear call per step)."""
     torch, al, args = kit.torch, kit.al, kit.args
     p, cfg = workload(name)
+    q4 = name.endswith("_q4")
+    if q4:
+        with_e2e = False  # the host-buffer entry point takes a bf16 base
     A_dev = {s: kit.t(ad.A) for s, ad in p.adapters.items()}
     B_dev = {s: kit.t(ad.B) for s, ad in p.adapters.items()}
 
@@ -567,23 +584,29 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
 
     # R layers, each its own W and adapter pool (like the layers of a model): the
     # layers' footprint is more than 3x L2, so no flush is needed between steps
-    W0 = kit.t(p.W)
+    W0 = tuple(kit.t(a) for a in q4_base(p)) if q4 else (kit.t(p.W),)
     layers = [new_layer(W0)]
-    layer_bytes = W0.numel() * 2 + layers[0][0].stats()["bytes_held"]
+    layer_bytes = sum(t.numel() * t.element_size() for t in W0) + layers[0][0].stats()["bytes_held"]
     R = max(2, min(32, -(-3 * kit.l2 // layer_bytes)))
     while len(layers) < R:
-        layers.append(new_layer(W0.clone()))
+        layers.append(new_layer(tuple(t.clone() for t in W0)))
     del A_dev, B_dev
     X, ids = kit.t(p.X), kit.t(p.ids)
     Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=kit.dev)
 
     def lora_step(k):
         pool, W = layers[k % R]
-        pool.linear(X, W, ids, Y)
+        if q4:
+            pool.linear_q4(X, *W, ids, Y)
+        else:
+            pool.linear(X, W[0], ids, Y)
 
     def base_step(k):
         pool, W = layers[k % R]
-        pool.base_linear(X, W, Y)
+        if q4:
+            pool.base_linear_q4(X, *W, Y)
+        else:
+            pool.base_linear(X, W[0], Y)
 
     for k in range(max(args.warmup, R)):
         lora_step(k)
@@ -626,7 +649,7 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
 
     e2e = None
     if with_e2e:
-        pool0, W = layers[0]
+        pool0, (W,) = layers[0]
         Xh = torch.from_numpy(p.X.view(np.int16)).view(torch.bfloat16).pin_memory()
         idh = torch.from_numpy(p.ids).pin_memory()
         Yh = torch.empty((p.T, p.d_out), dtype=torch.bfloat16).pin_memory()
@@ -648,12 +671,13 @@ def measure_layer(kit: Kit, name: str, K: int, with_e2e=True, headline=False):
         assert pool.check_errors() == al.LORA_OK
     kit.barrier()
 
-    ab = algorithmic_bytes(p)
+    ab = algorithmic_bytes(p, q4)
     step_ms = total_ms / K
     gemm_share = tr["share"]["base_gemm"]
     if decode:
         roof = roofline_decode(ab, gemm_share, kit.peaks,
-                               profiled_traffic(name) if headline else None)
+                               profiled_traffic(name) if headline else None,
+                               "gemm_decode_q4_kernel" if q4 else "gemm_decode_kernel")
         sb = step_bytes(ab)
         step_roof = {"bound": "hbm", "achieved": sb / (step_ms * 1e-3) / 1e9, "unit": "GB/s",
                      "peak": kit.peaks["hbm_gbs"],
@@ -1020,10 +1044,16 @@ def run_profile_calls(args):
     for slot, ad in p.adapters.items():
         pool.load_adapter(slot, t(ad.A), t(ad.B), ad.rank, ad.alpha)
     pool.reserve(p.T)
-    X, W, ids = t(p.X), t(p.W), t(p.ids)
+    X, ids = t(p.X), t(p.ids)
     Y = torch.empty((p.T, p.d_out), dtype=torch.bfloat16, device=dev)
-    for _ in range(args.profile):
-        pool.linear(X, W, ids, Y)
+    if name.endswith("_q4"):
+        Wq = tuple(t(a) for a in q4_base(p))
+        for _ in range(args.profile):
+            pool.linear_q4(X, *Wq, ids, Y)
+    else:
+        W = t(p.W)
+        for _ in range(args.profile):
+            pool.linear(X, W, ids, Y)
     torch.cuda.synchronize(dev)
     assert pool.check_errors() == al.LORA_OK
     pool.close()
@@ -1037,7 +1067,7 @@ def run_cpu_probe(args):
     print(json.dumps({"value": rate, "cores": cores, "sample": sample}), flush=True)
 
 
-CONFIG_ORDER = ("tiny", "llama3_layer", "prefill_mixed", "prefill_mixed_padded", "prefill_r16",
+CONFIG_ORDER = ("tiny", "llama3_layer", "q_proj_decode_q4", "prefill_mixed", "prefill_mixed_padded", "prefill_r16",
                 "hotswap_T256", "hotswap_stream")
 
 
