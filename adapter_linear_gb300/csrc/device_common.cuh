@@ -226,9 +226,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
 // Wait for the phase with `parity` to complete, for at most limit_ns.
 // Returns false (after raising the CTA's abort flag and, when err is not null,
 // the pool's timeout bit) if it runs out, or if another role of the CTA has
-// already aborted.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
-                                       int *err, uint64_t limit_ns = kWaitTimeoutNs)
+// already aborted. Inlined: for loops that wait once per pipeline unit.
+__device__ __forceinline__ bool mbar_wait_inl(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                             int *err, uint64_t limit_ns = kWaitTimeoutNs)
 {
     if (mbar_try_wait(bar, parity)) return true;
     uint64_t start = global_timer_ns();
@@ -243,6 +243,13 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, vo
             }
         }
     }
+}
+
+// The same wait out of line (most call sites: keeps the kernels' code small).
+static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort_flag,
+                                       int *err, uint64_t limit_ns = kWaitTimeoutNs)
+{
+    return mbar_wait_inl(bar, parity, abort_flag, err, limit_ns);
 }
 
 // ---------------------------------------------------------------------- TMA
@@ -583,6 +590,7 @@ __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count)
 {
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+
 
 // ------------------------------------------------ programmatic dependent launch
 

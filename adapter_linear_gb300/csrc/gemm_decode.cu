@@ -519,7 +519,7 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
             int it = 0;
             for (int u = u0; u < u1; ++u, ++it) {
                 const int i = it % raw;
-                if (it >= raw && !mbar_wait(&raw_empty[i], ((uint32_t)(it / raw) & 1u) ^ 1u, &abort_flag, err))
+                if (it >= raw && !mbar_wait_inl(&raw_empty[i], ((uint32_t)(it / raw) & 1u) ^ 1u, &abort_flag, err))
                     break;
                 const int tile = u / KB, kb = u - tile * KB;
                 uint8_t *rb = rawbuf + (size_t)i * kQ4RawBytes;
@@ -545,7 +545,7 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
             for (int u = u0; u < u1; ++u, ++it) {
                 const int st = it % stages;
                 if (it >= stages &&
-                    !mbar_wait(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err))
+                    !mbar_wait_inl(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err))
                     break;
                 const int kb = u % KB;
                 uint8_t *xs = smem + (size_t)st * stage_bytes + w_bytes;
@@ -570,9 +570,9 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
             const int i = it % raw, st = it % stages;
             bool ok = true;
             if (lane == 0) {
-                ok = mbar_wait(&raw_full[i], (uint32_t)(it / raw) & 1u, &abort_flag, err);
+                ok = mbar_wait_inl(&raw_full[i], (uint32_t)(it / raw) & 1u, &abort_flag, err);
                 if (ok && it >= stages)
-                    ok = mbar_wait(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err);
+                    ok = mbar_wait_inl(&empty[st], ((uint32_t)(it / stages) & 1u) ^ 1u, &abort_flag, err);
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) break;
@@ -622,13 +622,13 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
                 const bool seg_first = (kb == 0) || (u == u0);
                 if (seg_first) {
                     const int a = seg % n_acc;
-                    if (!mbar_wait(&acc_empty[a], ((uint32_t)(seg / n_acc) & 1u) ^ 1u, &abort_flag, err))
+                    if (!mbar_wait_inl(&acc_empty[a], ((uint32_t)(seg / n_acc) & 1u) ^ 1u, &abort_flag, err))
                         break;
                     tc_fence_after_sync();
                     d = tmem + (uint32_t)(a * p.ntok);
                 }
                 const int st = it % stages;
-                if (!mbar_wait(&full[st], (uint32_t)(it / stages) & 1u, &abort_flag, err)) break;
+                if (!mbar_wait_inl(&full[st], (uint32_t)(it / stages) & 1u, &abort_flag, err)) break;
                 tc_fence_after_sync();
                 const uint32_t wa = smem_u32(smem + (size_t)st * stage_bytes);
                 const uint32_t xa = wa + w_bytes;
@@ -662,7 +662,12 @@ __device__ __forceinline__ void gemm_decode_q4_body(const DecodeMapsQ4 &maps, co
     trace_exit(trace);
 }
 
-__global__ void __launch_bounds__(kQ4Threads, 1)
+// 64 registers: the CTA (352 threads) and two CTAs of the finishing pass fit one SM's
+// register file together, so the kernel launched early beside the previous call's
+// finishing pass starts on every SM at once (measured: q_proj T = 64 over a 4-bit
+// base, 15.8 -> 13.5 us a step with adapters, 12.8 -> 11.4 us base only; at 72
+// registers a CTA of the pass no longer fits and the step is back at 15.5 us).
+__global__ void __maxnreg__(64)
     gemm_decode_q4_kernel(const __grid_constant__ DecodeMapsQ4 maps, const __grid_constant__ DecodePlanT<1> p,
                           const int32_t *__restrict__ ids, float *__restrict__ partials, int *err)
 {
@@ -1107,7 +1112,7 @@ bool plan_decode_q4(DecodePlan *plan)
         const size_t fixed = 1024 + stages * stage_bytes + 512;
         if (fixed + 2 * kQ4RawBytes > kMaxSmem) continue;
         int raw = (int)((kMaxSmem - fixed) / kQ4RawBytes);
-        if (raw > 8) raw = 8;
+        if (raw > 5) raw = 5;  // five units of codes in flight (measured no slower than eight)
         p.stages = stages;
         p.raw_stages = raw;
         p.smem_bytes = 1024 + stages * stage_bytes + (size_t)raw * kQ4RawBytes +
