@@ -109,6 +109,23 @@ __device__ __forceinline__ TileLora tile_lora(int m, const PrefillArgs &a, const
     return r;
 }
 
+// acc[j] += vv . (the 8 rank values of column ncol + j of a B page) for 32 columns;
+// columns past d_out add nothing. The B words are loaded 16 at a time before any of
+// them is used, so that a batch's loads are in flight together.
+__device__ __forceinline__ void expand_page_32(float (&acc)[32], const float (&vv)[8], const uint16_t *bp,
+                                               int ncol, int d_out)
+{
+#pragma unroll
+    for (int j0 = 0; j0 < 32; j0 += 16) {
+        uint4 b[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            b[j] = ncol + j0 + j < d_out ? ldg_nc_v4(bp + (j0 + j) * kRankPage) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[j0 + j] = dot8_f32_bf16(vv, b[j], acc[j0 + j]);
+    }
+}
+
 // One epilogue warp's share of a finished accumulator: TMEM lanes 32*quarter.. (token
 // rows t = row0 + lane), columns 128*half.. of the tile at column n0, in chunks of 32;
 // with `own_expand`, each row's adapter expand added on CUDA cores; rounded to bf16
@@ -150,13 +167,7 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tmem_buf, int quarter, in
                                  bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
                                  bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
             const uint16_t *bp = pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + ncol) * kRankPage;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if (ncol + j < a.d_out) {
-                    const uint4 b = ldg_nc_v4(bp + j * kRankPage);
-                    acc[j] = dot8_f32_bf16(vv, b, acc[j]);
-                }
-            }
+            expand_page_32(acc, vv, bp, ncol, a.d_out);
         }
         if (row_ok) {
 #pragma unroll
@@ -408,13 +419,7 @@ __device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quar
                                      bf16_lo(h.z) + bf16_lo(l.z), bf16_hi(h.z) + bf16_hi(l.z),
                                      bf16_lo(h.w) + bf16_lo(l.w), bf16_hi(h.w) + bf16_hi(l.w)};
                 const uint16_t *bp = pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + ncol) * kRankPage;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    if (ncol + j < a.d_out) {
-                        const uint4 b = ldg_nc_v4(bp + j * kRankPage);
-                        acc[j] = dot8_f32_bf16(vv, b, acc[j]);
-                    }
-                }
+                expand_page_32(acc, vv, bp, ncol, a.d_out);
             }
 #pragma unroll
             for (int k = 0; k < 4; ++k) {

@@ -36,6 +36,7 @@ constexpr int HDR_NUMSEG = 1;   // segments (distinct loaded ids present)
 constexpr int HDR_UNITS = 2;    // sum over segments of ceil(len / kShrinkRows)
 
 constexpr int kShrinkRows = 128;       // token rows per tensor-core shrink unit
+constexpr int kShrinkSmallSeg = 16;    // segments of at most this many tokens: warp-level shrink
 constexpr int kDecodeMaxT = 256;       // largest batch of the decode path
 
 // Device error word bits.
@@ -90,6 +91,8 @@ cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, Seg
 // bf16 hi/lo pairs grouped per 32 rank columns (see shrink.cu) into Vhl [T][ldh].
 // tmA: the A arena with a box of one page (8 rows x 64); tmAw: a box of
 // round16(8 * max_pages) rows x 64 (consecutive pages in one copy).
+cudaError_t launch_shrink_small(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl,
+                                int ldh, int num_sms, int *err, cudaStream_t stream);
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
                              const CUtensorMap &tmAw, const uint16_t *X,
                              int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl, int ldh,

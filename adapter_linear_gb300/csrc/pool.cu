@@ -479,6 +479,7 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         const CUtensorMap *tmY = pair ? tmap_for(p, Y, p->d_out, T, 64, 32) : nullptr;
         if (!tmW || !tmX || !tmV || (pair && !tmY)) return LORA_ERR_ARG;
         if (with_lora) {
+            CUDA_TRY(launch_shrink_small(Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms, p->d_err, stream));
             CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
                                       p->d_err, stream, trace_slot(tr, 1)));
         }

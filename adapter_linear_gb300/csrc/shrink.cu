@@ -11,12 +11,20 @@
 // into the same 128-byte-swizzled layout), fp32 accumulator in TMEM,
 // double-buffered so one unit's epilogue overlaps the next unit's MMAs.
 //
+// Segments of at most kShrinkSmallSeg tokens, and segments whose tokens are not
+// consecutive rows of X (a batch whose tokens are spread over many adapters), are left
+// to shrink_small_kernel (warp-level MMAs on 16-token chunks): a 128-row tile holding a
+// few tokens would still run the whole K loop here, and scattered rows would have to be
+// gathered by one warp.
+//
 // Output Vhl, bf16 [T][ldh], row = token: each fp32 value v is stored as the
 // pair hi = bf16(v), lo = bf16(v - hi) (hi + lo carries about 16 significant
 // bits), grouped per 32 rank columns as [hi 0..31 | lo 0..31] [hi 32..63 | ...],
 // so a 64-column TMA box is exactly the A operand of four MMA K-steps of the
 // expand in the prefill GEMM. Columns past an adapter's rank, up to its last
 // 32-column group, are written as zeros.
+#include <algorithm>
+
 #include "device_common.cuh"
 
 namespace lora {
@@ -33,25 +41,42 @@ constexpr int kSBoxes = 2;
 
 struct UnitInfo {
     int p0, p1;       // positions in `order`
+    bool small;       // the segment is left to the warp-level shrink (seg_on_warp_shrink)
     int npages;       // adapter pages
     int n;            // MMA N: npages * 8 rounded up to 16
     const int32_t *pages;
     const int32_t *scales;  // fp32 bits, one per page (up to n / 8 entries readable)
 };
 
-__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs, int T,
-                                              int *err)
+// The segment of shrink unit u: the largest s with seg_ublk[s] <= u (seg_ublk ascending,
+// [num_seg + 1]).
+__device__ __forceinline__ int unit_segment(int u, const SegTables &tabs)
 {
-    // segment s: largest s with seg_ublk[s] <= u (seg_ublk ascending, [num_seg + 1])
     int lo = 0, hi = tabs.hdr[HDR_NUMSEG];
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
         if (tabs.seg_ublk[mid] <= u) lo = mid; else hi = mid;
     }
-    const int s = lo;
+    return lo;
+}
+
+// Whether segment s runs on the warp-level shrink: at most kShrinkSmallSeg tokens, or
+// tokens that are not consecutive rows (the order inside a segment ascends, so the
+// rows are consecutive exactly when the last minus the first is the length minus one).
+__device__ __forceinline__ bool seg_on_warp_shrink(int s, const SegTables &tabs)
+{
+    const int p0 = tabs.seg_start[s], len = tabs.seg_start[s + 1] - p0;
+    return len <= kShrinkSmallSeg || tabs.order[p0 + len - 1] - tabs.order[p0] != len - 1;
+}
+
+__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs, int T,
+                                              int *err)
+{
+    const int s = unit_segment(u, tabs);
     UnitInfo r;
     r.p0 = tabs.seg_start[s] + (u - tabs.seg_ublk[s]) * kShrinkRows;
     r.p1 = min(r.p0 + kShrinkRows, tabs.seg_start[s + 1]);
+    r.small = seg_on_warp_shrink(s, tabs);
     int slot = tabs.seg_slot[s];
 #ifdef LORA_CHECK
     // a unit outside the tokens or a slot outside the pool: an empty unit of slot 0
@@ -131,6 +156,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const UnitInfo ui = unit_info(u, pool, tabs, T, err);
+            if (ui.small) continue;  // (every role skips the same units)
             const int row0 = LORA_CHECKED(tabs.order[ui.p0], 0, T, err, 0);
             bool contiguous = true;
             for (int r = lane; r < ui.p1 - ui.p0; r += 32)
@@ -154,20 +180,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 uint8_t *xs = smem + (size_t)s * stage_bytes;
                 uint8_t *ps = xs + x_bytes;
                 if (!contiguous) {
-                    // gather 128 rows x 64 bf16 per box into the 128-byte-swizzled layout
+                    // gather 128 rows x 64 bf16 per box into the 128-byte-swizzled layout;
+                    // a row's 16 loads are issued before its stores (a store waiting for
+                    // its value would hold up the next load)
                     for (int r = lane; r < 128; r += 32) {
                         const int p = ui.p0 + r;
                         const int tok = (p < ui.p1) ? LORA_CHECKED(tabs.order[p], 0, T, err, -1) : -1;
+                        uint4 val[kSBoxes * 8];
 #pragma unroll
-                        for (int b = 0; b < kSBoxes; ++b)
+                        for (int j = 0; j < kSBoxes * 8; ++j) {
+                            const int k = kb * kSBoxes * 64 + j * 8;
+                            val[j] = make_uint4(0, 0, 0, 0);
+                            if (tok >= 0 && k < d_in) val[j] = ldg_nc_v4(X + (size_t)tok * d_in + k);
+                        }
 #pragma unroll
-                            for (int c = 0; c < 8; ++c) {
-                                const int k = (kb * kSBoxes + b) * 64 + c * 8;
-                                uint4 val = make_uint4(0, 0, 0, 0);
-                                if (tok >= 0 && k < d_in) val = ldg_nc_v4(X + (size_t)tok * d_in + k);
-                                *reinterpret_cast<uint4 *>(xs + b * kXTileBytes + r * 128 +
-                                                           ((c ^ (r & 7)) << 4)) = val;
-                            }
+                        for (int j = 0; j < kSBoxes * 8; ++j) {
+                            const int b = j >> 3, c = j & 7;
+                            *reinterpret_cast<uint4 *>(xs + b * kXTileBytes + r * 128 + ((c ^ (r & 7)) << 4)) =
+                                val[j];
+                        }
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -208,6 +239,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
                 const UnitInfo ui = unit_info(u, pool, tabs, T, err);
+                if (ui.small) continue;
                 const int buf = uc & 1;
                 ok = mbar_wait(&acc_empty[buf], ((uint32_t)(uc >> 1) & 1u) ^ 1u, &abort_flag, err);
                 if (!ok) break;
@@ -242,6 +274,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         int uc = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
             const UnitInfo ui = unit_info(u, pool, tabs, T, err);
+            if (ui.small) continue;
             const int buf = uc & 1;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(uc >> 1) & 1u, &abort_flag, err);
@@ -302,6 +335,131 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     trace_exit(trace);
 }
 
+// ======================================== warp-level shrink of small or scattered segments
+//
+// One warp per (128-row unit, chunk of up to 16 tokens, page) of the segments
+// seg_on_warp_shrink picks: D[16 tokens][8 ranks] = X_chunk . A_page^T over d_in with
+// warp-level bf16 MMAs (m16n8k16, fp32 accumulation) -- a 16 x 8 tile is what a few
+// tokens of one adapter need, far below the tcgen05 tile. The operands come straight from
+// global memory in a k order both share (a dot product does not depend on it): in each
+// 32-wide step at k0, thread (g = lane / 4, t = lane % 4) loads the 8 inputs k0 + 8t ..
+// k0 + 8t + 7 of token rows g and g + 8 and of rank row g of the page, and gives elements
+// 0-3 to the first MMA and 4-7 to the second, as the fragment elements of logical columns
+// {2t, 2t+1} and {2t+8, 2t+9}. Thread (g, t) ends with D[g][2t..2t+1] and D[g+8][2t..2t+1],
+// scales them by the page's scale and writes them in the tensor-core kernel's hi/lo column
+// layout (the warp of the adapter's last page also zeroes the rest of its last 32-column
+// group).
+constexpr int kSmallThreads = 128;
+constexpr int kSmallChunk = 16;  // tokens per MMA tile
+static_assert(kShrinkRows % kSmallChunk == 0, "a unit splits into whole chunks");
+
+__device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                                  uint32_t a3, uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__global__ void __launch_bounds__(kSmallThreads)
+    shrink_small_kernel(const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
+                        uint16_t *__restrict__ Vhl, int ldh, int *err, int T, int max_seg)
+{
+    // the unit prefix and the segment starts in shared memory (most work items are empty
+    // chunks, decided from these alone)
+    extern __shared__ int seg_smem[];
+    const int num_seg = tabs.hdr[HDR_NUMSEG];
+    const int nseg = min(num_seg, max_seg);
+    int *ublk = seg_smem, *start = ublk + (max_seg + 1);
+    for (int s = threadIdx.x; s <= nseg; s += blockDim.x) {
+        ublk[s] = tabs.seg_ublk[s];
+        start[s] = tabs.seg_start[s];
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+    constexpr int kChunks = kShrinkRows / kSmallChunk;  // chunks of one unit
+    const int units = ublk[nseg];
+    const int P = pool.max_pages, d_in = pool.d_in;
+    // work items (chunk, unit, page), the chunk index slowest: the first chunk of every
+    // unit (the only one most units have) comes first and spreads over all warps
+    const int items = kChunks * units * P;
+    for (int v = gw; v < items; v += nw) {
+        const int h = v / (units * P), rem = v - h * (units * P);
+        const int u = rem / P, q = rem - u * P;
+        int lo = 0, hi = nseg;  // the unit's segment: the largest s with ublk[s] <= u
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (ublk[mid] <= u) lo = mid; else hi = mid;
+        }
+        const int s = lo;
+        const int p0 = start[s] + (u - ublk[s]) * kShrinkRows + h * kSmallChunk;
+        const int p1u = min(start[s] + (u - ublk[s] + 1) * kShrinkRows, start[s + 1]);
+        if (p0 >= p1u || !seg_on_warp_shrink(s, tabs)) continue;
+        const int len = min(kSmallChunk, p1u - p0);
+#ifdef LORA_CHECK
+        if (!check_range(p0, 0, T, err) || !check_range(p0 + len, p0, T + 1, err)) continue;
+#endif
+        const int slot = LORA_CHECKED(tabs.seg_slot[s], 0, pool.max_adapters, err, 0);
+        const int32_t *row = pool.slots + (size_t)slot * pool.slot_stride;
+        const int npages = row[SLOT_NPAGES];
+        if (q >= npages) continue;
+        const int page = LORA_CHECKED(row[SLOT_PAGES + q], 0, pool.num_pages, err, 0);
+        const float scale = __int_as_float(row[slot_page_scale(P, q)]);
+        const bool has0 = g < len, has8 = g + 8 < len;
+        const int tok0 = has0 ? LORA_CHECKED(tabs.order[p0 + g], 0, T, err, 0) : 0;
+        const int tok8 = has8 ? LORA_CHECKED(tabs.order[p0 + g + 8], 0, T, err, 0) : 0;
+        const uint16_t *x0 = X + (size_t)tok0 * d_in + 8 * t;
+        const uint16_t *x8 = X + (size_t)tok8 * d_in + 8 * t;
+        const uint16_t *ar = pool.A_pages + ((size_t)page * kRankPage + g) * d_in + 8 * t;
+        float d[4] = {0.f, 0.f, 0.f, 0.f}, e[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        // eight 32-wide steps per round: all their loads are issued before their MMAs
+        // (the loads and the MMAs are asm statements that keep their program order)
+        constexpr int kSteps = 8;
+        for (int k0 = 0; k0 < d_in; k0 += 32 * kSteps) {
+            uint4 xa[kSteps], xb[kSteps], w[kSteps];
+#pragma unroll
+            for (int j = 0; j < kSteps; ++j) {
+                const int k = k0 + 32 * j;
+                const bool in = k + 8 * t < d_in;  // d_in is a multiple of 8
+                xa[j] = has0 && in ? ldg_nc_v4(x0 + k) : z;
+                xb[j] = has8 && in ? ldg_nc_v4(x8 + k) : z;
+                w[j] = in ? ldg_nc_v4(ar + k) : z;
+            }
+#pragma unroll
+            for (int j = 0; j < kSteps; ++j) {
+                mma_m16n8k16_bf16(d, xa[j].x, xb[j].x, xa[j].y, xb[j].y, w[j].x, w[j].y);
+                mma_m16n8k16_bf16(e, xa[j].z, xb[j].z, xa[j].w, xb[j].w, w[j].z, w[j].w);
+            }
+        }
+        // token g: ranks 2t, 2t+1 in d[0..1] + e[0..1]; token g + 8: in d[2..3] + e[2..3]
+        const int col = q * kRankPage + 2 * t;
+        const int group_end = ((npages * kRankPage + 31) / 32) * 32;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            if (half == 0 ? !has0 : !has8) continue;
+            const float a0 = scale * (d[2 * half] + e[2 * half]);
+            const float a1 = scale * (d[2 * half + 1] + e[2 * half + 1]);
+            const uint32_t hv = pack_bf16x2(a0, a1);
+            const uint32_t lv = pack_bf16x2(a0 - bf16_lo(hv), a1 - bf16_hi(hv));
+            uint16_t *hrow = Vhl + (size_t)(half == 0 ? tok0 : tok8) * ldh;
+            uint16_t *dst = hrow + (col / 32) * 64 + (col % 32);
+            *reinterpret_cast<uint32_t *>(dst) = hv;
+            *reinterpret_cast<uint32_t *>(dst + 32) = lv;
+            if (q == npages - 1)  // the rest of the last 32-column group: zeros
+                for (int zc = q * kRankPage + kRankPage + 2 * t; zc < group_end; zc += 8) {
+                    uint16_t *zd = hrow + (zc / 32) * 64 + (zc % 32);
+                    *reinterpret_cast<uint32_t *>(zd) = 0u;
+                    *reinterpret_cast<uint32_t *>(zd + 32) = 0u;
+                }
+        }
+    }
+}
+
 uint32_t pow2_cols(uint32_t n)
 {
     uint32_t c = 32;
@@ -310,6 +468,19 @@ uint32_t pow2_cols(uint32_t n)
 }
 
 }  // namespace
+
+cudaError_t launch_shrink_small(const uint16_t *X, int T, const PoolDev &pool, SegTables tabs, uint16_t *Vhl,
+                                int ldh, int num_sms, int *err, cudaStream_t stream)
+{
+    // the segment tables of up to min(T, adapters) segments in shared memory
+    const int max_seg = T < pool.max_adapters ? T : pool.max_adapters;
+    const size_t smem = 2 * ((size_t)max_seg + 1) * sizeof(int);
+    cudaError_t e = ensure_smem_attr((const void *)shrink_small_kernel, smem);
+    if (e != cudaSuccess) return e;
+    // work items (unit, chunk, page) strided over six CTAs of four warps per SM
+    shrink_small_kernel<<<6 * num_sms, kSmallThreads, smem, stream>>>(X, pool, tabs, Vhl, ldh, err, T, max_seg);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
                              const CUtensorMap &tmAw, const uint16_t *X,

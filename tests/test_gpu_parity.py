@@ -135,6 +135,30 @@ def test_hotswap_stream():
     assert pool.stats()["loads"] == 2000 + len(sched.swaps)
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_scattered_prefill(kernel):
+    """A prefill-sized batch spread over many adapters of mixed ranks (1, 2, 3 and 5
+    pages): most segments hold a few tokens, a Zipf head holds many scattered ones (both
+    on the warp-level shrink, the head in several 16-token chunks), some tokens have no
+    adapter; every 128-token tile of the GEMM mixes adapters (the epilogue expand)."""
+    d, T, n, seed = 512, 300, 120, 91
+    ranks = [8, 16, 24, 40]
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d, d), 1.0 / 32)
+    ids = L.zipf_ids(seed, T, n, 1.0)
+    ids[L.rng_for(seed, L.ROLE_IDS, 5).random(T) < 0.1] = -1
+    ads = {i: L.make_adapter(seed, i, d, d, ranks[i % 4], 2.0 * ranks[i % 4]) for i in range(n)}
+    prob = L.Problem("scattered", d, d, X, W, ids, ads, n, 40, seed)
+    sizes = np.bincount(ids[ids >= 0], minlength=n)
+    assert (sizes[sizes > 0] <= 16).sum() > 20 and sizes.max() > 32  # one-chunk and multi-chunk segments
+    pool = load_pool(al, prob)
+    pool.set_prefill_kernel({"single": al.LORA_PREFILL_SINGLE, "pair": al.LORA_PREFILL_PAIR}[kernel])
+    got = run(pool, prob, PATHS["prefill"])
+    ref, base = ref_of(prob)
+    assert_parity(got, ref, f"scattered/{kernel}")
+    assert_routing(got, ref, base, prob.ids, f"scattered/{kernel}")
+
+
 # ------------------------------------------------------------------ segments
 
 def seg_cases():
