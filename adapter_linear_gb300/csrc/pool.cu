@@ -199,24 +199,28 @@ SegTables seg_tables(const lora_pool *p)
 }
 
 // Tensor maps are pure host descriptors of (pointer, shape, box); a small
-// per-pool cache avoids re-encoding them on every call with the same buffers.
-const CUtensorMap *tmap_for(lora_pool *p, const void *base, uint64_t inner, uint64_t rows,
-                            uint32_t box_inner, uint32_t box_rows)
+// per-pool cache avoids re-encoding them on every call with the same buffers. The map
+// is copied out: a later lookup of the same call may reuse the cache entry.
+bool tmap_for(lora_pool *p, CUtensorMap *out, const void *base, uint64_t inner, uint64_t rows,
+              uint32_t box_inner, uint32_t box_rows)
 {
     for (auto &e : p->tmaps)
         if (e.base == base && e.inner == inner && e.rows == rows && e.box_inner == box_inner &&
-            e.box_rows == box_rows)
-            return &e.map;
+            e.box_rows == box_rows) {
+            *out = e.map;
+            return true;
+        }
     TmapEntry &e = p->tmaps[p->tmap_next];
     p->tmap_next = (p->tmap_next + 1) % (int)(sizeof(p->tmaps) / sizeof(p->tmaps[0]));
     e.base = nullptr;
-    if (!make_tmap_bf16_2d(&e.map, base, inner, rows, inner * 2, box_inner, box_rows)) return nullptr;
+    if (!make_tmap_bf16_2d(&e.map, base, inner, rows, inner * 2, box_inner, box_rows)) return false;
     e.base = base;
     e.inner = inner;
     e.rows = rows;
     e.box_inner = box_inner;
     e.box_rows = box_rows;
-    return &e.map;
+    *out = e.map;
+    return true;
 }
 
 __global__ void pack_adapter_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B,
@@ -359,11 +363,9 @@ lora_status run_decode(lora_pool *const *pools, int n, const void *const *X, con
     DecodeMaps maps;
     for (int m = 0; m < n; ++m) {
         lora_pool *p = pools[m];
-        const CUtensorMap *tmW = tmap_for(p, W[m], p->d_in, p->d_out, 64, 128);
-        const CUtensorMap *tmX = tmap_for(p, X[m], p->d_in, T, 64, plan.ntok);
-        if (!tmW || !tmX) return LORA_ERR_ARG;
-        maps.W[m] = *tmW;
-        maps.X[m] = *tmX;
+        if (!tmap_for(p, &maps.W[m], W[m], p->d_in, p->d_out, 64, 128) ||
+            !tmap_for(p, &maps.X[m], X[m], p->d_in, T, 64, plan.ntok))
+            return LORA_ERR_ARG;
         DecodeProblem &q = plan.prob[m];
         q.pool = pool_view(p);
         q.X = static_cast<const uint16_t *>(X[m]);
@@ -473,18 +475,19 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
         if (!mark(0)) return LORA_ERR_CUDA;
         const bool pair = p->pair_ok && (p->prefill_kernel == LORA_PREFILL_PAIR ||
                                          (p->prefill_kernel == LORA_PREFILL_AUTO && T > 128));
-        const CUtensorMap *tmX = tmap_for(p, X, p->d_in, T, 64, 128);
-        const CUtensorMap *tmW = tmap_for(p, W, p->d_in, p->d_out, 64, pair ? 128 : 256);
-        const CUtensorMap *tmV = tmap_for(p, p->Vhl, p->ldh, T, 64, 128);
-        const CUtensorMap *tmY = pair ? tmap_for(p, Y, p->d_out, T, 64, 32) : nullptr;
-        if (!tmW || !tmX || !tmV || (pair && !tmY)) return LORA_ERR_ARG;
+        CUtensorMap tmX, tmW, tmV, tmY;
+        if (!tmap_for(p, &tmX, X, p->d_in, T, 64, 128) ||
+            !tmap_for(p, &tmW, W, p->d_in, p->d_out, 64, pair ? 128 : 256) ||
+            !tmap_for(p, &tmV, p->Vhl, p->ldh, T, 64, 128) || (pair && !tmap_for(p, &tmY, Y, p->d_out, T, 64, 32)))
+            return LORA_ERR_ARG;
         if (with_lora) {
             CUDA_TRY(launch_shrink_small(Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms, p->d_err, stream));
-            CUDA_TRY(launch_shrink_tc(*tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
+            CUDA_TRY(launch_shrink_tc(tmX, p->tmA, p->tmAw, Xb, T, pd, tabs, p->Vhl, p->ldh, p->num_sms,
                                       p->d_err, stream, trace_slot(tr, 1)));
         }
         if (!mark(1)) return LORA_ERR_CUDA;
-        CUDA_TRY(launch_gemm_prefill(*tmX, *tmW, *tmV, pair ? &p->tmB : nullptr, tmY, T, with_lora ? ids : nullptr,
+        CUDA_TRY(launch_gemm_prefill(tmX, tmW, tmV, pair ? &p->tmB : nullptr, pair ? &tmY : nullptr, T,
+                                     with_lora ? ids : nullptr,
                                      with_lora ? p->tile_info : nullptr, pd, p->Vhl, p->ldh, Yb,
                                      p->num_sms, p->d_err, stream, trace_slot(tr, 2)));
         if (!mark(2)) return LORA_ERR_CUDA;

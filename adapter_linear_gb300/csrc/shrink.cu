@@ -235,9 +235,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     } else if (warp == 5) {
         // ----------------------------------------------------------------- MMA
         if (lane == 0) {
+            // uc counts the units this CTA runs (not the skipped ones): it picks the
+            // accumulator buffer and the phase of its barriers
             int it = 0, uc = 0;
             bool ok = true;
-            for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++uc) {
+            for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
                 const UnitInfo ui = unit_info(u, pool, tabs, T, err);
                 if (ui.small) continue;
                 const int buf = uc & 1;
@@ -263,6 +265,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                     mma_commit(&empty[s]);
                 }
                 if (ok) mma_commit(&acc_full[buf]);
+                ++uc;
             }
             mma_commit(drain);
             int dummy = 0;
@@ -271,8 +274,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------------ epilogue
-        int uc = 0;
-        for (int u = blockIdx.x; u < units; u += gridDim.x, ++uc) {
+        int uc = 0;  // units run, as in the MMA role
+        for (int u = blockIdx.x; u < units; u += gridDim.x) {
             const UnitInfo ui = unit_info(u, pool, tabs, T, err);
             if (ui.small) continue;
             const int buf = uc & 1;
@@ -323,6 +326,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[buf]);
+            ++uc;
         }
     }
 
