@@ -38,6 +38,7 @@ constexpr int HDR_UNITS = 2;    // sum over segments of ceil(len / kShrinkRows)
 constexpr int kShrinkRows = 128;       // token rows per tensor-core shrink unit
 constexpr int kShrinkSmallSeg = 16;    // segments of at most this many tokens: warp-level shrink
 constexpr int kDecodeMaxT = 256;       // largest batch of the decode path
+constexpr int kAutoDecodeMaxT = 512;   // AUTO runs larger batches up to this in decode slices
 
 // Device error word bits.
 constexpr int kErrBadIdBit = 1;

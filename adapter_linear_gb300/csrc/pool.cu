@@ -448,8 +448,22 @@ lora_status run_linear(lora_pool *p, const void *X, const void *W, const int32_t
 {
     if (!p || !X || !W || !Y || (with_lora && !ids) || T < 0) return LORA_ERR_ARG;
     int path = p->path;
-    if (path == LORA_PATH_AUTO) path = T <= kDecodeMaxT ? LORA_PATH_DECODE : LORA_PATH_PREFILL;
     if (path == LORA_PATH_DECODE && T > kDecodeMaxT) return LORA_ERR_ARG;
+    if (path == LORA_PATH_AUTO && T > kDecodeMaxT && T <= kAutoDecodeMaxT) {
+        // decode kernels over slices of kDecodeMaxT tokens: W streams once per slice, but
+        // the adapters' A and B pages are read per token, never staged per segment (at
+        // T = 512: 64 vs 167 us on tokens spread over 2000 adapters, 57 vs 75 us on
+        // 8 contiguous adapters, against the prefill kernels)
+        for (int t0 = 0; t0 < T; t0 += kDecodeMaxT) {
+            const int n = T - t0 < kDecodeMaxT ? T - t0 : kDecodeMaxT;
+            lora_status st = run_linear(p, static_cast<const uint16_t *>(X) + (size_t)t0 * p->d_in, W,
+                                        with_lora ? ids + t0 : nullptr, n,
+                                        static_cast<uint16_t *>(Y) + (size_t)t0 * p->d_out, stream, with_lora);
+            if (st != LORA_OK) return st;
+        }
+        return LORA_OK;
+    }
+    if (path == LORA_PATH_AUTO) path = T <= kDecodeMaxT ? LORA_PATH_DECODE : LORA_PATH_PREFILL;
     if (T == 0) return LORA_OK;
     lora_status st = ensure_scratch(p, T);
     if (st != LORA_OK) return st;

@@ -92,6 +92,11 @@ def workload(name: str):
                    "T": 16384, "d_in": 4096, "d_out": 14336, "adapters": 8,
                    "rank": "64 (padded from 8,8,16,16,32,32,64,64)" if padded else "8,8,16,16,32,32,64,64",
                    "alpha": "2*rank"}
+    if name == "prefill_zipf":
+        p = L.prefill_zipf()
+        return p, {"workload": "q_proj-shaped prefill, 4096 tokens spread over 2000 adapters", "T": 4096,
+                   "d_in": 4096, "d_out": 4096, "adapters": 2000, "rank": 16, "alpha": 32,
+                   "ids": "Zipf(s=1) over 2000"}
     if name == "prefill_r16":  # the same prefill with every adapter at rank 16 (alpha 32)
         p = L.prefill_mixed(ranks=[16])
         return p, {"workload": "gate_proj prefill, 8x2048 tokens, rank 16", "T": 16384,
@@ -1068,6 +1073,7 @@ def run_cpu_probe(args):
 
 
 CONFIG_ORDER = ("tiny", "llama3_layer", "q_proj_decode_q4", "prefill_mixed", "prefill_mixed_padded", "prefill_r16",
+                "prefill_zipf",
                 "hotswap_T256", "hotswap_stream")
 
 

@@ -85,8 +85,10 @@ typedef enum {
 #define LORA_RANK_PAGE 8          /* rank rows per pool page                   */
 #define LORA_MAX_GROUP 8          /* layers of one lora_linear_grouped call    */
 
-/* Which kernel family lora_linear uses. AUTO picks DECODE for T <= 256 and
- * PREFILL above; DECODE accepts T <= 256 only. Both compute the same result. */
+/* Which kernel family lora_linear uses. AUTO picks DECODE for T <= 256, the DECODE
+ * kernels over consecutive slices of 256 tokens for 256 < T <= 512, and PREFILL
+ * above; a forced DECODE accepts T <= 256 only. All compute the same result (up to
+ * the order of the fp32 sums). */
 typedef enum { LORA_PATH_AUTO = 0, LORA_PATH_DECODE = 1, LORA_PATH_PREFILL = 2 } lora_path;
 
 /* Which prefill GEMM kernel the PREFILL path uses. AUTO picks PAIR for T > 128:

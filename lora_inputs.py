@@ -209,6 +209,17 @@ def prefill_mixed(seed: int = 3, seq_len: int = 2048, n_seq: int = 8, d_in: int 
                    ads, max_adapters=n_seq, max_rank=max(64 if padded else 0, max(ranks)), seed=seed)
 
 
+def prefill_zipf(seed: int = 5, T: int = 4096, n_adapters: int = 2000, rank: int = 16,
+                 d: int = 4096) -> Problem:
+    """A prefill-sized batch whose tokens are spread over a large pool: ids Zipf(s=1)
+    over n_adapters (a few adapters hold many tokens, most hold one or two)."""
+    X = normal_bf16(seed, ROLE_X, 0, (T, d), 1.0)
+    W = normal_bf16(seed, ROLE_W, 0, (d, d), 1.0 / 64)
+    ids = zipf_ids(seed, T, n_adapters, 1.0)
+    ads = {i: make_adapter(seed, i, d, d, rank, 2.0 * rank) for i in range(n_adapters)}
+    return Problem("prefill_zipf", d, d, X, W, ids, ads, max_adapters=n_adapters, max_rank=rank, seed=seed)
+
+
 @dataclasses.dataclass
 class HotswapSchedule:
     calls: int

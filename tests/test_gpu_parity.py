@@ -135,6 +135,26 @@ def test_hotswap_stream():
     assert pool.stats()["loads"] == 2000 + len(sched.swaps)
 
 
+@pytest.mark.parametrize("T", [300, 512])
+def test_auto_decode_slices(T):
+    """AUTO runs 257..512 tokens as decode calls over 256-token slices (the last one
+    ragged at T = 300): the oracle's result, and the prefill kernels' within tolerance."""
+    d, n, seed = 512, 40, 93
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d, d), 1.0 / 32)
+    ids = L.zipf_ids(seed, T, n, 1.0)
+    ids[L.rng_for(seed, L.ROLE_IDS, 6).random(T) < 0.1] = -1
+    ads = {i: L.make_adapter(seed, i, d, d, 16, 32.0) for i in range(n)}
+    prob = L.Problem("auto_slices", d, d, X, W, ids, ads, n, 16, seed)
+    pool = load_pool(al, prob)
+    got = run(pool, prob, al.LORA_PATH_AUTO)
+    ref, base = ref_of(prob)
+    assert_parity(got, ref, f"auto T={T}")
+    assert_routing(got, ref, base, prob.ids, f"auto T={T}")
+    assert_parity(got, run(pool, prob, PATHS["prefill"]), f"auto vs prefill T={T}")
+    pool.close()
+
+
 @pytest.mark.parametrize("kernel", ["single", "pair"])
 def test_scattered_prefill(kernel):
     """A prefill-sized batch spread over many adapters of mixed ranks (1, 2, 3 and 5
