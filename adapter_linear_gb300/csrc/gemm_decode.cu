@@ -694,7 +694,11 @@ __global__ void dequant_q4_kernel(const uint8_t *__restrict__ Wq, const uint16_t
 constexpr int kFinishThreads = 128;  // each thread: 8 consecutive columns of one token
 constexpr int kFinishCols = 8;
 constexpr int kFinishBlockCols = kFinishThreads * kFinishCols;
-constexpr int kPrefetchPages = 2;     // B pages loaded into registers before the GEMM ends
+// B pages a finishing thread loads into registers before the GEMM ends (PF): two while
+// the finishing grid fits two CTAs per SM beside the GEMM (every CTA is resident and
+// loads them early), else one -- fewer registers, four CTAs per SM instead of three
+// (measured: T = 256 hot-swap pool 31.7 -> 31.3 us, the grouped 7-module layer 91.1 ->
+// 89.3; q_proj T = 64 with one page: 13.5 -> 14.1)
 // partial loads in flight per thread, fewer beside the LoRA variant's B words: five
 // for one layer (a q_proj tile has ~5.75 contributors; measured 1-3 % faster than four
 // on the single-layer workloads), four for a grouped call (five spill there: +1 %)
@@ -720,32 +724,33 @@ __device__ __forceinline__ int finish_adapter(const PoolDev &pool, int id, const
     return row[SLOT_NPAGES];
 }
 
-// The B words of columns n0..n0+7 of the first kPrefetchPages pages into registers,
-// the later pages' line into L2.
+// The B words of columns n0..n0+7 of the first PF pages into registers, the later
+// pages' line into L2.
+template <int PF>
 __device__ __forceinline__ void finish_b_words(const PoolDev &pool, const int32_t *pages, int np,
-                                               int n0, uint4 (&b)[kPrefetchPages][8], int *err)
+                                               int n0, uint4 (&b)[PF][8], int *err)
 {
 #pragma unroll
-    for (int q = 0; q < kPrefetchPages; ++q)
+    for (int q = 0; q < PF; ++q)
         if (q < np) {
             const int page = LORA_CHECKED(pages[q], 0, pool.num_pages, err, 0);
             const uint16_t *src = pool.B_pages + ((size_t)page * pool.d_out + n0) * kRankPage;
 #pragma unroll
             for (int c = 0; c < 8; ++c) b[q][c] = ldg_nc_v4(src + c * kRankPage);
         }
-    for (int q = kPrefetchPages; q < np; ++q)
+    for (int q = PF; q < np; ++q)
         prefetch_l2(pool.B_pages +
                     ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, err, 0) * pool.d_out + n0) *
                         kRankPage);
 }
 
 // The sums of one thread's 8 columns of token t (see finish_decode_body).
-template <int NP, bool LORA>
+template <int NP, bool LORA, int PF>
 __device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const DecodeProblem &pr,
                                                const float *__restrict__ partials, int t, int n0,
                                                int c_lo, int c_hi, int seg_lo, int np,
                                                const int32_t *pages, bool early,
-                                               const uint4 (&b)[kPrefetchPages][8])
+                                               const uint4 (&b)[PF][8])
 {
     const PoolDev &pool = pr.pool;
     const int nl = n0 & 127;
@@ -755,10 +760,10 @@ __device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const D
     // sums and the expand follow in the same order as before (partials in CTA order,
     // then the pages), so the loads of V no longer wait for the partial sums.
     const float *vrow = pr.V + (size_t)t * pr.ldv;
-    const int q_early = (LORA && early) ? (np < kPrefetchPages ? np : kPrefetchPages) : 0;
-    float4 vq[kPrefetchPages][2];
+    const int q_early = (LORA && early) ? (np < PF ? np : PF) : 0;
+    float4 vq[PF][2];
 #pragma unroll
-    for (int q = 0; q < kPrefetchPages; ++q)
+    for (int q = 0; q < PF; ++q)
         if (q < q_early) {
             vq[q][0] = *reinterpret_cast<const float4 *>(vrow + q * kRankPage);
             vq[q][1] = *reinterpret_cast<const float4 *>(vrow + q * kRankPage + 4);
@@ -792,7 +797,7 @@ __device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const D
             }
     }
 #pragma unroll
-    for (int q = 0; q < kPrefetchPages; ++q)
+    for (int q = 0; q < PF; ++q)
         if (q < q_early) {
             const float v[8] = {vq[q][0].x, vq[q][0].y, vq[q][0].z, vq[q][0].w,
                                 vq[q][1].x, vq[q][1].y, vq[q][1].z, vq[q][1].w};
@@ -822,7 +827,7 @@ __device__ __forceinline__ void finish_columns(const DecodePlanT<NP> &p, const D
 }
 
 // LORA = false: the base-only pass (no adapter state, few registers).
-template <int NP, bool LORA>
+template <int NP, bool LORA, int PF>
 __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
                                                    const float *__restrict__ partials,
                                                    const int32_t *__restrict__ ids)
@@ -849,11 +854,11 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
     // words are reloaded if it changed.
     int id = -1, np = 0;
     const int32_t *pages = nullptr;
-    uint4 b[kPrefetchPages][8];
+    uint4 b[PF][8];
     if (LORA && pool.slots != nullptr) {
         id = ids[t];
         np = finish_adapter(pool, id, pages);
-        if (col_ok) finish_b_words(pool, pages, np, n0, b, pr.err);
+        if (col_ok) finish_b_words<PF>(pool, pages, np, n0, b, pr.err);
     }
     // contributors of this tile: CTAs c_lo..c_hi (contiguous unit ranges). Only c_lo
     // can have started before the tile; its partial for the tile is its segment
@@ -891,7 +896,7 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
         if (np == 0 && id != -1 && threadIdx.x == 0 && (int)blockIdx.x == pr.col_blk_begin)
             atomicOr(pr.err, kErrBadIdBit);  // strict: never a silent base fall-back
     }
-    if (col_ok) finish_columns<NP, LORA>(p, pr, partials, t, n0, c_lo, c_hi, seg_lo, np, pages, early, b);
+    if (col_ok) finish_columns<NP, LORA, PF>(p, pr, partials, t, n0, c_lo, c_hi, seg_lo, np, pages, early, b);
     if (trace) {
         __syncthreads();
         trace_exit(trace);
@@ -932,20 +937,20 @@ __global__ void __maxnreg__(96)
     gemm_decode_body<NP>(maps, p, ids, partials, err);
 }
 
-template <int NP, bool LORA>
+template <int NP, bool LORA, int PF>
 __global__ void __launch_bounds__(kFinishThreads, 3)
     finish_decode_kernel(const __grid_constant__ DecodePlanT<NP> p, const float *__restrict__ partials,
                          const int32_t *__restrict__ ids)
 {
-    finish_decode_body<NP, LORA>(p, partials, ids);
+    finish_decode_body<NP, LORA, PF>(p, partials, ids);
 }
 
-template <int NP>
+template <int NP, int PF>
 __global__ void __maxnreg__(152)
     finish_decode_kernel_tight(const __grid_constant__ DecodePlanT<NP> p,
                                const float *__restrict__ partials, const int32_t *__restrict__ ids)
 {
-    finish_decode_body<NP, true>(p, partials, ids);
+    finish_decode_body<NP, true, PF>(p, partials, ids);
 }
 
 uint32_t pow2_cols(uint32_t n)
@@ -1010,6 +1015,7 @@ bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max
     if (pairs > p.grid) p.grid = (int)(pairs < max_G ? pairs : max_G);
     p.pairs = (int)pairs;
     p.col_blocks = (int)cols;
+    p.fin_two_pages = cols * T <= 2ll * max_G;
     // bounded registers where the finishing grid exceeds the SMs and each CTA's
     // shrink work (A bytes of its pairs) stays well under its share of the W stream
     int max_d_in = 0;
@@ -1077,9 +1083,9 @@ template <int NP>
 cudaError_t launch_finish_decode_n(const DecodePlan &plan, const float *partials, const int32_t *ids,
                                    cudaStream_t stream)
 {
-    auto kernel = ids == nullptr ? finish_decode_kernel<NP, false>
-                                 : (plan.tight ? finish_decode_kernel_tight<NP>
-                                               : finish_decode_kernel<NP, true>);
+    auto kernel = ids == nullptr   ? finish_decode_kernel<NP, false, 1>
+                  : plan.fin_two_pages ? (plan.tight ? finish_decode_kernel_tight<NP, 2> : finish_decode_kernel<NP, true, 2>)
+                                       : (plan.tight ? finish_decode_kernel_tight<NP, 1> : finish_decode_kernel<NP, true, 1>);
     cudaError_t e = ensure_smem_attr((const void *)kernel, 0);
     if (e != cudaSuccess) return e;
     return launch_pdl(kernel, dim3(plan.col_blocks, plan.T), dim3(kFinishThreads), 0, stream,

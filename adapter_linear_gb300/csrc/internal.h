@@ -132,6 +132,7 @@ struct DecodePlanHead {
     int stages;
     int pairs;              // shrink pairs of all problems
     int col_blocks;         // finishing grid.x
+    bool fin_two_pages;     // the finishing pass holds two B pages (else one) in registers
     bool tight;             // register-bounded kernel variants (see gemm_decode.cu)
     bool prefetch_a;        // A pages of the shrink pairs into L2 before the wait
     uint64_t *trace;        // measurement hook: LORA_KERNEL_SLOTS x 4 words (see trace_enter), or nullptr
