@@ -135,6 +135,28 @@ def test_hotswap_stream():
     assert pool.stats()["loads"] == 2000 + len(sched.swaps)
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_short_requests_prefill(kernel):
+    """Requests of 40 contiguous tokens, each with its own adapter (mixed ranks, one
+    request without): every GEMM tile mixes adapters, most epilogue warps' 32 rows share
+    one (the shared-B expand), the others straddle two."""
+    d, n, ln, seed = 512, 12, 40, 95
+    T = n * ln
+    ranks = [8, 16, 24, 40]
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d, d), 1.0 / 32)
+    ids = np.repeat(np.arange(n, dtype=np.int32), ln)
+    ids[ids == 5] = -1
+    ads = {i: L.make_adapter(seed, i, d, d, ranks[i % 4], 2.0 * ranks[i % 4]) for i in range(n)}
+    prob = L.Problem("short_requests", d, d, X, W, ids, ads, n, 40, seed)
+    pool = load_pool(al, prob)
+    pool.set_prefill_kernel({"single": al.LORA_PREFILL_SINGLE, "pair": al.LORA_PREFILL_PAIR}[kernel])
+    got = run(pool, prob, PATHS["prefill"])
+    ref, base = ref_of(prob)
+    assert_parity(got, ref, f"short requests/{kernel}")
+    assert_routing(got, ref, base, prob.ids, f"short requests/{kernel}")
+
+
 @pytest.mark.parametrize("T", [300, 512])
 def test_auto_decode_slices(T):
     """AUTO runs 257..512 tokens as decode calls over 256-token slices (the last one
