@@ -109,7 +109,7 @@ namespace {
 
 size_t seg_entries(const lora_pool *p, int T) { return (size_t)std::min(T, p->max_adapters) + 1; }
 
-// The multi-CTA segment builder's count table: (key, chunk) counts, then one row of
+// The multi-CTA segment builder's count table: (chunk, key) counts, then one row of
 // first positions (pools of up to kSegMultiMaxKeys keys; else 0: not used).
 size_t seg_chist_ints(const lora_pool *p, int T)
 {

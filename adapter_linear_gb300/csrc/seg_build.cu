@@ -14,13 +14,15 @@
 //      32-token step equal keys are ranked by lane, so ties keep token order.
 // The result is unique (a stable sort), so it is compared bit for bit.
 //
-// For pools of up to kSegMultiMaxKeys keys the same tables come from two kernels
-// spread over the SMs (one CTA alone is bound by its own instruction issue):
+// For pools of up to kSegMultiKeys keys, and for batches of kSegMultiMinT tokens and
+// more, the same tables come from two kernels spread over the SMs (one CTA alone is
+// bound by its own instruction issue):
 //   1. seg_count_kernel, one CTA per kSegChunk tokens: keys, the chunk's per-key
 //      counts, the per-tile adapter table and the zeroed shrink rows; the last CTA
-//      to finish (an atomic ticket, nothing waits) turns the counts into each
-//      (key, chunk)'s first position by a scan over chunks and then over keys, and
-//      writes the segment tables;
+//      to finish (an atomic ticket, nothing waits) turns the counts (chunk-major)
+//      into each (key, chunk)'s first position by a scan over chunks -- a warp per
+//      key when there are few keys, a thread per key otherwise -- and then over keys,
+//      and writes the segment tables;
 //   2. seg_scatter_kernel, one CTA per chunk: its warps place their tokens in turn,
 //      ties ranked by lane, so the order is stable across and within chunks.
 #include "device_common.cuh"
@@ -369,7 +371,7 @@ __global__ void __launch_bounds__(kSegChunk)
             tabs.tile_info[tile] = h < 0 ? kTileNoAdapter : (l == h ? h : kTileMixed);
         }
     }
-    for (int k = tid; k < K; k += kSegChunk) tabs.chist[(size_t)k * chunks + blockIdx.x] = hist[k];
+    for (int k = tid; k < K; k += kSegChunk) tabs.chist[(size_t)blockIdx.x * K + k] = hist[k];
 
     // the last chunk to finish turns the counts into positions
     __threadfence();
@@ -381,24 +383,42 @@ __global__ void __launch_bounds__(kSegChunk)
         return;
     }
     __threadfence();
-    // per key: exclusive scan over the chunks (a warp per key, 32 chunks per step),
-    // the key's total into hist[]
-    for (int k = warp; k < K; k += kWarps) {
-        int32_t *row = tabs.chist + (size_t)k * chunks;
-        int carry = 0;
-        for (int c0 = 0; c0 < chunks; c0 += 32) {
-            const int c = c0 + lane;
-            const int v = c < chunks ? __ldcg(row + c) : 0;
-            int inc = v;
+    // per key: exclusive scan over the chunks, the key's total into hist[]. Few keys
+    // (a prefill of a few long sequences): a warp per key, 32 chunks per step; many
+    // keys: a thread per key, its 16 chunks' loads issued together (the counts are
+    // chunk-major, so they are coalesced across the CTA)
+    if (K <= 2 * kWarps) {
+        for (int k = warp; k < K; k += kWarps) {
+            int carry = 0;
+            for (int c0 = 0; c0 < chunks; c0 += 32) {
+                const int c = c0 + lane;
+                const int v = c < chunks ? __ldcg(tabs.chist + (size_t)c * K + k) : 0;
+                int inc = v;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int n = __shfl_up_sync(0xffffffffu, inc, o);
-                if (lane >= o) inc += n;
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += n;
+                }
+                if (c < chunks) tabs.chist[(size_t)c * K + k] = carry + inc - v;
+                carry += __shfl_sync(0xffffffffu, inc, 31);
             }
-            if (c < chunks) row[c] = carry + inc - v;
-            carry += __shfl_sync(0xffffffffu, inc, 31);
+            if (lane == 0) hist[k] = carry;
         }
-        if (lane == 0) hist[k] = carry;
+    } else for (int k = tid; k < K; k += kSegChunk) {
+        int carry = 0;
+        for (int c0 = 0; c0 < chunks; c0 += 16) {
+            int v[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                v[i] = c0 + i < chunks ? __ldcg(tabs.chist + (size_t)(c0 + i) * K + k) : 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (c0 + i < chunks) {
+                    tabs.chist[(size_t)(c0 + i) * K + k] = carry;
+                    carry += v[i];
+                }
+        }
+        hist[k] = carry;
     }
     __syncthreads();
     scan_keys(hist, K, T, tabs, tabs.chist + (size_t)K * chunks);
@@ -416,7 +436,7 @@ __global__ void __launch_bounds__(kSegChunk)
     const int chunks = (int)gridDim.x;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t *first = tabs.chist + (size_t)K * chunks;
-    for (int k = tid; k < K; k += kSegChunk) run[k] = first[k] + tabs.chist[(size_t)k * chunks + blockIdx.x];
+    for (int k = tid; k < K; k += kSegChunk) run[k] = first[k] + tabs.chist[(size_t)blockIdx.x * K + k];
     const int t = (int)blockIdx.x * kSegChunk + tid;
     const int key = t < T ? tabs.keys[t] : 0;
     __syncthreads();
@@ -471,7 +491,7 @@ cudaError_t launch_seg_build(const int32_t *ids, int T, const PoolDev &pool, Seg
                              int *err, uint16_t *vhl, int ldh, cudaStream_t stream, uint64_t *trace)
 {
     const int K = pool.max_adapters + 1;
-    if (tabs.chist != nullptr && K <= kSegMultiMaxKeys) {
+    if (tabs.chist != nullptr && K <= kSegMultiMaxKeys && (K <= kSegMultiKeys || T >= kSegMultiMinT)) {
         const int chunks = (T + kSegChunk - 1) / kSegChunk;
         const size_t smem = (size_t)K * sizeof(int);
         cudaError_t e = ensure_smem_attr((const void *)seg_count_kernel, smem);
