@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // with a TMA store. The fused expand works as in the
 // single-CTA kernel when every adapter token of the 256 uses one adapter: V rows of
 // each half and each half's 128 columns of the adapter's B pages (one 2 KB TMA box
-// per page: the B arena read as [pages x d_out] rows of 8 rank values).
+// per page: the B arena read as rows of 64 values, 16 rows a box).
 
 // The pair kernel's epilogue for one warp: as epilogue_rows, but each 64-column chunk
 // goes, as bf16, into a 128-byte-swizzled 32-row x 64-column staging tile in shared
@@ -610,8 +610,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int page = q < tl.npages
                                                      ? LORA_CHECKED(tl.pages[q], 0, pool.num_pages, a.err, 0)
                                                      : 0;  // page 0 is zeros
+                                // columns n0.. of the page: 128 x 16 B from row (page d_out + n0) / 8
+                                // of the 128-byte-row view (n0 and d_out are multiples of 8)
                                 tma_load_2d_pair(bs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
-                                                 page * a.d_out + n0);
+                                                 (int)(((long long)page * a.d_out + n0) >> 3));
                             }
                         }
                     }

@@ -624,11 +624,12 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
         lora_pool_destroy(p);
         return LORA_ERR_CUDA;
     }
-    // the CTA-pair prefill kernel reads B page slices with one TMA box each; its row
-    // coordinate (page * d_out + column) is a 32-bit int
-    const uint64_t b_rows = (uint64_t)p->num_pages * d_out;
-    p->pair_ok = b_rows + 256 < (1ull << 31) &&
-                 make_tmap_bf16_2d(&p->tmB, p->B_pages, kRankPage, b_rows, kRankPage * 2, kRankPage, 128, false);
+    // the CTA-pair prefill kernel reads the slice of a B page for its 128 columns (2 KB,
+    // contiguous) with one TMA box: the arena viewed as rows of 64 values (8 columns of
+    // 8 rank values), box 16 rows; the row coordinate is a 32-bit int
+    const uint64_t b_rows = (uint64_t)p->num_pages * d_out / 8;
+    p->pair_ok = b_rows + 32 < (1ull << 31) &&
+                 make_tmap_bf16_2d(&p->tmB, p->B_pages, 64, b_rows, 128, 64, 16, false);
     *out = p;
     return LORA_OK;
 }

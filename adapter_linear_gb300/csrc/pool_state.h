@@ -68,7 +68,7 @@ struct lora_pool {
     cudaStream_t waited_stream = nullptr;
     CUtensorMap tmA;   // A arena [num_pages*8 rows x d_in], box 8 x 64
     CUtensorMap tmAw;  // the same, box round16(8 * max_pages) x 64
-    CUtensorMap tmB;   // B arena as [num_pages*d_out rows x 8], box 128 x 8, no swizzle
+    CUtensorMap tmB;   // B arena as [num_pages*d_out/8 rows x 64], box 16 x 64, no swizzle
     bool pair_ok = false;  // tmB exists (rows < 2^31): the CTA-pair prefill kernel can run
 
     // per-call scratch, sized for cap_T tokens
