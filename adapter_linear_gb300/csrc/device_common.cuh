@@ -150,6 +150,13 @@ __device__ __forceinline__ void prefetch_l2(const void *p)
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Bulk prefetch of `bytes` bytes at p into L2 (both multiples of 16): one request,
+// carried out by the copy engine, not by the issuing thread's load slots.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint4 ldg_nc_v4(const void *p)
 {
     uint4 r;

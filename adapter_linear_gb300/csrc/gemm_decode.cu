@@ -188,13 +188,13 @@ __device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const 
     tc_fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     // Before the wait on the previous kernel: the A pages of this CTA's shrink pairs
-    // into L2 (line prefetches, so the TMA engine keeps serving the W ring), where
-    // the plan says it pays. The ids read here may still be written by an earlier
-    // kernel in the stream, so they only steer these requests; the pairs below
-    // read the ids again after the wait.
+    // into L2, one bulk prefetch per page (a thread per pair), so the per-lane loads
+    // of the shrink below hit L2. The ids read here may still be written by an
+    // earlier kernel in the stream, so they only steer these requests; the pairs
+    // below read the ids again after the wait.
     if (ids != nullptr && p.prefetch_a) {
         int m = 0;
-        for (int u = c; u < p.pairs; u += (int)gridDim.x) {
+        for (int u = c + (int)threadIdx.x * (int)gridDim.x; u < p.pairs; u += 128 * (int)gridDim.x) {
             while (NP > 1 && m + 1 < p.n && p.prob[pick<NP>(m + 1)].pair_begin <= u) ++m;
             const DecodeProblem &pr = p.prob[pick<NP>(m)];
             const int lp = u - pr.pair_begin;
@@ -205,10 +205,8 @@ __device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const 
             if (q >= row[SLOT_NPAGES]) continue;
             const int page = row[SLOT_PAGES + q];
             if (page < 0 || page >= pr.pool.num_pages) continue;
-            const uint8_t *Ap = reinterpret_cast<const uint8_t *>(pr.pool.A_pages) +
-                                (size_t)page * kRankPage * pr.pool.d_in * 2;
-            for (int i = threadIdx.x; i < kRankPage * pr.pool.d_in * 2 / 128; i += 128)
-                prefetch_l2(Ap + (size_t)i * 128);
+            prefetch_l2_bulk(pr.pool.A_pages + (size_t)page * kRankPage * pr.pool.d_in,
+                             (uint32_t)(kRankPage * pr.pool.d_in * 2));
         }
     }
     pdl_wait_prior();  // X, ids, V and the partials belong to the stream's order
@@ -1023,11 +1021,12 @@ bool plan_decode(int n, int T, const int *d_in, const int *d_out, const int *max
     const double shrink_bytes = (double)((pairs + p.grid - 1) / p.grid) * 2.0 * kRankPage * max_d_in;
     const double stream_bytes = (double)U / (double)G * kBoxes * kWTileBytes;
     p.tight = pairs > 0 && cols * T > max_G && 2.0 * shrink_bytes <= stream_bytes;
-    // the A pages requested into L2 before the wait on the previous kernel: measured
-    // faster where a CTA has one pair (k_proj T = 32: 10.5 -> 10.0 us) or its pairs'
-    // A bytes are small beside its W bytes (the 7-module layer: 95 -> 92 us), slower
-    // where they are as large as its W share (T = 256, ~3.4 pairs per CTA: 34 -> 37)
-    p.prefetch_a = pairs > 0 && (pairs <= p.grid || 4.0 * shrink_bytes <= stream_bytes);
+    // the A pages requested into L2 before the wait on the previous kernel, one bulk
+    // prefetch per page: faster for every plan measured (T = 256 over 2000 adapters,
+    // ~3.4 pairs per CTA: 31.3 -> 28.7 us a step; q_proj T = 64: 13.49 -> 13.35; the
+    // 7-module layer 89.3 -> 89.0). Line prefetches by the epilogue warps had paid only
+    // where a CTA's pairs were few (T = 256: 34 -> 37 us with them)
+    p.prefetch_a = pairs > 0;
     int max_seg = 1;
     for (int c = 0; c < p.G; ++c) {
         const int u0 = cta_start(c, p.U, p.G), u1 = cta_start(c + 1, p.U, p.G);
