@@ -65,10 +65,8 @@ def check(T, d_in, d_out, pages, sms=152):
     if pairs > info["G"]:
         assert info["grid"] == min(pairs, sms)
     assert info["partials_floats"] == info["G"] * max_seg * T * 128
-    # A-page prefetch: one pair per CTA, or the pairs' A bytes a quarter of the W share
-    shrink = -(-pairs // info["grid"]) * 16 * max(d_in) if pairs else 0
-    stream = U / info["G"] * 2 * 128 * 128
-    assert info["prefetch_a"] == int(pairs > 0 and (pairs <= info["grid"] or 4 * shrink <= stream))
+    # A-page prefetch (one bulk request per page) whenever there are shrink pairs
+    assert info["prefetch_a"] == int(pairs > 0)
     assert U * info["G"] < 2 ** 31
     return info
 
