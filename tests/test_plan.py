@@ -79,7 +79,7 @@ def test_plan_of_the_benchmarked_shapes():
     assert layer["units"] == 13312 and layer["col_blocks"] == 42
     hs = check(256, [4096], [4096], [2])
     assert hs["tight"] == 0 and hs["n_acc"] == 2       # 256 columns per accumulator
-    assert (q["prefetch_a"], layer["prefetch_a"], hs["prefetch_a"]) == (1, 1, 0)
+    assert (q["prefetch_a"], layer["prefetch_a"], hs["prefetch_a"]) == (1, 1, 1)
     tiny = check(64, [256], [256], [1])
     assert tiny["G"] == 4 and tiny["grid"] == 64       # extra CTAs run shrink pairs only
     base = check(64, [4096], [4096], [0])
