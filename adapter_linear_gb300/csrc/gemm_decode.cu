@@ -84,6 +84,9 @@ __host__ __device__ __forceinline__ int unit_tile(const Plan &p, int u)
 }
 
 // One (token, page) pair of the shrink, computed by the 128 threads of warps 0-3.
+// UNR: chunks of d_in whose loads one thread has in flight at a time (the shrink is
+// bound by the loads in flight per SM; the register-bounded kernel variant keeps 2).
+template <int UNR>
 __device__ __forceinline__ void shrink_pair(int t, int page, float scale, const DecodeProblem &pr,
                                             int q, float (*red)[8])
 {
@@ -95,7 +98,7 @@ __device__ __forceinline__ void shrink_pair(int t, int page, float scale, const 
     float acc[kRankPage];
 #pragma unroll
     for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = 0.f;
-#pragma unroll 2
+#pragma unroll UNR
     for (int c = tid; c < d_in / 8; c += 128) {
         const uint4 x = ldg_nc_v4(xr + c * 8);
         uint4 a[kRankPage];
@@ -121,6 +124,7 @@ __device__ __forceinline__ void shrink_pair(int t, int page, float scale, const 
 
 // The same pair computed by one warp alone (lanes stride over d_in): when a CTA has
 // several pairs, its four epilogue warps each take one and run them in parallel.
+template <int UNR>
 __device__ __forceinline__ void shrink_pair_warp(int t, int page, float scale, const DecodeProblem &pr,
                                                  int q)
 {
@@ -131,7 +135,7 @@ __device__ __forceinline__ void shrink_pair_warp(int t, int page, float scale, c
     float acc[kRankPage];
 #pragma unroll
     for (int jj = 0; jj < kRankPage; ++jj) acc[jj] = 0.f;
-#pragma unroll 2
+#pragma unroll UNR
     for (int c = lane; c < d_in / 8; c += 32) {
         const uint4 x = ldg_nc_v4(xr + c * 8);
         uint4 a[kRankPage];
@@ -175,7 +179,7 @@ struct UnitCursor {
 // over `threads` threads, the shrink pairs dealt to this CTA (after the wait on the
 // previous kernel), then each of its segments' accumulators read out of TMEM into the
 // split-K partial sums.
-template <int NP>
+template <int NP, int UNR = 2>
 __device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const int32_t *__restrict__ ids,
                                                 float *__restrict__ partials, int *err, int c, int nseg,
                                                 uint64_t *acc_full, uint64_t *acc_empty,
@@ -229,9 +233,9 @@ __device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const 
             const float scale = __int_as_float(row[slot_page_scale(pr.pool.max_pages, q)]);
             const int page = LORA_CHECKED(row[SLOT_PAGES + q], 0, pr.pool.num_pages, pr.err, 0);
             if (by_warp)
-                shrink_pair_warp(t, page, scale, pr, q);
+                shrink_pair_warp<UNR>(t, page, scale, pr, q);
             else
-                shrink_pair(t, page, scale, pr, q, red);
+                shrink_pair<UNR>(t, page, scale, pr, q, red);
         }
     }
     for (int seg = 0; seg < nseg; ++seg) {
@@ -258,7 +262,7 @@ __device__ __forceinline__ void decode_epilogue(const DecodePlanT<NP> &p, const 
     }
 }
 
-template <int NP>
+template <int NP, int UNR = 2>
 __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, const DecodePlanT<NP> &p,
                                                  const int32_t *__restrict__ ids,
                                                  float *__restrict__ partials, int *err)
@@ -415,7 +419,7 @@ __device__ __forceinline__ void gemm_decode_body(const DecodeMapsT<NP> &maps, co
         __syncwarp();
     } else {
         // ------------------------------------- warps 0-3: shrink, then epilogue
-        decode_epilogue<NP>(p, ids, partials, err, c, nseg, acc_full, acc_empty, &abort_flag, red, tmem_slot,
+        decode_epilogue<NP, UNR>(p, ids, partials, err, c, nseg, acc_full, acc_empty, &abort_flag, red, tmem_slot,
                             kThreads);
     }
 
@@ -916,14 +920,18 @@ __device__ __forceinline__ void finish_decode_body(const DecodePlanT<NP> &p,
 // T = 32 and the grouped 7-module layer; slower for T = 32 layers whose finishing
 // grid fits the SMs and for T = 256 with ~4 shrink pairs per CTA). The unbounded
 // finishing pass is still held to three CTAs per SM (168 registers): at 180 its
-// residency fell to two and T = 256 took 38 instead of 34.6 us a step.
+// residency fell to two and T = 256 took 38 instead of 34.6 us a step. The unbounded
+// GEMM keeps four chunks of shrink loads in flight per thread (146 registers, two
+// unbounded finishing CTAs still fit beside it): T = 256 over 2000 adapters, where
+// the shrink of ~3.4 pairs per CTA outlasts the MMAs, 28.6 -> 27.7 us a step (three
+// chunks: 28.5); the tight variant keeps two.
 template <int NP>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_decode_kernel(const __grid_constant__ DecodeMapsT<NP> maps,
                        const __grid_constant__ DecodePlanT<NP> p, const int32_t *__restrict__ ids,
                        float *__restrict__ partials, int *err)
 {
-    gemm_decode_body<NP>(maps, p, ids, partials, err);
+    gemm_decode_body<NP, 4>(maps, p, ids, partials, err);
 }
 
 template <int NP>
