@@ -148,6 +148,16 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tmem_buf, int quarter, in
             hrow = a.Vhl + (size_t)t * a.ldh;
         }
     }
+    // this row's B words for the warp's 128 columns, one bulk prefetch per page into L2,
+    // so that the expand's gathers below hit L2
+    if (np > 0 && n0 + half * 128 < a.d_out) {
+        const int c0 = n0 + half * 128;
+        const uint32_t bytes = (uint32_t)min(128, a.d_out - c0) * 16u;
+        for (int q = 0; q < np; ++q)
+            prefetch_l2_bulk(pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + c0) *
+                                                kRankPage,
+                             bytes);
+    }
     uint16_t *yrow = a.Y + (size_t)t * a.d_out;
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
@@ -396,6 +406,16 @@ __device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quar
             pages = row + SLOT_PAGES;
             hrow = a.Vhl + (size_t)t * a.ldh;
         }
+    }
+    // this row's B words for the warp's 128 columns, one bulk prefetch per page into L2,
+    // so that the expand's gathers below hit L2
+    if (np > 0 && n0 + half * 128 < a.d_out) {
+        const int c0 = n0 + half * 128;
+        const uint32_t bytes = (uint32_t)min(128, a.d_out - c0) * 16u;
+        for (int q = 0; q < np; ++q)
+            prefetch_l2_bulk(pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + c0) *
+                                                kRankPage,
+                             bytes);
     }
 #pragma unroll 1
     for (int ch = 0; ch < 2; ++ch) {
