@@ -126,6 +126,20 @@ __device__ __forceinline__ void expand_page_32(float (&acc)[32], const float (&v
     }
 }
 
+// The B words of one row's expand for the warp's 128 columns starting at c0 (2 KB
+// contiguous per page) into L2, one bulk prefetch per page, so that the gathers of the
+// expand hit L2.
+__device__ __forceinline__ void prefetch_row_b(const int32_t *pages, int np, int c0, const PrefillArgs &a,
+                                               const PoolDev &pool)
+{
+    if (np <= 0 || c0 >= a.d_out) return;
+    const uint32_t bytes = (uint32_t)min(128, a.d_out - c0) * 16u;
+    for (int q = 0; q < np; ++q) {
+        const int page = LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0);
+        prefetch_l2_bulk(pool.B_pages + ((size_t)page * a.d_out + c0) * kRankPage, bytes);
+    }
+}
+
 // One epilogue warp's share of a finished accumulator: TMEM lanes 32*quarter.. (token
 // rows t = row0 + lane), columns 128*half.. of the tile at column n0, in chunks of 32;
 // with `own_expand`, each row's adapter expand added on CUDA cores; rounded to bf16
@@ -148,16 +162,7 @@ __device__ __forceinline__ void epilogue_rows(uint32_t tmem_buf, int quarter, in
             hrow = a.Vhl + (size_t)t * a.ldh;
         }
     }
-    // this row's B words for the warp's 128 columns, one bulk prefetch per page into L2,
-    // so that the expand's gathers below hit L2
-    if (np > 0 && n0 + half * 128 < a.d_out) {
-        const int c0 = n0 + half * 128;
-        const uint32_t bytes = (uint32_t)min(128, a.d_out - c0) * 16u;
-        for (int q = 0; q < np; ++q)
-            prefetch_l2_bulk(pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + c0) *
-                                                kRankPage,
-                             bytes);
-    }
+    prefetch_row_b(pages, np, n0 + half * 128, a, pool);
     uint16_t *yrow = a.Y + (size_t)t * a.d_out;
 #pragma unroll 1
     for (int ch = 0; ch < 4; ++ch) {
@@ -407,16 +412,7 @@ __device__ __forceinline__ void epilogue_rows_staged(uint32_t tmem_buf, int quar
             hrow = a.Vhl + (size_t)t * a.ldh;
         }
     }
-    // this row's B words for the warp's 128 columns, one bulk prefetch per page into L2,
-    // so that the expand's gathers below hit L2
-    if (np > 0 && n0 + half * 128 < a.d_out) {
-        const int c0 = n0 + half * 128;
-        const uint32_t bytes = (uint32_t)min(128, a.d_out - c0) * 16u;
-        for (int q = 0; q < np; ++q)
-            prefetch_l2_bulk(pool.B_pages + ((size_t)LORA_CHECKED(pages[q], 0, pool.num_pages, a.err, 0) * a.d_out + c0) *
-                                                kRankPage,
-                             bytes);
-    }
+    prefetch_row_b(pages, np, n0 + half * 128, a, pool);
 #pragma unroll 1
     for (int ch = 0; ch < 2; ++ch) {
         if (lane == 0) bulk_wait_read_all();  // the previous chunk's store has read ybuf
