@@ -371,38 +371,63 @@ __global__ void __launch_bounds__(kSmallThreads)
     shrink_small_kernel(const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
                         uint16_t *__restrict__ Vhl, int ldh, int *err, int T, int max_seg)
 {
-    // the unit prefix and the segment starts in shared memory (most work items are empty
-    // chunks, decided from these alone)
+    // in shared memory: the segment starts and, as an exclusive prefix, the number of
+    // 16-position chunks of each segment this kernel takes (none for the segments left
+    // to the tensor-core shrink), so that the work items are exactly the chunks to do
     extern __shared__ int seg_smem[];
+    __shared__ int warp_sum[kSmallThreads / 32];
     const int num_seg = tabs.hdr[HDR_NUMSEG];
     const int nseg = min(num_seg, max_seg);
-    int *ublk = seg_smem, *start = ublk + (max_seg + 1);
-    for (int s = threadIdx.x; s <= nseg; s += blockDim.x) {
-        ublk[s] = tabs.seg_ublk[s];
-        start[s] = tabs.seg_start[s];
-    }
+    int *start = seg_smem, *chk = start + (max_seg + 1);
+    for (int s = threadIdx.x; s <= nseg; s += blockDim.x) start[s] = tabs.seg_start[s];
     __syncthreads();
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
+    {
+        // each thread a contiguous run of segments: its count, a scan across the block,
+        // then the run's prefixes
+        const int per = (nseg + kSmallThreads - 1) / kSmallThreads;
+        const int s0 = min(nseg, (int)threadIdx.x * per), s1 = min(nseg, s0 + per);
+        int local = 0;
+        for (int s = s0; s < s1; ++s)
+            if (seg_on_warp_shrink(s, tabs)) local += (start[s + 1] - start[s] + kSmallChunk - 1) / kSmallChunk;
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) warp_sum[warp] = incl;
+        __syncthreads();
+        int base = 0, total = 0;
+#pragma unroll
+        for (int w = 0; w < kSmallThreads / 32; ++w) {
+            if (w < warp) base += warp_sum[w];
+            total += warp_sum[w];
+        }
+        int run = base + incl - local;
+        for (int s = s0; s < s1; ++s) {
+            chk[s] = run;
+            if (seg_on_warp_shrink(s, tabs)) run += (start[s + 1] - start[s] + kSmallChunk - 1) / kSmallChunk;
+        }
+        if (threadIdx.x == 0) chk[nseg] = total;
+        __syncthreads();
+    }
     const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nw = (int)((gridDim.x * blockDim.x) >> 5);
-    constexpr int kChunks = kShrinkRows / kSmallChunk;  // chunks of one unit
-    const int units = ublk[nseg];
     const int P = pool.max_pages, d_in = pool.d_in;
-    // work items (chunk, unit, page), the chunk index slowest: the first chunk of every
-    // unit (the only one most units have) comes first and spreads over all warps
-    const int items = kChunks * units * P;
+    // work items (chunk, page) in segment order: the grid has about a warp per item
+    const int items = chk[nseg] * P;
     for (int v = gw; v < items; v += nw) {
-        const int h = v / (units * P), rem = v - h * (units * P);
-        const int u = rem / P, q = rem - u * P;
-        int lo = 0, hi = nseg;  // the unit's segment: the largest s with ublk[s] <= u
+        const int c = v / P, q = v - c * P;
+        int lo = 0, hi = nseg;  // the chunk's segment: the largest s with chk[s] <= c
         while (hi - lo > 1) {
             const int mid = (lo + hi) >> 1;
-            if (ublk[mid] <= u) lo = mid; else hi = mid;
+            if (chk[mid] <= c) lo = mid; else hi = mid;
         }
         const int s = lo;
-        const int p0 = start[s] + (u - ublk[s]) * kShrinkRows + h * kSmallChunk;
-        const int p1u = min(start[s] + (u - ublk[s] + 1) * kShrinkRows, start[s + 1]);
-        if (p0 >= p1u || !seg_on_warp_shrink(s, tabs)) continue;
+        const int p0 = start[s] + (c - chk[s]) * kSmallChunk;
+        const int p1u = start[s + 1];
+        if (p0 >= p1u) continue;
         const int len = min(kSmallChunk, p1u - p0);
 #ifdef LORA_CHECK
         if (!check_range(p0, 0, T, err) || !check_range(p0 + len, p0, T + 1, err)) continue;
@@ -416,6 +441,11 @@ __global__ void __launch_bounds__(kSmallThreads)
         const bool has0 = g < len, has8 = g + 8 < len;
         const int tok0 = has0 ? LORA_CHECKED(tabs.order[p0 + g], 0, T, err, 0) : 0;
         const int tok8 = has8 ? LORA_CHECKED(tabs.order[p0 + g + 8], 0, T, err, 0) : 0;
+        // the page (8 rows of d_in, contiguous) and the chunk's X rows requested into L2 as
+        // whole rows, so the rounds of loads below hit L2 instead of trickling from DRAM
+        if (lane == 0) prefetch_l2_bulk(pool.A_pages + (size_t)page * kRankPage * d_in, (uint32_t)(kRankPage * d_in * 2));
+        if (t == 0 && has0) prefetch_l2_bulk(X + (size_t)tok0 * d_in, (uint32_t)(d_in * 2));
+        if (t == 0 && has8) prefetch_l2_bulk(X + (size_t)tok8 * d_in, (uint32_t)(d_in * 2));
         const uint16_t *x0 = X + (size_t)tok0 * d_in + 8 * t;
         const uint16_t *x8 = X + (size_t)tok8 * d_in + 8 * t;
         const uint16_t *ar = pool.A_pages + ((size_t)page * kRankPage + g) * d_in + 8 * t;
@@ -481,8 +511,11 @@ cudaError_t launch_shrink_small(const uint16_t *X, int T, const PoolDev &pool, S
     const size_t smem = 2 * ((size_t)max_seg + 1) * sizeof(int);
     cudaError_t e = ensure_smem_attr((const void *)shrink_small_kernel, smem);
     if (e != cudaSuccess) return e;
-    // work items (unit, chunk, page) strided over six CTAs of four warps per SM
-    shrink_small_kernel<<<6 * num_sms, kSmallThreads, smem, stream>>>(X, pool, tabs, Vhl, ldh, err, T, max_seg);
+    // about a warp per work item (chunk, page): up to T / 16 + segments chunks
+    const long long max_items = ((long long)T / kSmallChunk + max_seg) * pool.max_pages;
+    const long long want = (max_items + kSmallThreads / 32 - 1) / (kSmallThreads / 32);
+    const int grid = (int)std::max<long long>(num_sms, std::min<long long>(want, 8ll * num_sms));
+    shrink_small_kernel<<<grid, kSmallThreads, smem, stream>>>(X, pool, tabs, Vhl, ldh, err, T, max_seg);
     return cudaGetLastError();
 }
 
