@@ -41,7 +41,6 @@ constexpr int kSBoxes = 2;
 
 struct UnitInfo {
     int p0, p1;       // positions in `order`
-    bool small;       // the segment is left to the warp-level shrink (seg_on_warp_shrink)
     int npages;       // adapter pages
     int n;            // MMA N: npages * 8 rounded up to 16
     const int32_t *pages;
@@ -69,14 +68,36 @@ __device__ __forceinline__ bool seg_on_warp_shrink(int s, const SegTables &tabs)
     return len <= kShrinkSmallSeg || tabs.order[p0 + len - 1] - tabs.order[p0] != len - 1;
 }
 
-__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs, int T,
-                                              int *err)
+// The tensor-core shrink's copy of the segments' unit prefix in shared memory, each entry
+// with bit 31 set when the segment is left to the warp-level shrink ([nseg + 1], the last
+// entry the number of units); nullptr when it did not fit (the global tables are read).
+constexpr uint32_t kSmallBit = 0x80000000u;
+
+__device__ __forceinline__ int unit_segment_smem(int u, const uint32_t *sseg, int nseg)
 {
-    const int s = unit_segment(u, tabs);
+    int lo = 0, hi = nseg;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((int)(sseg[mid] & ~kSmallBit) <= u) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Whether unit u belongs to a segment the warp-level shrink takes (every role of the
+// tensor-core shrink skips the same units).
+__device__ __forceinline__ bool unit_is_small(int u, const uint32_t *sseg, int nseg, const SegTables &tabs)
+{
+    if (sseg != nullptr) return (sseg[unit_segment_smem(u, sseg, nseg)] & kSmallBit) != 0;
+    return seg_on_warp_shrink(unit_segment(u, tabs), tabs);
+}
+
+__device__ __forceinline__ UnitInfo unit_info(int u, const PoolDev &pool, const SegTables &tabs, int T,
+                                              int *err, const uint32_t *sseg = nullptr, int nseg = 0)
+{
+    const int s = sseg != nullptr ? unit_segment_smem(u, sseg, nseg) : unit_segment(u, tabs);
     UnitInfo r;
     r.p0 = tabs.seg_start[s] + (u - tabs.seg_ublk[s]) * kShrinkRows;
     r.p1 = min(r.p0 + kShrinkRows, tabs.seg_start[s + 1]);
-    r.small = seg_on_warp_shrink(s, tabs);
     int slot = tabs.seg_slot[s];
 #ifdef LORA_CHECK
     // a unit outside the tokens or a slot outside the pool: an empty unit of slot 0
@@ -102,7 +123,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                      const __grid_constant__ CUtensorMap tmAw,
                      const uint16_t *__restrict__ X, PoolDev pool, SegTables tabs,
                      uint16_t *__restrict__ Vhl, int ldh, int nmax, int stages, uint32_t tmem_cols,
-                     int *err, uint64_t *trace, int T)
+                     int *err, uint64_t *trace, int T, int sseg_cap)
 {
     trace_enter_released(trace);
     extern __shared__ uint8_t shrink_smem_raw[];
@@ -121,6 +142,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int units = tabs.hdr[HDR_UNITS];
+    // the unit prefix and the small flags in shared memory, where they fit: each unit's
+    // segment and whether it is skipped then cost no global loads
+    const int nseg = tabs.hdr[HDR_NUMSEG];
+    uint32_t *sseg = nseg + 1 <= sseg_cap ? tmem_slot + 4 : nullptr;
+    if (sseg != nullptr)
+        for (int s = threadIdx.x; s <= nseg; s += blockDim.x)
+            sseg[s] = (uint32_t)tabs.seg_ublk[s] | (s < nseg && seg_on_warp_shrink(s, tabs) ? kSmallBit : 0u);
     const int d_in = pool.d_in;
     const int KB = (d_in + 64 * kSBoxes - 1) / (64 * kSBoxes);
 
@@ -155,8 +183,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ producer
         int it = 0;
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(u, pool, tabs, T, err);
-            if (ui.small) continue;  // (every role skips the same units)
+            if (unit_is_small(u, sseg, nseg, tabs)) continue;  // (every role skips the same units)
+            const UnitInfo ui = unit_info(u, pool, tabs, T, err, sseg, nseg);
             const int row0 = LORA_CHECKED(tabs.order[ui.p0], 0, T, err, 0);
             bool contiguous = true;
             for (int r = lane; r < ui.p1 - ui.p0; r += 32)
@@ -240,8 +268,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             int it = 0, uc = 0;
             bool ok = true;
             for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-                const UnitInfo ui = unit_info(u, pool, tabs, T, err);
-                if (ui.small) continue;
+                if (unit_is_small(u, sseg, nseg, tabs)) continue;
+                const UnitInfo ui = unit_info(u, pool, tabs, T, err, sseg, nseg);
                 const int buf = uc & 1;
                 ok = mbar_wait(&acc_empty[buf], ((uint32_t)(uc >> 1) & 1u) ^ 1u, &abort_flag, err);
                 if (!ok) break;
@@ -276,8 +304,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         // ------------------------------------------------------------ epilogue
         int uc = 0;  // units run, as in the MMA role
         for (int u = blockIdx.x; u < units; u += gridDim.x) {
-            const UnitInfo ui = unit_info(u, pool, tabs, T, err);
-            if (ui.small) continue;
+            if (unit_is_small(u, sseg, nseg, tabs)) continue;
+            const UnitInfo ui = unit_info(u, pool, tabs, T, err, sseg, nseg);
             const int buf = uc & 1;
             bool ok = true;
             if (lane == 0) ok = mbar_wait(&acc_full[buf], (uint32_t)(uc >> 1) & 1u, &abort_flag, err);
@@ -529,16 +557,18 @@ cudaError_t launch_shrink_tc(const CUtensorMap &tmX, const CUtensorMap &tmA,
     int stages = (int)((200 * 1024) / stage_bytes);
     if (stages > 6) stages = 6;
     if (stages < 2) stages = 2;
-    const size_t smem = 1024 + stages * stage_bytes + (2 * stages + 5) * 8 + 16;
-    const uint32_t tmem_cols = pow2_cols(2 * nmax);
     const int max_seg = T < pool.max_adapters ? T : pool.max_adapters;
+    // the segments' unit prefix in shared memory when it fits in 16 KB
+    const int sseg_cap = max_seg + 1 <= 4096 ? max_seg + 1 : 0;
+    const size_t smem = 1024 + stages * stage_bytes + (2 * stages + 5) * 8 + 16 + (size_t)sseg_cap * 4;
+    const uint32_t tmem_cols = pow2_cols(2 * nmax);
     const int max_units = (T + kShrinkRows - 1) / kShrinkRows + max_seg;
     int grid = max_units < num_sms ? max_units : num_sms;
     if (grid <= 0) return cudaSuccess;
     cudaError_t e = ensure_smem_attr((const void *)shrink_tc_kernel, smem);
     if (e != cudaSuccess) return e;
     shrink_tc_kernel<<<grid, kTcThreads, smem, stream>>>(tmX, tmA, tmAw, X, pool, tabs, Vhl, ldh, nmax,
-                                                          stages, tmem_cols, err, trace, T);
+                                                          stages, tmem_cols, err, trace, T, sseg_cap);
     return cudaGetLastError();
 }
 
