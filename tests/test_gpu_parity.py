@@ -201,6 +201,33 @@ def test_scattered_prefill(kernel):
     assert_routing(got, ref, base, prob.ids, f"scattered/{kernel}")
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_many_adapter_prefill_full_size(kernel):
+    """The large-pool prefill at its benchmarked size: 4096 tokens over 2000 rank-16
+    adapters with Zipf ids (~1100 segments; every GEMM tile mixes adapters, every segment
+    goes to the warp-level shrink, in one pass of work items). 128 sampled rows (the
+    largest segment's, singletons', others) against the oracle, element by element."""
+    prob = L.prefill_zipf()
+    pool = load_pool(al, prob)
+    pool.set_prefill_kernel({"single": al.LORA_PREFILL_SINGLE, "pair": al.LORA_PREFILL_PAIR}[kernel])
+    got = run(pool, prob, PATHS["prefill"])
+    assert pool.check_errors() == al.LORA_OK
+    ids = prob.ids
+    sizes = np.bincount(ids[ids >= 0], minlength=prob.max_adapters)
+    g = L.rng_for(77, 9)
+    head = np.flatnonzero(ids == int(np.argmax(sizes)))
+    single = np.flatnonzero(sizes[np.maximum(ids, 0)] == 1)
+    rows = np.unique(np.concatenate([g.choice(head, 32, replace=False), g.choice(single, 32, replace=False),
+                                     g.choice(prob.T, 64, replace=False)]))
+    used = {int(s) for s in ids[rows] if s >= 0}
+    ads = {s: (a.A, a.B, a.rank, a.alpha) for s, a in prob.adapters.items() if s in used}
+    ref = oracle.lora_linear(prob.X[rows], prob.W, ids[rows], ads, prob.max_adapters)
+    base = oracle.lora_linear(prob.X[rows], prob.W, np.full(len(rows), -1, np.int32), {}, prob.max_adapters)
+    assert_parity(got[rows], ref, f"many adapters/{kernel}")
+    assert_routing(got[rows], ref, base, ids[rows], f"many adapters/{kernel}")
+    pool.close()
+
+
 # ------------------------------------------------------------------ segments
 
 def seg_cases():
