@@ -461,7 +461,7 @@ constexpr int kPBlockBytes = 2 * kPHalfBytes;  // one k-block of one CTA: X half
 constexpr int kPKps = 2;                       // k-blocks per pipeline stage
 constexpr int kPStageBytes = kPKps * kPBlockBytes;
 constexpr int kPStages = 3;
-constexpr int kPGroupM = 8;                   // 8 x 256 tokens share one column sweep
+constexpr int kPGroupM = 16;                  // 16 x 256 tokens share one column sweep
 constexpr int kPSliceBytes = 128 * 16;        // 128 columns x 8 rank values of one page
 constexpr int kPYStageBytes = 32 * 128;       // one epilogue warp's 32 x 64 bf16 staging tile
 constexpr size_t kPairSmem =
