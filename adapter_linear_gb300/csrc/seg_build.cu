@@ -404,21 +404,31 @@ __global__ void __launch_bounds__(kSegChunk)
             }
             if (lane == 0) hist[k] = carry;
         }
-    } else for (int k = tid; k < K; k += kSegChunk) {
-        int carry = 0;
+    } else for (int k = tid; k < K; k += 2 * kSegChunk) {
+        // two keys per thread (k and k + kSegChunk): 32 loads in flight per round
+        const int k2 = k + kSegChunk;
+        const bool two = k2 < K;
+        int carry = 0, carry2 = 0;
         for (int c0 = 0; c0 < chunks; c0 += 16) {
-            int v[16];
+            int v[16], v2[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 16; ++i) {
                 v[i] = c0 + i < chunks ? __ldcg(tabs.chist + (size_t)(c0 + i) * K + k) : 0;
+                v2[i] = two && c0 + i < chunks ? __ldcg(tabs.chist + (size_t)(c0 + i) * K + k2) : 0;
+            }
 #pragma unroll
             for (int i = 0; i < 16; ++i)
                 if (c0 + i < chunks) {
                     tabs.chist[(size_t)(c0 + i) * K + k] = carry;
                     carry += v[i];
+                    if (two) {
+                        tabs.chist[(size_t)(c0 + i) * K + k2] = carry2;
+                        carry2 += v2[i];
+                    }
                 }
         }
         hist[k] = carry;
+        if (two) hist[k2] = carry2;
     }
     __syncthreads();
     scan_keys(hist, K, T, tabs, tabs.chist + (size_t)K * chunks);
