@@ -369,8 +369,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
 // ======================================== warp-level shrink of small or scattered segments
 //
-// One warp per (128-row unit, chunk of up to 16 tokens, page) of the segments
-// seg_on_warp_shrink picks: D[16 tokens][8 ranks] = X_chunk . A_page^T over d_in with
+// One warp per (chunk of up to 16 tokens, page) of the segments seg_on_warp_shrink picks
+// (each CTA numbers exactly these work items through a shared-memory prefix of the
+// segments' chunk counts; the grid has about a warp per item; each item first requests
+// its A page and its X rows into L2 with bulk prefetches): D[16 tokens][8 ranks] = X_chunk . A_page^T over d_in with
 // warp-level bf16 MMAs (m16n8k16, fp32 accumulation) -- a 16 x 8 tile is what a few
 // tokens of one adapter need, far below the tcgen05 tile. The operands come straight from
 // global memory in a k order both share (a dot product does not depend on it): in each
@@ -383,7 +385,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // group).
 constexpr int kSmallThreads = 128;
 constexpr int kSmallChunk = 16;  // tokens per MMA tile
-static_assert(kShrinkRows % kSmallChunk == 0, "a unit splits into whole chunks");
 
 __device__ __forceinline__ void mma_m16n8k16_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                                   uint32_t a3, uint32_t b0, uint32_t b1)
