@@ -228,6 +228,35 @@ def test_many_adapter_prefill_full_size(kernel):
     pool.close()
 
 
+@pytest.mark.parametrize("kernel", ["single", "pair"])
+def test_many_small_segments_more_items_than_warps(kernel):
+    """16384 tokens uniform over 4000 rank-16 adapters at d = 256: more (chunk, page) work
+    items for the warp-level shrink than its grid has warps, so warps take several items;
+    256 sampled rows against the oracle."""
+    d, T, n, seed = 256, 16384, 4000, 97
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d, d), 1.0 / 16)
+    ids = L.rng_for(seed, L.ROLE_IDS, 0).integers(0, n, T).astype(np.int32)
+    ids[L.rng_for(seed, L.ROLE_IDS, 3).random(T) < 0.05] = -1
+    ads = {i: L.make_adapter(seed, i, d, d, 16, 32.0) for i in range(n)}
+    prob = L.Problem("many_small", d, d, X, W, ids, ads, n, 16, seed)
+    sizes = np.bincount(ids[ids >= 0], minlength=n)
+    chunks = int(((sizes + 15) // 16).sum())
+    assert chunks * 2 > 8 * 152 * 4  # (chunk, page) items beyond one per warp of the largest grid
+    pool = load_pool(al, prob)
+    pool.set_prefill_kernel({"single": al.LORA_PREFILL_SINGLE, "pair": al.LORA_PREFILL_PAIR}[kernel])
+    got = run(pool, prob, PATHS["prefill"])
+    assert pool.check_errors() == al.LORA_OK
+    rows = np.sort(L.rng_for(seed, 9).choice(T, 256, replace=False))
+    used = {int(s) for s in ids[rows] if s >= 0}
+    sub = {s: (a.A, a.B, a.rank, a.alpha) for s, a in ads.items() if s in used}
+    ref = oracle.lora_linear(X[rows], W, ids[rows], sub, n)
+    base = oracle.lora_linear(X[rows], W, np.full(len(rows), -1, np.int32), {}, n)
+    assert_parity(got[rows], ref, f"many small segments/{kernel}")
+    assert_routing(got[rows], ref, base, ids[rows], f"many small segments/{kernel}")
+    pool.close()
+
+
 # ------------------------------------------------------------------ segments
 
 def seg_cases():
