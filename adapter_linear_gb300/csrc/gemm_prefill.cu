@@ -599,6 +599,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sb = (a.KB + kPKps - 1) / kPKps, steps = sb + (ne + kPKps - 1) / kPKps;
                 const int n0 = cur.n * kBN + (int)rank * 128;   // this CTA's W rows / B columns
                 const int r0 = cur.m * kPBM + (int)rank * 128;  // this CTA's token rows
+                // the first expand block's page numbers, loaded now and used after the
+                // base k-blocks (each copy is an asm statement that keeps its place, so
+                // a load written beside it would hold up the producer for its latency)
+                int pg0[kPagesPerBlock];
+#pragma unroll
+                for (int i = 0; i < kPagesPerBlock; ++i) pg0[i] = ne > 0 && i < tl.npages ? tl.pages[i] : 0;
                 for (int st = 0; st < steps; ++st, ++it) {
                     const int s = it % kPStages;
                     ok = mbar_wait_cluster(&empty[s], ((uint32_t)(it / kPStages) & 1u) ^ 1u, &abort_flag,
@@ -620,12 +626,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int j = 0; j < nj; ++j) {
                             const int e = e0 + j;
                             uint8_t *bs = xs + j * kPBlockBytes;
-                            tma_load_2d_pair(bs, &tmV, fb, e * 64, r0);
+                            // the block's page numbers (page 0 is zeros), all loaded before
+                            // the first copy is issued
+                            int pg[kPagesPerBlock];
+#pragma unroll
                             for (int i = 0; i < kPagesPerBlock; ++i) {
                                 const int q = e * kPagesPerBlock + i;
-                                const int page = q < tl.npages
-                                                     ? LORA_CHECKED(tl.pages[q], 0, pool.num_pages, a.err, 0)
-                                                     : 0;  // page 0 is zeros
+                                pg[i] = e == 0 ? pg0[i] : q < tl.npages ? tl.pages[q] : 0;
+                            }
+                            tma_load_2d_pair(bs, &tmV, fb, e * 64, r0);
+#pragma unroll
+                            for (int i = 0; i < kPagesPerBlock; ++i) {
+                                const int page = LORA_CHECKED(pg[i], 0, pool.num_pages, a.err, 0);
                                 // columns n0.. of the page: 128 x 16 B from row (page d_out + n0) / 8
                                 // of the 128-byte-row view (n0 and d_out are multiples of 8)
                                 tma_load_2d_pair(bs + kPHalfBytes + i * kPSliceBytes, &tmB, fb, 0,
