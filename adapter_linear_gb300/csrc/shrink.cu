@@ -146,9 +146,33 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // segment and whether it is skipped then cost no global loads
     const int nseg = tabs.hdr[HDR_NUMSEG];
     uint32_t *sseg = nseg + 1 <= sseg_cap ? tmem_slot + 4 : nullptr;
-    if (sseg != nullptr)
-        for (int s = threadIdx.x; s <= nseg; s += blockDim.x)
-            sseg[s] = (uint32_t)tabs.seg_ublk[s] | (s < nseg && seg_on_warp_shrink(s, tabs) ? kSmallBit : 0u);
+    if (sseg != nullptr) {
+        // four segments a thread per round, every load of a kind issued before any use
+        // (the test of seg_on_warp_shrink: rows from `order` only above kShrinkSmallSeg)
+        constexpr int kR = 4;
+        for (int s0 = threadIdx.x; s0 <= nseg; s0 += kR * (int)blockDim.x) {
+            int ub[kR], p0[kR], p1[kR], o0[kR], o1[kR];
+#pragma unroll
+            for (int j = 0; j < kR; ++j) {
+                const int s = s0 + j * (int)blockDim.x;
+                ub[j] = s <= nseg ? tabs.seg_ublk[s] : 0;
+                p0[j] = s < nseg ? tabs.seg_start[s] : 0;
+                p1[j] = s < nseg ? tabs.seg_start[s + 1] : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < kR; ++j) {
+                const bool big = p1[j] - p0[j] > kShrinkSmallSeg;
+                o0[j] = big ? tabs.order[p0[j]] : 0;
+                o1[j] = big ? tabs.order[p1[j] - 1] : 0;
+            }
+#pragma unroll
+            for (int j = 0; j < kR; ++j) {
+                const int s = s0 + j * (int)blockDim.x, len = p1[j] - p0[j];
+                const bool small = s < nseg && (len <= kShrinkSmallSeg || o1[j] - o0[j] != len - 1);
+                if (s <= nseg) sseg[s] = (uint32_t)ub[j] | (small ? kSmallBit : 0u);
+            }
+        }
+    }
     const int d_in = pool.d_in;
     const int KB = (d_in + 64 * kSBoxes - 1) / (64 * kSBoxes);
 
@@ -410,15 +434,23 @@ __global__ void __launch_bounds__(kSmallThreads)
     int *start = seg_smem, *chk = start + (max_seg + 1);
     for (int s = threadIdx.x; s <= nseg; s += blockDim.x) start[s] = tabs.seg_start[s];
     __syncthreads();
+    // each segment's chunk count (0 for a segment left to the tensor-core shrink), from
+    // the starts in shared memory: only a segment above kShrinkSmallSeg tokens reads its
+    // first and last row from `order` (the test of seg_on_warp_shrink)
+    for (int s = threadIdx.x; s < nseg; s += blockDim.x) {
+        const int p0 = start[s], len = start[s + 1] - p0;
+        const bool mine = len <= kShrinkSmallSeg || tabs.order[p0 + len - 1] - tabs.order[p0] != len - 1;
+        chk[s] = mine ? (len + kSmallChunk - 1) / kSmallChunk : 0;
+    }
+    __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, g = lane >> 2, t = lane & 3;
     {
         // each thread a contiguous run of segments: its count, a scan across the block,
-        // then the run's prefixes
+        // then the run's prefixes (in place of the counts)
         const int per = (nseg + kSmallThreads - 1) / kSmallThreads;
         const int s0 = min(nseg, (int)threadIdx.x * per), s1 = min(nseg, s0 + per);
         int local = 0;
-        for (int s = s0; s < s1; ++s)
-            if (seg_on_warp_shrink(s, tabs)) local += (start[s + 1] - start[s] + kSmallChunk - 1) / kSmallChunk;
+        for (int s = s0; s < s1; ++s) local += chk[s];
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -435,8 +467,9 @@ __global__ void __launch_bounds__(kSmallThreads)
         }
         int run = base + incl - local;
         for (int s = s0; s < s1; ++s) {
+            const int n = chk[s];
             chk[s] = run;
-            if (seg_on_warp_shrink(s, tabs)) run += (start[s + 1] - start[s] + kSmallChunk - 1) / kSmallChunk;
+            run += n;
         }
         if (threadIdx.x == 0) chk[nseg] = total;
         __syncthreads();
