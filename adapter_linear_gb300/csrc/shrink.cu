@@ -396,9 +396,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // One warp per (chunk of up to 16 tokens, page) of the segments seg_on_warp_shrink picks
 // (each CTA numbers exactly these work items through a shared-memory prefix of the
 // segments' chunk counts; the grid has about a warp per item; each item first requests
-// its A page and its X rows into L2 with bulk prefetches): D[16 tokens][8 ranks] = X_chunk . A_page^T over d_in with
-// warp-level bf16 MMAs (m16n8k16, fp32 accumulation) -- a 16 x 8 tile is what a few
-// tokens of one adapter need, far below the tcgen05 tile. The operands come straight from
+// its A page and its X rows into L2 with bulk prefetches):
+// D[16 tokens][8 ranks] = X_chunk . A_page^T over d_in with warp-level bf16 MMAs
+// (m16n8k16, fp32 accumulation) -- a 16 x 8 tile is what a few tokens of one adapter
+// need, far below the tcgen05 tile. The operands come straight from
 // global memory in a k order both share (a dot product does not depend on it): in each
 // 32-wide step at k0, thread (g = lane / 4, t = lane % 4) loads the 8 inputs k0 + 8t ..
 // k0 + 8t + 7 of token rows g and g + 8 and of rank row g of the page, and gives elements
