@@ -37,8 +37,8 @@ lora_status ensure_tier(lora_pool *p)
     return LORA_OK;
 }
 
-// Take cached slot s out of the GPU: its pages return to the free list and its
-// table row is cleared (asynchronously, after the calls already enqueued).
+// Take cached slot s out of the GPU: its table row is cleared and its pages are
+// freed (asynchronously, after the calls already enqueued).
 lora_status evict(lora_pool *p, int s)
 {
     int32_t *row = &p->h_slots[(size_t)s * p->slot_stride];
@@ -46,8 +46,7 @@ lora_status evict(lora_pool *p, int s)
     lora_status st = stage_row_ready(p, p->max_adapters, &zero);
     if (st != LORA_OK) return st;
     if ((st = enqueue_row(p, s, zero)) != LORA_OK) return st;
-    const int npages = row[SLOT_NPAGES];
-    for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
+    if ((st = release_pages(p, &row[SLOT_PAGES], row[SLOT_NPAGES])) != LORA_OK) return st;
     std::fill(row, row + p->slot_stride, 0);
     p->host_tier[p->slot_key[s]].slot = -1;
     p->slot_key[s] = kNoKey;
@@ -84,7 +83,7 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
 {
     const int npages = (h.rank + kRankPage - 1) / kRankPage;
     int slot = empty_slot(p);
-    while (slot < 0 || (int)p->free_pages.size() < npages) {
+    while (slot < 0 || free_page_count(p) < npages) {
         const int victim = lru_victim(p);
         if (victim < 0) return LORA_ERR_OOM;  // everything left is held
         lora_status st = evict(p, victim);
@@ -97,7 +96,8 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
     if (st != LORA_OK) return st;
     int32_t *pages = row + p->slot_stride;
     std::fill(row, row + p->slot_stride + p->max_pages, 0);
-    for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
+    bool fresh = false;  // written on the copy stream, after the calls, in any case
+    take_pages(p, npages, pages, &fresh);
     const float scale = h.alpha / (float)h.rank;
     row[SLOT_RANK] = h.rank;
     row[SLOT_NPAGES] = npages;
@@ -117,7 +117,6 @@ lora_status swap_in(lora_pool *p, int64_t key, HostAdapter &h)
                                  pool_view(p), p->A_pages, p->B_pages, p->d_err, s));
     if ((st = enqueue_row(p, slot, row)) != LORA_OK) return st;
 
-    p->free_pages.resize(p->free_pages.size() - npages);
     std::copy(row, row + p->slot_stride, &p->h_slots[(size_t)slot * p->slot_stride]);
     p->slot_key[slot] = key;
     h.slot = slot;

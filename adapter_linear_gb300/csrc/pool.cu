@@ -103,6 +103,72 @@ lora_status enqueue_row(lora_pool *p, int slot, const int32_t *row)
     return LORA_OK;
 }
 
+lora_status release_pages(lora_pool *p, const int32_t *pages, int n)
+{
+    if (n <= 0) return LORA_OK;
+    cudaEvent_t ev = nullptr;
+    if (!p->idle_events.empty()) {
+        ev = p->idle_events.back();
+        p->idle_events.pop_back();
+    } else {
+        CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    }
+    if (cudaEventRecord(ev, p->copy_stream) != cudaSuccess) {
+        cudaGetLastError();
+        cudaEventDestroy(ev);
+        return LORA_ERR_CUDA;  // the pages stay out of the free list
+    }
+    p->freed.push_back({ev, std::vector<int32_t>(pages, pages + n)});
+    return LORA_OK;
+}
+
+// Freed batches whose event has completed join the free list (the batches were
+// recorded in order on one stream, so the first pending one ends the scan).
+static void reclaim_pages(lora_pool *p)
+{
+    while (!p->freed.empty()) {
+        lora_pool::FreedBatch &b = p->freed.front();
+        const cudaError_t q = cudaEventQuery(b.ev);
+        if (q != cudaSuccess) {
+            if (q != cudaErrorNotReady) cudaGetLastError();
+            break;
+        }
+        p->free_pages.insert(p->free_pages.end(), b.pages.rbegin(), b.pages.rend());
+        p->idle_events.push_back(b.ev);
+        p->freed.pop_front();
+    }
+}
+
+int free_page_count(const lora_pool *p)
+{
+    size_t n = p->free_pages.size();
+    for (const lora_pool::FreedBatch &b : p->freed) n += b.pages.size();
+    return (int)n;
+}
+
+void take_pages(lora_pool *p, int n, int32_t *out, bool *fresh)
+{
+    reclaim_pages(p);
+    *fresh = (int)p->free_pages.size() >= n;
+    int k = 0;
+    while (k < n && !p->free_pages.empty()) {
+        out[k++] = p->free_pages.back();
+        p->free_pages.pop_back();
+    }
+    // not enough: the oldest freed pages, written on the copy stream after the calls
+    while (k < n && !p->freed.empty()) {
+        lora_pool::FreedBatch &b = p->freed.front();
+        while (k < n && !b.pages.empty()) {
+            out[k++] = b.pages.back();
+            b.pages.pop_back();
+        }
+        if (b.pages.empty()) {
+            p->idle_events.push_back(b.ev);  // a later record replaces its pending one
+            p->freed.pop_front();
+        }
+    }
+}
+
 }  // namespace lora
 
 namespace {
@@ -563,7 +629,10 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
     p->d_in = d_in;
     p->d_out = d_out;
     p->max_pages = (max_rank + kRankPage - 1) / kRankPage;
-    p->num_pages = max_adapters * p->max_pages + 1;
+    // the zero page, room for max_adapters adapters at max_rank, and a reserve of two
+    // adapters' pages so that a swap on a full pool can write pages no call still reads
+    p->reserve_pages = 2 * p->max_pages;
+    p->num_pages = max_adapters * p->max_pages + 1 + p->reserve_pages;
     // page ids, then one scale per page, and one more readable scale entry (the
     // tensor-core shrink reads the scale of the zero page that pads an odd count)
     p->slot_stride = ((slot_page_scale(p->max_pages, p->max_pages) + 1 + 3) / 4) * 4;
@@ -586,7 +655,8 @@ lora_status lora_pool_create(int max_adapters, int max_rank, int d_in, int d_out
         (st = alloc_dev(p, (void **)&p->stage_B, (size_t)d_out * max_rank * 2)) ||
         (st = alloc_dev(p, (void **)&p->load_A, (size_t)d_in * max_rank * 2)) ||
         (st = alloc_dev(p, (void **)&p->load_B, (size_t)d_out * max_rank * 2)) ||
-        (st = alloc_dev(p, (void **)&p->d_page_list, sizeof(int32_t) * p->max_pages))) {
+        (st = alloc_dev(p, (void **)&p->d_page_list, sizeof(int32_t) * p->max_pages)) ||
+        (st = alloc_dev(p, (void **)&p->d_page_list_load, sizeof(int32_t) * p->max_pages))) {
         lora_pool_destroy(p);
         return st;
     }
@@ -653,6 +723,9 @@ lora_status lora_pool_destroy(lora_pool_t p)
     free_dev(p, p->wdq, 0);
     free_dev(p, p->load_B, 0);
     free_dev(p, p->d_page_list, 0);
+    free_dev(p, p->d_page_list_load, 0);
+    for (const lora_pool::FreedBatch &b : p->freed) cudaEventDestroy(b.ev);
+    for (cudaEvent_t e : p->idle_events) cudaEventDestroy(e);
     if (p->copy_stream) cudaStreamDestroy(p->copy_stream);
     if (p->load_stream) cudaStreamDestroy(p->load_stream);
     for (auto &e : p->ev)
@@ -682,25 +755,39 @@ lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void
     int32_t *row = &p->h_slots[(size_t)slot * p->slot_stride];
     if (row[SLOT_RANK] != 0) return LORA_ERR_SLOT_OCCUPIED;
     const int npages = (rank + kRankPage - 1) / kRankPage;
-    if ((int)p->free_pages.size() < npages) return LORA_ERR_OOM;
+    if (free_page_count(p) < npages) return LORA_ERR_OOM;
 
     // The caller's A and B into the pool's load buffers first, on a stream of their
     // own (not behind the pool's calls), so that the caller may free them on return;
     // the previous load's packing must have read those buffers.
     const size_t a_bytes = (size_t)p->d_in * rank * 2, b_bytes = (size_t)rank * p->d_out * 2;
     CUDA_TRY(cudaEventSynchronize(p->ev_loaded));
-    if (cudaMemcpyAsync(p->load_A, A, a_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
-        cudaMemcpyAsync(p->load_B, B, b_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
-        cudaStreamSynchronize(p->load_stream) != cudaSuccess) {
-        cudaGetLastError();
-        return LORA_ERR_CUDA;
-    }
     int32_t *srow = nullptr;
     lora_status st = stage_row_ready(p, slot, &srow);
     if (st != LORA_OK) return st;
     int32_t *pages = srow + p->slot_stride;
     std::fill(srow, srow + p->slot_stride + p->max_pages, 0);
-    for (int q = 0; q < npages; ++q) pages[q] = p->free_pages[p->free_pages.size() - 1 - q];
+    bool fresh = false;
+    take_pages(p, npages, pages, &fresh);
+    // Pages that no enqueued call can read are written at once on the load stream,
+    // behind the copies (the wait below covers both); pages freed by an unload whose
+    // earlier calls may still be running are written on the copy stream after every
+    // call enqueued on the pool so far. Either way the table row follows on the copy
+    // stream, before every call enqueued from now on.
+    cudaStream_t ps = fresh ? p->load_stream : p->copy_stream;
+    int32_t *d_list = fresh ? p->d_page_list_load : p->d_page_list;
+    if (cudaMemcpyAsync(p->load_A, A, a_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
+        cudaMemcpyAsync(p->load_B, B, b_bytes, cudaMemcpyDefault, p->load_stream) != cudaSuccess ||
+        (!fresh && cudaStreamSynchronize(p->load_stream) != cudaSuccess) ||
+        cudaMemcpyAsync(d_list, pages, sizeof(int32_t) * npages, cudaMemcpyHostToDevice, ps) != cudaSuccess ||
+        launch_pack_adapter(p->load_A, p->load_B, rank, d_list, npages, pool_view(p), p->A_pages,
+                            p->B_pages, p->d_err, ps) != cudaSuccess ||
+        cudaEventRecord(p->ev_loaded, ps) != cudaSuccess ||
+        (fresh && cudaStreamSynchronize(p->load_stream) != cudaSuccess)) {
+        cudaGetLastError();
+        release_pages(p, pages, npages);  // back to the free list, after the calls so far
+        return LORA_ERR_CUDA;
+    }
     srow[SLOT_RANK] = rank;
     srow[SLOT_NPAGES] = npages;
     const float scale = alpha / (float)rank;
@@ -709,20 +796,7 @@ lora_status lora_load_adapter(lora_pool_t p, int slot, const void *A, const void
         srow[SLOT_PAGES + q] = pages[q];
         std::memcpy(&srow[slot_page_scale(p->max_pages, q)], &scale, sizeof(float));
     }
-    // Pages and table row on the copy stream: after every call enqueued on the pool so
-    // far (a free page may still be read by a call enqueued before its unload), and
-    // before every call enqueued from now on.
-    cudaStream_t s = p->copy_stream;
-    if (cudaMemcpyAsync(p->d_page_list, pages, sizeof(int32_t) * npages, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess ||
-        launch_pack_adapter(p->load_A, p->load_B, rank, p->d_page_list, npages, pool_view(p),
-                            p->A_pages, p->B_pages, p->d_err, s) != cudaSuccess ||
-        cudaEventRecord(p->ev_loaded, s) != cudaSuccess) {
-        cudaGetLastError();
-        return LORA_ERR_CUDA;
-    }
     if ((st = enqueue_row(p, slot, srow)) != LORA_OK) return st;
-    p->free_pages.resize(p->free_pages.size() - npages);
     std::copy(srow, srow + p->slot_stride, row);
     p->n_loads += 1;
     return LORA_OK;
@@ -737,8 +811,7 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
     if (p->chain_refs[slot] > 0) return LORA_ERR_IN_USE;  // a chain still lists it
     if (slot_is_held(p, slot)) return LORA_ERR_IN_USE;    // acquired from the host tier
     // the empty row goes in on the copy stream, after the calls enqueued so far; the
-    // pages return to the free list now, and whatever reuses them next writes them on
-    // the same stream, after this
+    // pages are free once those calls have run
     int32_t *zero = nullptr;
     lora_status st = stage_row_ready(p, p->max_adapters, &zero);
     if (st != LORA_OK) return st;
@@ -748,8 +821,8 @@ lora_status lora_unload_adapter(lora_pool_t p, int slot)
         // a chain owns no pages: release its members
         for (int m : p->chain_members[slot]) p->chain_refs[m] -= 1;
         p->chain_members.erase(slot);
-    } else {
-        for (int q = npages - 1; q >= 0; --q) p->free_pages.push_back(row[SLOT_PAGES + q]);
+    } else if ((st = release_pages(p, &row[SLOT_PAGES], npages)) != LORA_OK) {
+        return st;
     }
     std::fill(row, row + p->slot_stride, 0);
     forget_cached_slot(p, slot);
@@ -995,8 +1068,10 @@ lora_status lora_pool_stats(lora_pool_t p, int64_t *out)
     for (int i = 0; i < p->max_adapters; ++i)
         if (p->h_slots[(size_t)i * p->slot_stride + SLOT_RANK] != 0) ++loaded;
     out[0] = loaded;
-    out[1] = (int64_t)p->free_pages.size();
-    out[2] = (int64_t)p->num_pages - 1;
+    // pages for loads, without the zero page and the reserve (loaded adapters never
+    // hold more than max_adapters * max_pages pages, so the free count covers it)
+    out[1] = std::max<int64_t>(0, (int64_t)free_page_count(p) - p->reserve_pages);
+    out[2] = (int64_t)p->num_pages - 1 - p->reserve_pages;
     out[3] = p->n_loads;
     out[4] = p->n_unloads;
     out[5] = p->n_calls;

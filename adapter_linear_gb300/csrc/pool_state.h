@@ -5,6 +5,7 @@
 #pragma once
 
 #include <climits>
+#include <deque>
 #include <map>
 #include <unordered_map>
 #include <vector>
@@ -42,13 +43,26 @@ struct lora_pool {
     int max_adapters = 0, max_rank = 0, d_in = 0, d_out = 0;
     int max_pages = 0;   // pages per adapter at max_rank
     int num_pages = 0;   // arena pages, page 0 = zero page
+    int reserve_pages = 0;  // arena pages beyond max_adapters * max_pages (see free_pages)
     int slot_stride = 0;
     int ldv = 0;         // fp32 row stride of the decode path's low-rank intermediate
     int ldh = 0;         // bf16 row stride of the prefill path's hi/lo intermediate
     uint16_t *A_pages = nullptr, *B_pages = nullptr;
     int32_t *d_slots = nullptr;
     std::vector<int32_t> h_slots;
-    std::vector<int32_t> free_pages;  // stack; back() is taken first
+    // Free pages that no enqueued layer call can read (stack; back() is taken first).
+    // Pages an unload or eviction gives back may still be read by the calls enqueued
+    // before it: they wait in `freed`, a batch per change with an event recorded on the
+    // copy stream after it, and join free_pages once that event has completed. A load
+    // that finds enough free pages writes them at once, beside the running calls; the
+    // reserve pages let a swap on a full pool do so too.
+    std::vector<int32_t> free_pages;
+    struct FreedBatch {
+        cudaEvent_t ev;
+        std::vector<int32_t> pages;
+    };
+    std::deque<FreedBatch> freed;
+    std::vector<cudaEvent_t> idle_events;  // recorded-and-completed batch events, for reuse
     std::vector<int32_t> chain_refs;  // per slot: chains that list it as a member
     std::map<int, std::vector<int>> chain_members;  // chain slot -> member slots
     int *d_err = nullptr;             // [0] the error word, [1] its value at the last read
@@ -56,7 +70,8 @@ struct lora_pool {
     uint16_t *stage_A = nullptr, *stage_B = nullptr;  // swap-ins of the host tier
     uint16_t *load_A = nullptr, *load_B = nullptr;    // lora_load_adapter's copy of A, B
     uint16_t *wdq = nullptr;  // a 4-bit base dequantised to bf16 for the prefill path (first use)
-    int32_t *d_page_list = nullptr;
+    int32_t *d_page_list = nullptr;       // page list of a packing on the copy stream
+    int32_t *d_page_list_load = nullptr;  // ... on the load stream
     // Changes of pages and table rows (loads, unloads, chains, swap-ins) run on the
     // copy stream, which waits for every layer call enqueued on the pool before them;
     // layer calls enqueued after a change wait for the copy stream (ev_copy).
@@ -137,6 +152,15 @@ lora_status stage_row_ready(lora_pool *p, int slot, int32_t **row);
 // Enqueue the copy of a staging row into the device table row of `slot` on the
 // copy stream; later layer calls are ordered after it.
 lora_status enqueue_row(lora_pool *p, int slot, const int32_t *row);
+// Pages given back by an unload or eviction whose table change was just enqueued on
+// the copy stream: free once the calls enqueued before it have run.
+lora_status release_pages(lora_pool *p, const int32_t *pages, int n);
+// Free pages, those still waiting for earlier calls included.
+int free_page_count(const lora_pool *p);
+// Take n free pages into out[] (the caller checked free_page_count). *fresh: every
+// page taken is free of enqueued readers, so it may be written before the calls
+// already enqueued have run; otherwise it must be written on the copy stream.
+void take_pages(lora_pool *p, int n, int32_t *out, bool *fresh);
 // Free the host tier's pinned memory and events (pool destruction).
 void destroy_host_tier(lora_pool *p);
 // A slot the host tier holds for an outstanding acquisition?

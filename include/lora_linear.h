@@ -106,7 +106,9 @@ typedef enum { LORA_PREFILL_AUTO = 0, LORA_PREFILL_SINGLE = 1, LORA_PREFILL_PAIR
  * of one adapter (8 columns of A, stored transposed as 8 x d_in, and 8 rows
  * of B, stored interleaved as d_out x 8); an adapter of rank r holds ceil(r/8)
  * pages taken from a free list. All page arenas, the slot table and the error
- * word are allocated here, once: loading and unloading never allocate.
+ * word are allocated here, once: loading and unloading never allocate. The
+ * arenas hold max_adapters * ceil(max_rank/8) pages, a zero page and a reserve
+ * of 2 * ceil(max_rank/8) pages (see lora_load_adapter).
  * Scratch for lora_linear is sized by lora_pool_reserve (or grown by the
  * first call with a larger T).
  *
@@ -148,10 +150,14 @@ lora_status lora_pool_reserve(lora_pool_t pool, int max_tokens);
  * Ordering without a device-wide stall (icman.com.cn Multi-LoRA article,
  * section 4.2: a cold adapter load must not hold up the requests already
  * running): the call waits on the host only for its own copy of A and B into
- * pool-owned memory. The pages and the table row are then written on the
- * pool's internal copy stream, after every layer call already enqueued on this
- * pool (on any stream; they keep seeing the old state), and every layer call
- * enqueued on the pool after the return waits for them on the GPU. Other
+ * pool-owned memory and, when the pool has pages that no enqueued layer call
+ * can still read, for writing those pages. (Pages an unload frees become such
+ * once the calls enqueued before it have run; the reserve of lora_pool_create
+ * lets a swap on a full pool find them.) Otherwise the pages are written on
+ * the pool's internal copy stream after every layer call already enqueued on
+ * this pool. The table row always is (on any stream, those calls keep seeing
+ * the old state), and every layer call enqueued on the pool after the return
+ * waits for it on the GPU. Other
  * streams and other pools are not held up (on the GPU, the changes of a pool
  * used on the legacy default stream also follow other streams' earlier work:
  * see lora_pool_check_errors). Calls replayed from a CUDA graph
@@ -477,7 +483,9 @@ lora_status lora_build_segments(lora_pool_t pool, const int32_t *ids, int T, int
 
 /* Pool counters, written to out[0..LORA_STATS_COUNT):
  * loaded slots, free pages, total pages, loads, unloads, linear calls,
- * bytes of device memory held. The counterpart in the pages is the startup
+ * bytes of device memory held. Total pages = max_adapters * ceil(max_rank/8)
+ * (the zero page and the reserve not counted); free pages = total pages minus
+ * the pages loaded adapters hold. The counterpart in the pages is the startup
  * check of icman.com.cn Multi-LoRA article, section 4.1 (confirm from the logs
  * which adapters are loaded); the counters read the host mirror, no GPU work. */
 #define LORA_STATS_COUNT 7
