@@ -113,3 +113,54 @@ def test_unload_then_bad_id_is_reported():
     assert pool.check_errors() == al.LORA_ERR_BAD_ADAPTER_ID
     assert pool.check_errors() == al.LORA_OK        # read and cleared
     pool.close()
+
+
+def test_back_to_back_swaps_on_a_full_pool():
+    """Four unload + reload swaps of one slot of a full pool, each followed by a call,
+    while every call is held back behind a bounded 50 ms kernel on the calls' stream: the
+    first two swaps write the pool's reserve pages at once (no enqueued call can read
+    them); the next two find only pages freed by the earlier swaps, whose calls have not
+    run yet, and must write those on the copy stream after them. Every call sees the
+    adapter generation loaded when it was enqueued (oracle parity on each)."""
+    d, T, seed, slot, n = 256, 64, 83, 2, 4
+    X = L.normal_bf16(seed, L.ROLE_X, 0, (T, d), 1.0)
+    W = L.normal_bf16(seed, L.ROLE_W, 0, (d, d), 1.0 / 16)
+    ads = {i: L.make_adapter(seed, i, d, d, 16, 32.0, std=0.05) for i in range(n)}
+    ids = L.rng_for(seed, L.ROLE_IDS).integers(-1, n, size=T).astype(np.int32)
+    ids[::3] = slot
+    prob = L.Problem("full_pool_swaps", d, d, X, W, ids, ads, n, 16, seed)
+    gens = [ads[slot]] + [L.make_adapter(seed, slot, d, d, 16, 32.0, std=0.05, generation=g)
+                          for g in range(1, 5)]
+
+    pool = load_pool(al, prob)
+    pool.set_path(al.LORA_PATH_DECODE)
+    pool.reserve(T)
+    st = pool.stats()
+    assert st["total_pages"] == 2 * n and st["free_pages"] == 0     # full
+    Xd, Wd, idsd = to_dev(X), to_dev(W), to_dev(ids)
+    main = torch.cuda.Stream()
+    pool.linear(Xd, Wd, idsd, stream=main)            # warm
+    new_AB = [(to_dev(a.A), to_dev(a.B)) for a in gens]
+    torch.cuda.synchronize()
+
+    src = torch.arange(16, dtype=torch.int32, device="cuda")
+    dst = torch.zeros(16, dtype=torch.int32, device="cuda")
+    al.delayed_copy(src, dst, 16, DELAY_US, stream=main)  # holds back every call below
+    Ys = [torch.empty((T, d), dtype=torch.bfloat16, device="cuda") for _ in gens]
+    pool.linear(Xd, Wd, idsd, Ys[0], stream=main)
+    for g in range(1, len(gens)):
+        pool.unload_adapter(slot)
+        pool.load_adapter(slot, new_AB[g][0], new_AB[g][1], 16, 32.0)
+        pool.linear(Xd, Wd, idsd, Ys[g], stream=main)
+    torch.cuda.synchronize()
+
+    assert pool.check_errors() == al.LORA_OK
+    assert torch.equal(dst, src)
+    st = pool.stats()
+    assert st["total_pages"] == 2 * n and st["free_pages"] == 0
+    for g, Y in enumerate(Ys):
+        tup = {s: (a.A, a.B, a.rank, a.alpha) for s, a in ads.items()}
+        tup[slot] = (gens[g].A, gens[g].B, 16, 32.0)
+        ref = oracle.lora_linear(X, W, ids, tup, n)
+        assert_parity(to_host_f64(Y), ref, f"call after swap {g}")
+    pool.close()
